@@ -1,0 +1,421 @@
+"""Benchmark: decode-attention µs per layer-step and KV GB/s on GB300.
+
+A step is one decode token through one attention layer for every sequence of
+the workload: the host plan, the split kernel and the combine kernel, called
+through the library's C ABI. Default workload: 16 query / 4 KV heads,
+head_dim 256, f16 KV cache, f32 q, context 151552 (the Qwen3.5-9B-like
+geometry at its rung nearest 128k; 620.8 MB of K+V per step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-extra]
+
+Timing: W untimed warm-up steps (plus a short soak so the clocks settle);
+then K steps, each bracketed by CUDA events on the launching stream
+(start | split kernel | mid | combine | end); an L2 flush (a write of
+2 x L2 bytes) runs between steps outside the events; barrier + synchronize
+on both sides; max over ranks. `--impl reference` times the double-precision
+CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: (named case, seq_len override)
+    "gqa16x4_f16_L151552": ("gqa_16x4", 151552),
+    "gqa16x4_f16_L262144": ("gqa_16x4", 262144),
+    "gqa16x4_f16_L61440": ("gqa_16x4", 61440),
+    "gqa16x4_f16_L20480": ("gqa_16x4", 20480),
+    "gqa16x4_f16_L4096": ("gqa_16x4", 4096),
+    "gqa8x2_f32_L4096": ("gqa_8x2", None),
+    "gqa24x4_f32_b4": ("gqa_24x4", None),
+    "ragged32_bf16": ("ragged_32", None),
+}
+DEFAULT = "gqa16x4_f16_L151552"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gqa_split_traffic.txt")
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return 6800.0, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "split_kv_decode_gb300", "csrc")
+    for f in sorted(os.listdir(src)):
+        if f.startswith("gqa") or f in ("ptx.cuh", "internal.h"):
+            h.update(open(os.path.join(src, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """Per-launch DRAM bytes of the split kernel from the committed ncu summary,
+    or None if there is none for this workload or the kernel changed since."""
+    try:
+        lines = open(PROFILE_TRAFFIC).read().splitlines()
+    except OSError:
+        return None
+    kv = dict(l.split(":", 1) for l in lines if ":" in l and not l.startswith("#"))
+    kv = {k.strip(): v.strip() for k, v in kv.items()}
+    if kv.get("workload") != workload or kv.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(float(kv["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        mhz = statistics.median(r[0] for r in rows)
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for n, v in zip(names, r[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": mhz, "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def make_inputs(workload, device):
+    from split_kv_decode_gb300 import workloads as W
+    name, L = WORKLOADS[workload]
+    case = W.named(name, seq_len=L) if L else W.named(name)
+    q = case.q.to(device)
+    k = case.k.to(device)
+    v = k if case.shared_kv else case.v.to(device)
+    return case, q, k, v
+
+
+def cpu_baseline(case, budget_s=12.0):
+    """Time the oracle (as it stands) on all host cores over a bounded sample of
+    the workload: whole (b, h) rows, as many as fit in about budget_s seconds,
+    scaled to one full layer-step."""
+    import oracle
+    threads = oracle.max_threads()
+    pairs_all = [(b, h) for b in range(case.batch) for h in range(case.n_heads)]
+    # one row first to size the sample
+    t0 = time.perf_counter()
+    oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
+                     pairs=[pairs_all[0]], threads=1)
+    t_row = time.perf_counter() - t0
+    n = max(1, min(len(pairs_all), int(budget_s / max(t_row, 1e-6) * threads * 0.8)))
+    n = max(threads, n) if n < len(pairs_all) else n
+    n = min(n, len(pairs_all))
+    step = max(1, len(pairs_all) // n)
+    pairs = pairs_all[::step][:n]
+    t0 = time.perf_counter()
+    oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
+                     pairs=pairs, threads=threads)
+    dt = time.perf_counter() - t0
+    # scale by the attended positions of the sample vs the whole step
+    pos_sample = sum(int(case.seq_lens[b]) for b, _ in pairs)
+    pos_all = sum(int(case.seq_lens[b]) for b, _ in pairs_all)
+    us = dt * 1e6 * pos_all / pos_sample
+    return {"value": round(us, 1), "unit": "us/layer-step", "cores": threads, "kind": "oracle",
+            "sample": f"{len(pairs)} of {len(pairs_all)} (b,h) rows at full context, "
+                      f"{dt:.1f} s wall, scaled by attended positions"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed on host cores, rank 0 only."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from split_kv_decode_gb300 import workloads as W  # noqa: F401
+    case, _, _, _ = make_inputs(args.workload, "cpu")
+    import oracle
+    threads = oracle.max_threads()
+    pairs_all = [(b, h) for b in range(case.batch) for h in range(case.n_heads)]
+    # each step: a bounded sample of rows (about 2 s of host work), scaled to a full step
+    t0 = time.perf_counter()
+    oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
+                     pairs=[pairs_all[0]], threads=1)
+    t_row = time.perf_counter() - t0
+    n = max(1, min(len(pairs_all), int(2.0 / max(t_row, 1e-6) * threads)))
+    stride = max(1, len(pairs_all) // n)
+    pairs = pairs_all[::stride][:n]
+    pos_sample = sum(int(case.seq_lens[b]) for b, _ in pairs)
+    pos_all = sum(int(case.seq_lens[b]) for b, _ in pairs_all)
+    for _ in range(args.warmup):
+        oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
+                         pairs=pairs[:1], threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
+                         pairs=pairs, threads=threads)
+        times.append((time.perf_counter() - t0) * pos_all / pos_sample)
+    us = statistics.mean(times) * 1e6
+    line = {
+        "impl": "reference", "metric": "decode-attention us/layer-step", "value": round(us, 1),
+        "unit": "us/layer-step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.workload, case),
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/layer-step", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{len(pairs)} of {len(pairs_all)} (b,h) rows per step, "
+                                   "scaled by attended positions"},
+        "e2e": {"value": round(us, 1), "unit": "us/layer-step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(workload, case):
+    return {"workload": workload, "batch": case.batch, "n_heads": case.n_heads,
+            "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim, "v_dim": case.v_dim,
+            "seq_lens": (case.seq_lens.tolist() if case.batch <= 8 else
+                         f"{case.batch} lengths, sum {int(case.seq_lens.sum())}"),
+            "kv_dtype": case.kv_dtype, "q_dtype": "f32", "out_dtype": case.out_dtype,
+            "kv_bytes_per_step": case.kv_bytes, "parallelism": "replicas",
+            "l2": "flushed between steps (2 x L2 write, outside the events)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the e2e and cpu_baseline measurements")
+    ap.add_argument("--no-soak", action="store_true",
+                    help="skip the clock soak (for profiler runs, which serialise launches)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    from split_kv_decode_gb300 import api as A
+    from split_kv_decode_gb300 import _native as N
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    case, q, k, v = make_inputs(args.workload, dev)
+    out_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[case.out_dtype]
+    stream = torch.cuda.current_stream(dev)
+
+    a_split = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
+                          flags=N.DA_FLAG_NO_COMBINE)
+    plan = A.decode_attn_plan(a_split, case.seq_lens.tolist())
+    ws = torch.empty(A.decode_attn_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+    out = torch.empty(case.batch, case.n_heads, case.v_dim, dtype=out_dt, device=dev)
+    lens = case.seq_lens.tolist()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def step():
+        p = A.decode_attn_plan(a_split, lens)           # host plan (no sync)
+        A.decode_attn_splitk_ex(a_split, p, q, k, v, out, ws, stream)
+        return p
+
+    def combine(p):
+        A.decode_attn_combine(a_split, p, ws, out, stream)
+
+    for _ in range(args.warmup):
+        combine(step())
+    torch.cuda.synchronize()
+    # clocks are sampled from here on: a short untimed soak brings them under
+    # load, then the timed steps run; every sample is taken with the GPU busy
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.time() + (0.0 if args.no_soak else 0.6)
+    while time.time() < t_end:
+        for _ in range(20):
+            combine(step())
+        torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        p = step()
+        ev[i][1].record(stream)
+        combine(p)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    clocks["window"] = "untimed soak (0.6 s) + timed steps"
+    if world > 1:
+        dist.barrier()
+    A.decode_attn_device_status(ws, stream)
+
+    step_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(args.steps)]
+    split_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(args.steps)]
+    total_us = sum(step_us)
+    if world > 1:
+        t = torch.tensor([total_us], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_us = float(t.item())
+    value = total_us / (args.steps * world)                # µs per layer-step, whole job
+    split_mean = statistics.mean(split_us)
+    peak, peak_src = load_peaks()
+    achieved = case.kv_bytes / (split_mean * 1e-6) / 1e9
+    kv_gbs_step = case.kv_bytes / (statistics.mean(step_us) * 1e-6) / 1e9
+
+    line = {
+        "metric": "decode-attention us/layer-step (and KV GB/s)", "value": round(value, 2),
+        "unit": "us/layer-step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value / 1e3, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(args.workload, case),
+        "kv_gbs": round(kv_gbs_step, 1),
+        "hbm_frac_of_8tbs": round(kv_gbs_step / 8000.0, 4),
+        "step_us_median": round(statistics.median(step_us), 2),
+        "split_us_median": round(statistics.median(split_us), 2),
+        "plan": {"grid": plan.grid, "items": plan.n_items, "tile": plan.tile,
+                 "chunk": plan.chunk[0], "n_splits": plan.n_splits[0]},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(args.workload),
+                     "kernel": "gqa_split_kernel", "peak_source": peak_src,
+                     "bytes_per_launch": case.kv_bytes},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if rank == 0 and not args.no_extra:
+        line["e2e"] = measure_e2e(case, q, out_dt, dev, stream, args)
+        line["cpu_baseline"] = cpu_baseline(case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(case, q_dev, out_dt, dev, stream, args):
+    """The same step through the public API with host buffers: per step the
+    inputs (q and the K/V cache) are copied from pinned host memory, the call
+    runs, and the output is copied back; all inside the events."""
+    import torch
+    from split_kv_decode_gb300 import api as A
+    hq = case.q.pin_memory()
+    hk = case.k.pin_memory()
+    hv = hk if case.shared_kv else case.v.pin_memory()
+    hout = torch.empty(case.batch, case.n_heads, case.v_dim, dtype=out_dt).pin_memory()
+    dq = torch.empty_like(hq, device=dev)
+    dk = torch.empty_like(hk, device=dev)
+    dv = dk if case.shared_kv else torch.empty_like(hv, device=dev)
+    dout = torch.empty(hout.shape, dtype=out_dt, device=dev)
+    lens = case.seq_lens.tolist()
+    a = A.make_args(dq, dk, dv, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
+    p = A.decode_attn_plan(a, lens)
+    ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    n = max(3, min(args.steps, 20))
+
+    def once():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        if not case.shared_kv:
+            dv.copy_(hv, non_blocking=True)
+        pp = A.decode_attn_plan(a, lens)
+        A.decode_attn_splitk_ex(a, pp, dq, dk, dv, dout, ws, stream)
+        hout.copy_(dout, non_blocking=True)
+
+    for _ in range(2):
+        once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        once()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    h2d = hq.numel() * hq.element_size() + hk.numel() * hk.element_size() + (
+        0 if case.shared_kv else hv.numel() * hv.element_size())
+    d2h = hout.numel() * hout.element_size()
+    # the cache-resident variant: only q in and out back per step
+    e0.record(stream)
+    for _ in range(n):
+        dq.copy_(hq, non_blocking=True)
+        pp = A.decode_attn_plan(a, lens)
+        A.decode_attn_splitk_ex(a, pp, dq, dk, dv, dout, ws, stream)
+        hout.copy_(dout, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us_res = e0.elapsed_time(e1) * 1e3 / n
+    return {"value": round(us, 1), "unit": "us/layer-step", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n,
+            "cache_resident": {"value": round(us_res, 2), "unit": "us/layer-step",
+                               "h2d_bytes_per_step": hq.numel() * hq.element_size(),
+                               "d2h_bytes_per_step": d2h}}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,200 @@
+/*
+ * split_kv_decode.h -- C ABI of the split-KV decode-attention library
+ * (libsplitkv.so, GB300 / sm_103a).
+ *
+ * The operation: one query token per sequence attends over a long KV cache,
+ *     out[b,h,:] = softmax(q[b,h,:] . K[b,0:L_b,kv,:]^T * scale) . V[b,0:L_b,kv,:]
+ * with kv = h / G, G = n_heads / n_kv_heads (GQA; MQA/MLA when n_kv_heads = 1),
+ * computed split over context ("flash-decoding"): every (sequence, KV head,
+ * split) work item streams one contiguous slice of K/V once for all G query
+ * heads that share it, keeps the online-softmax state (m, l, acc) on chip,
+ * and writes one un-normalised partial per query head; a combine kernel
+ * merges the partials by rescaling with exp(m_i - m).
+ *   - Split over context, contiguous slices, neutral empty slices, per-device
+ *     scratch, launch guard: "Attention at 128k: Split Over Context, Split
+ *     Over Heads" (jared-hpc.com, Part 4 Lecture 06), sections 2 and 5.3.
+ *   - Kernel A / Kernel B pair, raw device pointers plus a storage tag,
+ *     caller-owned partials, split count chosen on the host from L:
+ *     aprender issue 3725 design note, sections 2 and 3.
+ *   - Partial triple and LSE merge; MLA absorbed decode as 96..128 heads
+ *     over one 576-wide latent; plan/run separation: "The Kernel Level:
+ *     Attention and MoE" (llm-serving.xyz lecture 07), sections "Decode
+ *     Starves the SMs" and "A kernel alone is not a serving system".
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *     owned by the caller; the library never frees them.
+ *   - q is float32 [batch][n_heads][head_dim], contiguous.
+ *   - K/V element (b, pos, kv, d) lives at base + b*batch_stride +
+ *     pos*pos_stride + kv*head_stride + d (strides in ELEMENTS). For MLA pass
+ *     the same buffer as k_cache and v_cache with v_dim < head_dim: the
+ *     values are the first v_dim columns of each latent row.
+ *   - out is [batch][n_heads][v_dim], contiguous, of type out_dtype.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). No call below synchronises or allocates, except where its
+ *     comment says so.
+ *   - Every call returns a da_status_t. On failure a thread-local message
+ *     naming the phase ("args", "plan", "split", "combine", ...) is
+ *     available from decode_attn_last_error().
+ */
+#ifndef SPLIT_KV_DECODE_H
+#define SPLIT_KV_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *da_stream_t; /* same type as cudaStream_t */
+
+typedef enum { DA_F32 = 0, DA_F16 = 1, DA_BF16 = 2 } da_dtype_t;
+
+typedef enum {
+    DA_OK = 0,
+    DA_EINVAL = 1,       /* an argument is out of range or inconsistent            */
+    DA_EUNSUPPORTED = 2, /* valid, but no kernel here serves it (reason in message) */
+    DA_ENOSPACE = 3,     /* workspace smaller than decode_attn_workspace_bytes()   */
+    DA_ELAUNCH = 4,      /* a kernel launch failed; the message names the phase    */
+    DA_ETIMEOUT = 5,     /* a bounded in-kernel wait ran out (see device_status)   */
+    DA_ECUDA = 6         /* another CUDA runtime error                             */
+} da_status_t;
+
+#define DA_MAX_BATCH 256
+
+/* da_args_t.flags */
+#define DA_FLAG_NO_COMBINE 0x1   /* decode_attn_splitk_ex runs the split kernel only */
+#define DA_FLAG_TEST_NO_TMA 0x100 /* test hook: the producer issues no copy, so every
+                                     consumer wait runs out after timeout_us and the
+                                     kernel reports DA_ETIMEOUT through device_status */
+
+/* Kernels the planner can choose (da_plan_t.kernel). */
+#define DA_KERNEL_GQA_TMA 1 /* SIMT split kernel, TMA-staged K/V tiles (GQA, MQA) */
+#define DA_KERNEL_MLA_TC 2  /* tcgen05/TMEM split kernel for MLA (576/512 latent)  */
+
+typedef struct {
+    int32_t batch;       /* 1 .. DA_MAX_BATCH                                  */
+    int32_t n_heads;     /* query heads                                        */
+    int32_t n_kv_heads;  /* KV heads; n_heads % n_kv_heads == 0                */
+    int32_t head_dim;    /* q/K width: 128 or 256 (GQA), 576 (MLA)             */
+    int32_t v_dim;       /* V width: == head_dim (GQA), 512 (MLA)              */
+    int32_t capacity;    /* positions allocated per sequence; seq_lens <= it   */
+    int64_t k_batch_stride, k_pos_stride, k_head_stride; /* elements            */
+    int64_t v_batch_stride, v_pos_stride, v_head_stride; /* elements            */
+    int32_t kv_dtype;    /* da_dtype_t of the cache                            */
+    int32_t out_dtype;   /* da_dtype_t of out (DA_F32, DA_F16 or DA_BF16)      */
+    float scale;         /* score scale, usually 1/sqrt(head_dim)              */
+    int32_t force_splits;/* 0: heuristic; n > 0: n splits per sequence (capped
+                            so that no split is empty)                         */
+    int32_t flags;       /* DA_FLAG_*                                          */
+    int32_t timeout_us;  /* bound on every in-kernel wait; 0 = 2 000 000 us    */
+} da_args_t;
+
+/* A host-side plan (plan/run separation): which kernel, how the context is
+ * cut, and how many CTAs run. Pure host data; decode_attn_plan fills it. */
+typedef struct {
+    int32_t kernel;                     /* DA_KERNEL_*                                  */
+    int32_t num_sms;                    /* SMs the plan was made for                    */
+    int32_t ctas_per_sm;                /* resident split CTAs per SM                   */
+    int32_t tile;                       /* positions per staged tile                    */
+    int32_t grid;                       /* split-kernel CTAs (persistent)               */
+    int32_t n_items;                    /* (sequence, KV head, split) work items        */
+    int32_t total_splits;               /* sum over b of n_splits[b]                    */
+    int32_t max_splits;                 /* max over b of n_splits[b]                    */
+    int32_t batch;
+    int32_t seq_lens[DA_MAX_BATCH];     /* copied from the caller                       */
+    int32_t chunk[DA_MAX_BATCH];        /* positions per split of sequence b            */
+    int32_t n_splits[DA_MAX_BATCH];     /* ceil(seq_lens[b] / chunk[b]); none empty     */
+    int32_t split_base[DA_MAX_BATCH];   /* prefix sum of n_splits                       */
+    int64_t workspace_bytes;            /* bytes decode_attn_splitk_ex needs            */
+    int64_t est_cost;                   /* planner's makespan estimate (positions)      */
+} da_plan_t;
+
+/*
+ * decode_attn_plan -- choose the kernel and the split of the context.
+ * Pure host code (Kernel-Level page: "a host-side plan inspects the batch's
+ * length distribution and decides tile partitioning and load balance").
+ * The split count follows aprender issue 3725 §2 (chunk = ceil(L / S),
+ * n_splits = ceil(L / chunk), so no split is ever empty) with the budget taken
+ * on the product (sequences x KV heads x splits), as "Attention at 128k"
+ * §5.1 asks, so that every SM gets equal work.
+ *   args           shapes, strides, dtypes (validated here)
+ *   seq_lens_host  HOST int32[args->batch], each in [1, args->capacity]
+ *   num_sms        SM count to plan for; <= 0 queries the current device
+ *   plan           out
+ * Returns DA_OK, DA_EINVAL, DA_EUNSUPPORTED, or DA_ECUDA (device query).
+ */
+int decode_attn_plan(const da_args_t *args, const int32_t *seq_lens_host, int num_sms,
+                     da_plan_t *plan);
+
+/* Workspace bytes the plan needs (partials + a small status header). */
+int64_t decode_attn_workspace_bytes(const da_plan_t *plan);
+
+/*
+ * decode_attn_splitk_ex -- run the split kernel and (unless
+ * DA_FLAG_NO_COMBINE) the combine kernel on `stream`.
+ * Split kernel: Kernel A of aprender issue 3725 §2 re-designed for sm_103a,
+ * or for MLA the heads-batched kernel of "Attention at 128k" §4 on tensor
+ * cores; partials (m, l, acc) are written per (query head, split), acc left
+ * un-normalised; empty slices are neutral (l = 0, m = -1e30).
+ *   workspace   DEVICE memory, >= plan->workspace_bytes, 256-byte aligned,
+ *               caller-owned (per device; "Attention at 128k" §2 explains why
+ *               one pointer must never serve two devices). Contents need no
+ *               initialisation.
+ * Validation before any launch: DA_EINVAL / DA_EUNSUPPORTED / DA_ENOSPACE.
+ * A failed launch: DA_ELAUNCH, message names the phase ("split"/"combine").
+ * Asynchronous: a timed-out wait inside the kernel is reported later by
+ * decode_attn_device_status().
+ */
+int decode_attn_splitk_ex(const da_args_t *args, const da_plan_t *plan, const float *q,
+                          const void *k_cache, const void *v_cache, void *out,
+                          void *workspace, size_t workspace_bytes, da_stream_t stream);
+
+/*
+ * decode_attn_combine -- merge the partials in `workspace` into out:
+ *   m = max_i m_i, w_i = exp(m_i - m), out = sum_i w_i acc_i / sum_i w_i l_i
+ * ("Attention at 128k" §2; aprender issue 3725 §2, Kernel B). One CTA per
+ * (sequence, query head). Reads what decode_attn_splitk_ex (with
+ * DA_FLAG_NO_COMBINE) left for the same args and plan.
+ */
+int decode_attn_combine(const da_args_t *args, const da_plan_t *plan, const void *workspace,
+                        void *out, da_stream_t stream);
+
+/*
+ * decode_attn_splitk -- the short form: batch 1, f32 q/K/V/out,
+ * v_dim = head_dim, caches laid out [seq_len][n_kv_heads][head_dim]
+ * contiguous, scale given.
+ *   seq_lens  HOST int32[1]: the context length L (>= 1)
+ * Plans on the host and runs split + combine on `stream` using a workspace
+ * the library owns, one per device ("Attention at 128k" §2: per-device
+ * scratch). The first call on a device, and a call that needs a larger
+ * workspace than before, allocates it with cudaMalloc (which synchronises);
+ * decode_attn_release() frees them.
+ */
+int decode_attn_splitk(const float *q, const float *k_cache, const float *v_cache,
+                       const int32_t *seq_lens, int n_heads, int n_kv_heads, int head_dim,
+                       float scale, float *out, da_stream_t stream);
+
+/*
+ * decode_attn_device_status -- synchronise `stream`, then read and clear the
+ * status word at the start of `workspace` that the split kernel sets when a
+ * bounded wait runs out. Returns DA_OK, DA_ETIMEOUT (message names the
+ * kernel), or DA_ECUDA if the synchronisation itself failed.
+ */
+int decode_attn_device_status(void *workspace, da_stream_t stream);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char *decode_attn_last_error(void);
+
+/* Frees the short form's per-device workspaces (synchronises each device). */
+void decode_attn_release(void);
+
+/* Library version string. */
+const char *decode_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLIT_KV_DECODE_H */

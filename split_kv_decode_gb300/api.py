@@ -1,0 +1,162 @@
+"""Python binding of the C ABI, with the same names.
+
+Argument marshalling only: tensors become device pointers and element
+strides, the current torch stream becomes the cudaStream_t, and every
+non-zero status becomes a DecodeAttnError carrying the library's message.
+Every step of the computation runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from . import _native as N
+
+_DT = {torch.float32: N.DA_F32, torch.float16: N.DA_F16, torch.bfloat16: N.DA_BF16}
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{N.STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+def _check(rc: int) -> None:
+    if rc != N.DA_OK:
+        raise DecodeAttnError(rc, decode_attn_last_error())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(handle)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt not in _DT:
+        raise TypeError(f"unsupported dtype {dt}")
+    return _DT[dt]
+
+
+def make_args(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float, *,
+              v_dim: Optional[int] = None, out_dtype: torch.dtype = torch.float32,
+              force_splits: int = 0, flags: int = 0, timeout_us: int = 0) -> N.DaArgs:
+    """Describe q [B, Hq, Dk] and caches [B, cap, Hkv, D] (any element strides)
+    as a da_args_t. For MLA pass the same tensor as both caches and v_dim."""
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, D] and caches [B, cap, Hkv, D]")
+    B, Hq, Dk = q.shape
+    a = N.DaArgs()
+    a.batch, a.n_heads, a.n_kv_heads, a.head_dim = B, Hq, k_cache.shape[2], Dk
+    a.v_dim = int(v_dim) if v_dim is not None else v_cache.shape[3]
+    a.capacity = k_cache.shape[1]
+    ks, vs = k_cache.stride(), v_cache.stride()
+    a.k_batch_stride, a.k_pos_stride, a.k_head_stride = ks[0], ks[1], ks[2]
+    a.v_batch_stride, a.v_pos_stride, a.v_head_stride = vs[0], vs[1], vs[2]
+    if ks[3] != 1 or vs[3] != 1:
+        raise ValueError("the last cache dimension must be contiguous")
+    a.kv_dtype = dtype_code(k_cache.dtype)
+    a.out_dtype = dtype_code(out_dtype)
+    a.scale = float(scale)
+    a.force_splits = int(force_splits)
+    a.flags = int(flags)
+    a.timeout_us = int(timeout_us)
+    return a
+
+
+def decode_attn_plan(args: N.DaArgs, seq_lens_host: Sequence[int], num_sms: int = 0) -> N.DaPlan:
+    lens = (ctypes.c_int32 * max(1, args.batch))(*[int(x) for x in seq_lens_host])
+    plan = N.DaPlan()
+    _check(N.load().decode_attn_plan(ctypes.byref(args), ctypes.cast(lens, ctypes.c_void_p),
+                                     int(num_sms), ctypes.byref(plan)))
+    return plan
+
+
+def decode_attn_workspace_bytes(plan: N.DaPlan) -> int:
+    return int(N.load().decode_attn_workspace_bytes(ctypes.byref(plan)))
+
+
+def new_workspace(plan: N.DaPlan, device=None) -> torch.Tensor:
+    """Caller-owned workspace for one device (torch's allocator aligns to 512 bytes)."""
+    return torch.empty(decode_attn_workspace_bytes(plan), dtype=torch.uint8,
+                       device=device or "cuda")
+
+
+def decode_attn_splitk_ex(args: N.DaArgs, plan: N.DaPlan, q: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                          stream=None) -> None:
+    _check(N.load().decode_attn_splitk_ex(ctypes.byref(args), ctypes.byref(plan), _ptr(q),
+                                          _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream(stream)))
+
+
+def decode_attn_combine(args: N.DaArgs, plan: N.DaPlan, workspace: torch.Tensor,
+                        out: torch.Tensor, stream=None) -> None:
+    _check(N.load().decode_attn_combine(ctypes.byref(args), ctypes.byref(plan), _ptr(workspace),
+                                        _ptr(out), _stream(stream)))
+
+
+def decode_attn_splitk(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                       seq_lens: Sequence[int], n_heads: int, n_kv_heads: int, head_dim: int,
+                       scale: float, out: torch.Tensor, stream=None) -> None:
+    """Short form: batch 1, f32 everything, caches [L, Hkv, D] contiguous."""
+    lens = (ctypes.c_int32 * 1)(int(seq_lens[0]))
+    _check(N.load().decode_attn_splitk(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                       ctypes.cast(lens, ctypes.c_void_p), int(n_heads),
+                                       int(n_kv_heads), int(head_dim), float(scale), _ptr(out),
+                                       _stream(stream)))
+
+
+def decode_attn_device_status(workspace: torch.Tensor, stream=None) -> None:
+    _check(N.load().decode_attn_device_status(_ptr(workspace), _stream(stream)))
+
+
+def decode_attn_last_error() -> str:
+    return N.load().decode_attn_last_error().decode()
+
+
+def decode_attn_release() -> None:
+    N.load().decode_attn_release()
+
+
+def decode_attn_version() -> str:
+    return N.load().decode_attn_version().decode()
+
+
+class DecodeAttention:
+    """Plan once, run many times: holds the args, the plan and a workspace for
+    fixed shapes and lengths (the plan/run split of the Kernel Level page)."""
+
+    def __init__(self, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 seq_lens: Sequence[int], scale: Optional[float] = None, *,
+                 v_dim: Optional[int] = None, out_dtype: torch.dtype = torch.float32,
+                 force_splits: int = 0, flags: int = 0, num_sms: int = 0,
+                 timeout_us: int = 0):
+        sc = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+        self.args = make_args(q, k_cache, v_cache, sc, v_dim=v_dim, out_dtype=out_dtype,
+                              force_splits=force_splits, flags=flags, timeout_us=timeout_us)
+        self.plan = decode_attn_plan(self.args, list(seq_lens), num_sms)
+        self.workspace = torch.empty(decode_attn_workspace_bytes(self.plan), dtype=torch.uint8,
+                                     device=q.device)
+        self.out_dtype = out_dtype
+
+    def new_out(self, device) -> torch.Tensor:
+        a = self.args
+        return torch.empty((a.batch, a.n_heads, a.v_dim), dtype=self.out_dtype, device=device)
+
+    def __call__(self, q, k_cache, v_cache, out=None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = self.new_out(q.device)
+        decode_attn_splitk_ex(self.args, self.plan, q, k_cache, v_cache, out, self.workspace,
+                              stream)
+        return out

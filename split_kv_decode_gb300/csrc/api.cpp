@@ -1,0 +1,494 @@
+// C ABI of libsplitkv.so: argument validation, planning, TMA descriptors,
+// launches with a per-phase launch guard, and the short form's per-device
+// workspace.
+//
+// Launch guard: every launch is followed by cudaGetLastError(), and a failure
+// is reported with the phase that raised it ("Attention at 128k" §5.3: poll
+// per phase so a bad launch is reported where it happened, not at some later
+// collective).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "plan_internal.h"
+
+namespace skv {
+
+bool gqa_config_f32(int D, int G, GqaConfig *cfg);
+bool gqa_config_f16(int D, int G, GqaConfig *cfg);
+bool gqa_config_bf16(int D, int G, GqaConfig *cfg);
+cudaError_t gqa_launch_f32(int D, int G, int grid, cudaStream_t st, const CUtensorMap &km,
+                           const CUtensorMap &vm, const SplitParams &p);
+cudaError_t gqa_launch_f16(int D, int G, int grid, cudaStream_t st, const CUtensorMap &km,
+                           const CUtensorMap &vm, const SplitParams &p);
+cudaError_t gqa_launch_bf16(int D, int G, int grid, cudaStream_t st, const CUtensorMap &km,
+                            const CUtensorMap &vm, const SplitParams &p);
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *phase, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = std::string(phase) + ": " + buf;
+    return code;
+}
+
+int dtype_size(int dt)
+{
+    switch (dt) {
+    case DA_F32: return 4;
+    case DA_F16:
+    case DA_BF16: return 2;
+    default: return 0;
+    }
+}
+
+const char *dtype_name(int dt)
+{
+    switch (dt) {
+    case DA_F32: return "f32";
+    case DA_F16: return "f16";
+    case DA_BF16: return "bf16";
+    default: return "?";
+    }
+}
+
+bool gqa_config_any(int dt, int D, int G, GqaConfig *cfg)
+{
+    switch (dt) {
+    case DA_F32: return gqa_config_f32(D, G, cfg);
+    case DA_F16: return gqa_config_f16(D, G, cfg);
+    case DA_BF16: return gqa_config_bf16(D, G, cfg);
+    default: return false;
+    }
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int check_args(const da_args_t *a)
+{
+    if (!a) return fail(DA_EINVAL, "args", "args is NULL");
+    if (a->batch < 1 || a->batch > DA_MAX_BATCH)
+        return fail(DA_EINVAL, "args", "batch %d outside [1, %d]", a->batch, DA_MAX_BATCH);
+    if (a->n_heads < 1 || a->n_kv_heads < 1)
+        return fail(DA_EINVAL, "args", "n_heads %d / n_kv_heads %d must be >= 1", a->n_heads,
+                    a->n_kv_heads);
+    if (a->n_heads % a->n_kv_heads)
+        return fail(DA_EINVAL, "args", "n_heads %d is not a multiple of n_kv_heads %d",
+                    a->n_heads, a->n_kv_heads);
+    if (a->head_dim < 1 || a->v_dim < 1 || a->v_dim > 1024)
+        return fail(DA_EINVAL, "args", "head_dim %d / v_dim %d out of range", a->head_dim,
+                    a->v_dim);
+    if (a->capacity < 1) return fail(DA_EINVAL, "args", "capacity %d < 1", a->capacity);
+    if (!dtype_size(a->kv_dtype)) return fail(DA_EINVAL, "args", "kv_dtype %d", a->kv_dtype);
+    if (!dtype_size(a->out_dtype)) return fail(DA_EINVAL, "args", "out_dtype %d", a->out_dtype);
+    if (!std::isfinite(a->scale)) return fail(DA_EINVAL, "args", "scale is not finite");
+    if (a->k_pos_stride < 1 || a->k_head_stride < 1 || a->v_pos_stride < 1 ||
+        a->v_head_stride < 1 || a->k_batch_stride < 0 || a->v_batch_stride < 0)
+        return fail(DA_EINVAL, "args", "cache strides must be positive");
+    if (a->batch > 1 && (a->k_batch_stride < 1 || a->v_batch_stride < 1))
+        return fail(DA_EINVAL, "args", "batch strides must be positive when batch > 1");
+    if (a->force_splits < 0) return fail(DA_EINVAL, "args", "force_splits < 0");
+    if (a->timeout_us < 0) return fail(DA_EINVAL, "args", "timeout_us < 0");
+    return DA_OK;
+}
+
+struct KernelChoice {
+    int kernel;
+    int tile;
+    int ctas_per_sm;
+};
+
+int select_kernel(const da_args_t *a, KernelChoice *kc)
+{
+    const int G = a->n_heads / a->n_kv_heads;
+    const int es = dtype_size(a->kv_dtype);
+    if (a->head_dim == 576 && a->v_dim == 512 && a->n_kv_heads == 1)
+        return fail(DA_EUNSUPPORTED, "plan",
+                    "MLA shape (576/512 latent): the tensor-core MLA kernel is not in this build");
+    if (a->head_dim != a->v_dim)
+        return fail(DA_EUNSUPPORTED, "plan", "GQA kernel needs v_dim == head_dim (got %d, %d)",
+                    a->head_dim, a->v_dim);
+    GqaConfig cfg;
+    if (!gqa_config_any(a->kv_dtype, a->head_dim, G, &cfg))
+        return fail(DA_EUNSUPPORTED, "plan",
+                    "no GQA kernel for head_dim %d, group %d, %s KV (head_dim 128 or 256; "
+                    "group 1, 2, 4, 6 or 8)",
+                    a->head_dim, G, dtype_name(a->kv_dtype));
+    const int64_t st[6] = {a->k_pos_stride, a->k_head_stride, a->v_pos_stride,
+                           a->v_head_stride, a->batch > 1 ? a->k_batch_stride : 0,
+                           a->batch > 1 ? a->v_batch_stride : 0};
+    for (int i = 0; i < 6; ++i)
+        if ((st[i] * es) % 16)
+            return fail(DA_EUNSUPPORTED, "plan",
+                        "cache strides must be multiples of 16 bytes for TMA tiles");
+    kc->kernel = DA_KERNEL_GQA_TMA;
+    kc->tile = cfg.tile;
+    kc->ctas_per_sm = cfg.ctas_per_sm;
+    return DA_OK;
+}
+
+// ---- TMA descriptors ----------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+CUtensorMapDataType tma_dtype(int dt)
+{
+    switch (dt) {
+    case DA_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case DA_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    }
+}
+
+// 4-D map over (d, kv head, position, batch) with box (D, 1, rows, 1).
+int encode_cache_map(CUtensorMap *map, const void *base, int dt, int D, int hkv, int cap,
+                     int batch, int64_t head_st, int64_t pos_st, int64_t batch_st, int rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(DA_ECUDA, "tma", "cuTensorMapEncodeTiled is unavailable");
+    const int es = dtype_size(dt);
+    if (batch == 1) batch_st = pos_st * cap;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)cap, (cuuint64_t)batch};
+    cuuint64_t strides[3] = {(cuuint64_t)(head_st * es), (cuuint64_t)(pos_st * es),
+                             (cuuint64_t)(batch_st * es)};
+    cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, tma_dtype(dt), 4, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(DA_EUNSUPPORTED, "tma", "cuTensorMapEncodeTiled rejected the cache layout (%d)",
+                    (int)r);
+    return DA_OK;
+}
+
+int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
+{
+    if (!pl) return fail(DA_EINVAL, "args", "plan is NULL");
+    int rc = select_kernel(a, kc);
+    if (rc) return rc;
+    if (pl->batch != a->batch || pl->kernel != kc->kernel || pl->tile != kc->tile)
+        return fail(DA_EINVAL, "plan", "plan was made for other arguments");
+    int64_t base = 0, items = 0;
+    for (int b = 0; b < a->batch; ++b) {
+        const int L = pl->seq_lens[b];
+        if (L < 1 || L > a->capacity)
+            return fail(DA_EINVAL, "plan", "seq_lens[%d] = %d outside [1, capacity %d]", b, L,
+                        a->capacity);
+        if (pl->chunk[b] < 1 || pl->n_splits[b] != ceil_div(L, pl->chunk[b]) ||
+            pl->split_base[b] != base)
+            return fail(DA_EINVAL, "plan", "inconsistent split table at b = %d", b);
+        base += pl->n_splits[b];
+        items += (int64_t)pl->n_splits[b] * a->n_kv_heads;
+    }
+    if (pl->total_splits != base || pl->n_items != items || pl->grid < 1 || pl->grid > items)
+        return fail(DA_EINVAL, "plan", "inconsistent plan totals");
+    if (pl->workspace_bytes != ws_total(pl->total_splits, a->n_heads, a->v_dim))
+        return fail(DA_EINVAL, "plan", "inconsistent workspace size");
+    return DA_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
+                 const void *v, void *ws, cudaStream_t st)
+{
+    SplitParams p;
+    std::memset(&p, 0, sizeof p);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    p.q = q;
+    p.ml = reinterpret_cast<float2 *>(w + ws_ml_offset());
+    p.acc = reinterpret_cast<float *>(w + ws_acc_offset(pl->total_splits, a->n_heads));
+    p.status = reinterpret_cast<int *>(w);
+    p.n_heads = a->n_heads;
+    p.scale_log2 = a->scale * 1.4426950408889634f;
+    p.timeout_ns = (uint64_t)(a->timeout_us > 0 ? a->timeout_us : 2000000) * 1000ull;
+    p.flags = a->flags;
+    p.items.batch = a->batch;
+    p.items.n_items = pl->n_items;
+    p.items.n_kv_heads = a->n_kv_heads;
+    for (int b = 0; b < a->batch; ++b) {
+        p.items.seq_lens[b] = pl->seq_lens[b];
+        p.items.chunk[b] = pl->chunk[b];
+        p.items.split_base[b] = pl->split_base[b];
+    }
+    p.items.split_base[a->batch] = pl->total_splits;
+
+    CUtensorMap km, vm;
+    int rc = encode_cache_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, a->capacity,
+                              a->batch, a->k_head_stride, a->k_pos_stride, a->k_batch_stride,
+                              pl->tile);
+    if (rc) return rc;
+    rc = encode_cache_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, a->capacity, a->batch,
+                          a->v_head_stride, a->v_pos_stride, a->v_batch_stride, pl->tile);
+    if (rc) return rc;
+
+    const int G = a->n_heads / a->n_kv_heads;
+    cudaError_t e;
+    switch (a->kv_dtype) {
+    case DA_F32: e = gqa_launch_f32(a->head_dim, G, pl->grid, st, km, vm, p); break;
+    case DA_F16: e = gqa_launch_f16(a->head_dim, G, pl->grid, st, km, vm, p); break;
+    default: e = gqa_launch_bf16(a->head_dim, G, pl->grid, st, km, vm, p); break;
+    }
+    if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
+    return DA_OK;
+}
+
+int launch_combine_phase(const da_args_t *a, const da_plan_t *pl, const void *ws, void *out,
+                         cudaStream_t st)
+{
+    CombineParams c;
+    std::memset(&c, 0, sizeof c);
+    const uint8_t *w = static_cast<const uint8_t *>(ws);
+    c.ml = reinterpret_cast<const float2 *>(w + ws_ml_offset());
+    c.acc = reinterpret_cast<const float *>(w + ws_acc_offset(pl->total_splits, a->n_heads));
+    c.out = out;
+    c.n_heads = a->n_heads;
+    c.v_dim = a->v_dim;
+    c.batch = a->batch;
+    for (int b = 0; b < a->batch; ++b) {
+        c.n_splits[b] = pl->n_splits[b];
+        c.split_base[b] = pl->split_base[b];
+    }
+    cudaError_t e = launch_combine(a->out_dtype, a->v_dim, c, a->n_heads, a->batch, st, true);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DA_ELAUNCH, "combine", "%s", cudaGetErrorString(e));
+    return DA_OK;
+}
+
+int check_buffers(const da_args_t *a, const float *q, const void *k, const void *v,
+                  const void *out)
+{
+    if (!q || !k || !v || !out) return fail(DA_EINVAL, "args", "a tensor pointer is NULL");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+        return fail(DA_EINVAL, "args", "q, caches and out must be 16-byte aligned");
+    (void)a;
+    return DA_OK;
+}
+
+// short form: one workspace per device
+std::mutex g_ws_mu;
+std::vector<std::pair<void *, size_t>> g_ws;
+
+} // namespace
+} // namespace skv
+
+using namespace skv;
+
+extern "C" {
+
+int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_plan_t *plan)
+{
+    int rc = check_args(a);
+    if (rc) return rc;
+    if (!lens || !plan) return fail(DA_EINVAL, "args", "seq_lens or plan is NULL");
+    for (int b = 0; b < a->batch; ++b)
+        if (lens[b] < 1 || lens[b] > a->capacity)
+            return fail(DA_EINVAL, "args", "seq_lens[%d] = %d outside [1, capacity %d]", b,
+                        lens[b], a->capacity);
+    KernelChoice kc;
+    rc = select_kernel(a, &kc);
+    if (rc) return rc;
+    if (num_sms <= 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return fail(DA_ECUDA, "plan", "SM count query failed: %s", cudaGetErrorString(e));
+    }
+    PlanOut po;
+    const int slots = num_sms * kc.ctas_per_sm;
+    const int prc = plan_splits(lens, a->batch, a->n_kv_heads, kc.tile, slots, a->force_splits,
+                                1 << 22, &po);
+    if (prc == 1) return fail(DA_EINVAL, "plan", "invalid lengths");
+    if (prc == 2) return fail(DA_EUNSUPPORTED, "plan", "too many work items");
+    std::memset(plan, 0, sizeof *plan);
+    plan->kernel = kc.kernel;
+    plan->num_sms = num_sms;
+    plan->ctas_per_sm = kc.ctas_per_sm;
+    plan->tile = kc.tile;
+    plan->grid = po.grid;
+    plan->n_items = po.n_items;
+    plan->batch = a->batch;
+    int64_t base = 0;
+    int32_t mx = 0;
+    for (int b = 0; b < a->batch; ++b) {
+        plan->seq_lens[b] = lens[b];
+        plan->chunk[b] = po.chunk[b];
+        plan->n_splits[b] = po.n_splits[b];
+        plan->split_base[b] = (int32_t)base;
+        base += po.n_splits[b];
+        if (po.n_splits[b] > mx) mx = po.n_splits[b];
+    }
+    plan->total_splits = (int32_t)base;
+    plan->max_splits = mx;
+    plan->workspace_bytes = ws_total(base, a->n_heads, a->v_dim);
+    plan->est_cost = po.est_cost;
+    return DA_OK;
+}
+
+int64_t decode_attn_workspace_bytes(const da_plan_t *plan)
+{
+    return plan ? plan->workspace_bytes : 0;
+}
+
+int decode_attn_splitk_ex(const da_args_t *a, const da_plan_t *plan, const float *q,
+                          const void *k, const void *v, void *out, void *ws, size_t ws_bytes,
+                          da_stream_t stream)
+{
+    int rc = check_args(a);
+    if (rc) return rc;
+    KernelChoice kc;
+    rc = check_plan(a, plan, &kc);
+    if (rc) return rc;
+    rc = check_buffers(a, q, k, v, out);
+    if (rc) return rc;
+    if (!ws || !aligned(ws, 256))
+        return fail(DA_EINVAL, "args", "workspace must be non-NULL and 256-byte aligned");
+    if ((int64_t)ws_bytes < plan->workspace_bytes)
+        return fail(DA_ENOSPACE, "args", "workspace %zu bytes < %lld needed", ws_bytes,
+                    (long long)plan->workspace_bytes);
+    cudaError_t pre = cudaGetLastError();
+    if (pre != cudaSuccess)
+        return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    rc = launch_split(a, plan, q, k, v, ws, st);
+    if (rc) return rc;
+    if (a->flags & DA_FLAG_NO_COMBINE) return DA_OK;
+    return launch_combine_phase(a, plan, ws, out, st);
+}
+
+int decode_attn_combine(const da_args_t *a, const da_plan_t *plan, const void *ws, void *out,
+                        da_stream_t stream)
+{
+    int rc = check_args(a);
+    if (rc) return rc;
+    KernelChoice kc;
+    rc = check_plan(a, plan, &kc);
+    if (rc) return rc;
+    if (!ws || !aligned(ws, 256)) return fail(DA_EINVAL, "args", "workspace misaligned or NULL");
+    if (!out || !aligned(out, 16)) return fail(DA_EINVAL, "args", "out misaligned or NULL");
+    cudaError_t pre = cudaGetLastError();
+    if (pre != cudaSuccess)
+        return fail(DA_ECUDA, "before combine", "pending CUDA error: %s",
+                    cudaGetErrorString(pre));
+    return launch_combine_phase(a, plan, ws, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int decode_attn_splitk(const float *q, const float *k, const float *v, const int32_t *seq_lens,
+                       int n_heads, int n_kv_heads, int head_dim, float scale, float *out,
+                       da_stream_t stream)
+{
+    if (!seq_lens) return fail(DA_EINVAL, "args", "seq_lens is NULL");
+    if (n_kv_heads < 1 || head_dim < 1)
+        return fail(DA_EINVAL, "args", "n_kv_heads %d / head_dim %d must be >= 1", n_kv_heads,
+                    head_dim);
+    const int L = seq_lens[0];
+    da_args_t a;
+    std::memset(&a, 0, sizeof a);
+    a.batch = 1;
+    a.n_heads = n_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.v_dim = head_dim;
+    a.capacity = L;
+    a.k_pos_stride = a.v_pos_stride = (int64_t)n_kv_heads * head_dim;
+    a.k_head_stride = a.v_head_stride = head_dim;
+    a.k_batch_stride = a.v_batch_stride = (int64_t)L * n_kv_heads * head_dim;
+    a.kv_dtype = DA_F32;
+    a.out_dtype = DA_F32;
+    a.scale = scale;
+    da_plan_t plan;
+    int rc = decode_attn_plan(&a, seq_lens, 0, &plan);
+    if (rc) return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(DA_ECUDA, "workspace", "%s", cudaGetErrorString(e));
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1, {nullptr, 0});
+        auto &slot = g_ws[dev];
+        if (slot.second < (size_t)plan.workspace_bytes) {
+            if (slot.first) cudaFree(slot.first);
+            slot = {nullptr, 0};
+            size_t want = (size_t)plan.workspace_bytes * 2;
+            e = cudaMalloc(&slot.first, want);
+            if (e != cudaSuccess)
+                return fail(DA_ECUDA, "workspace", "cudaMalloc of %zu bytes: %s", want,
+                            cudaGetErrorString(e));
+            slot.second = want;
+        }
+        ws = slot.first;
+    }
+    return decode_attn_splitk_ex(&a, &plan, q, k, v, out, ws, (size_t)plan.workspace_bytes,
+                                 stream);
+}
+
+int decode_attn_device_status(void *ws, da_stream_t stream)
+{
+    if (!ws) return fail(DA_EINVAL, "args", "workspace is NULL");
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(DA_ECUDA, "sync", "%s", cudaGetErrorString(e));
+    int v = 0;
+    e = cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(DA_ECUDA, "status", "%s", cudaGetErrorString(e));
+    if (v == 0) return DA_OK;
+    const int zero = 0;
+    cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    const int code = v & 0xff, kernel = (v >> 8) & 0xff;
+    if (code == DA_ETIMEOUT)
+        return fail(DA_ETIMEOUT, kernel == DA_KERNEL_MLA_TC ? "split (mla)" : "split (gqa)",
+                    "a bounded in-kernel wait ran out");
+    return fail(DA_ECUDA, "status", "unexpected status word 0x%x", v);
+}
+
+const char *decode_attn_last_error(void) { return g_err.c_str(); }
+
+void decode_attn_release(void)
+{
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (size_t d = 0; d < g_ws.size(); ++d)
+        if (g_ws[d].first) {
+            cudaSetDevice((int)d);
+            cudaFree(g_ws[d].first);
+            g_ws[d] = {nullptr, 0};
+        }
+    cudaSetDevice(cur);
+}
+
+const char *decode_attn_version(void) { return "split_kv_decode_gb300 0.1 (sm_103a)"; }
+
+} // extern "C"

@@ -1,0 +1,540 @@
+// GQA / MQA split kernel ("Kernel A"), sm_103a.
+//
+// One persistent CTA per SM walks a static round-robin list of work items.
+// An item is (sequence b, KV head, split s): a contiguous slice
+// [s*chunk, min(L, (s+1)*chunk)) of that KV head's cache, read once for all
+// G query heads of the group ("Attention at 128k: Split Over Context", §2:
+// contiguous slices; aprender issue 3725 design note §2: one block per
+// (KV head, split) serving all G heads).
+//
+// Warp roles:
+//   warp NCW (producer, one lane) streams the slice's K and V tiles of T rows
+//     into an NST-stage shared-memory ring with TMA tensor copies; each stage
+//     has a "full" mbarrier (transaction bytes) and an "empty" mbarrier
+//     (one arrival per consumer warp).
+//   warps 0..NCW-1 (consumers) each own P = T/NCW rows of every tile. A warp
+//     reads a row with 128-bit shared loads spread over its 32 lanes, forms
+//     the G dot products against q (held in registers), and reduces the P*G
+//     partial dots across lanes with a transpose-reduce (each shuffle step
+//     halves the number of live values per lane). Every warp keeps its own
+//     online-softmax state (running max m, per-lane partial sums of l, and
+//     acc[G][D] in registers), following the recurrence of "The Kernel
+//     Level", section "But Softmax Wants the Whole Row".
+// At the end of an item the NCW warp states are merged through shared memory
+// with the same rescaling as the combine (m = max m_w, weights e^{m_w - m}),
+// and one un-normalised partial (m, l, acc[D]) per query head is written.
+//
+// Scores are kept in base-2 units: q is pre-multiplied by scale*log2(e) so
+// that e^{s - m} = 2^{s2 - m2}; the stored m is converted back to natural
+// units. Positions past the slice (or past the sequence) are masked to -inf
+// before the max and skipped in the PV update, so whatever the cache holds
+// there (never-written memory, NaN) cannot leak in.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace skv {
+
+// ---- storage conversion: one chunk of EPC elements (16 or 8 bytes) -----------
+template <typename DT, int EPC> struct Chunk;
+
+template <> struct Chunk<float, 4> {
+    static __device__ __forceinline__ void load(const float *p, float *f)
+    {
+        float4 x = *reinterpret_cast<const float4 *>(p);
+        f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+    }
+};
+
+__device__ __forceinline__ void h2_to_f(uint32_t w, float &a, float &b)
+{
+    __half2 h = *reinterpret_cast<__half2 *>(&w);
+    float2 f = __half22float2(h);
+    a = f.x;
+    b = f.y;
+}
+
+__device__ __forceinline__ void bf2_to_f(uint32_t w, float &a, float &b)
+{
+    a = __uint_as_float(w << 16);
+    b = __uint_as_float(w & 0xffff0000u);
+}
+
+template <> struct Chunk<__half, 8> {
+    static __device__ __forceinline__ void load(const __half *p, float *f)
+    {
+        uint4 x = *reinterpret_cast<const uint4 *>(p);
+        h2_to_f(x.x, f[0], f[1]); h2_to_f(x.y, f[2], f[3]);
+        h2_to_f(x.z, f[4], f[5]); h2_to_f(x.w, f[6], f[7]);
+    }
+};
+template <> struct Chunk<__half, 4> {
+    static __device__ __forceinline__ void load(const __half *p, float *f)
+    {
+        uint2 x = *reinterpret_cast<const uint2 *>(p);
+        h2_to_f(x.x, f[0], f[1]); h2_to_f(x.y, f[2], f[3]);
+    }
+};
+template <> struct Chunk<__nv_bfloat16, 8> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float *f)
+    {
+        uint4 x = *reinterpret_cast<const uint4 *>(p);
+        bf2_to_f(x.x, f[0], f[1]); bf2_to_f(x.y, f[2], f[3]);
+        bf2_to_f(x.z, f[4], f[5]); bf2_to_f(x.w, f[6], f[7]);
+    }
+};
+template <> struct Chunk<__nv_bfloat16, 4> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float *f)
+    {
+        uint2 x = *reinterpret_cast<const uint2 *>(p);
+        bf2_to_f(x.x, f[0], f[1]); bf2_to_f(x.y, f[2], f[3]);
+    }
+};
+
+// ---- transpose-reduce of N per-lane values over the 32 lanes of a warp ------
+// While N is even, each step keeps one half of the values and sends the other
+// half to the partner lane (lane ^ MASK), halving N; once N is odd the
+// remaining steps are plain butterflies. Afterwards a lane holds
+// tr_out<N,16>() totals whose original indices are tr_base(lane) + r.
+template <int N, int MASK> __host__ __device__ constexpr int tr_out()
+{
+    if constexpr (MASK == 0) return N;
+    else if constexpr (N % 2 == 0 && N > 1) return tr_out<N / 2, MASK / 2>();
+    else return tr_out<N, MASK / 2>();
+}
+
+template <int N, int MASK> __device__ __forceinline__ int tr_base(int lane)
+{
+    if constexpr (MASK == 0) return 0;
+    else if constexpr (N % 2 == 0 && N > 1)
+        return ((lane & MASK) ? N / 2 : 0) + tr_base<N / 2, MASK / 2>(lane);
+    else return tr_base<N, MASK / 2>(lane);
+}
+
+// true for exactly one lane among those holding the same totals
+template <int N, int MASK> __device__ __forceinline__ bool tr_writer(int lane)
+{
+    if constexpr (MASK == 0) return true;
+    else if constexpr (N % 2 == 0 && N > 1) return tr_writer<N / 2, MASK / 2>(lane);
+    else return ((lane & MASK) == 0) && tr_writer<N, MASK / 2>(lane);
+}
+
+template <int N, int MASK> __device__ __forceinline__ void tr_reduce(float *v, int lane)
+{
+    if constexpr (MASK > 0) {
+        if constexpr (N % 2 == 0 && N > 1) {
+            const bool up = (lane & MASK) != 0;
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                float send = up ? v[i] : v[i + N / 2];
+                float keep = up ? v[i + N / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
+            }
+            tr_reduce<N / 2, MASK / 2>(v, lane);
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], MASK);
+            tr_reduce<N, MASK / 2>(v, lane);
+        }
+    }
+}
+
+__device__ __forceinline__ bool named_bar_or(int id, int threads, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "setp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, %2, %3, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(id), "r"(threads)
+                 : "memory");
+    return r != 0;
+}
+
+// item -> (b, kv head, split)
+__device__ __forceinline__ void decode_item(const ItemTable &it, int item, int &b, int &kvh,
+                                            int &s)
+{
+    const int t = item / it.n_kv_heads;
+    kvh = item - t * it.n_kv_heads;
+    int lo = 0, hi = it.batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (it.split_base[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    b = lo;
+    s = t - it.split_base[lo];
+}
+
+template <int X> __host__ __device__ constexpr int align_up(int v) { return (v + X - 1) / X * X; }
+
+template <typename DT, int D, int G, int T, int NCW, int NST> struct GqaKernel {
+    static constexpr int ES = sizeof(DT);
+    static constexpr int EPL = D / 32;                       // elements per lane per row
+    static constexpr int CB = (EPL * ES < 16) ? EPL * ES : 16; // bytes per chunk load
+    static constexpr int EPC = CB / ES;                      // elements per chunk
+    static constexpr int NCH = EPL / EPC;                    // chunks per lane per row
+    static constexpr int P = T / NCW;                        // rows per warp per tile
+    static constexpr int NV = P * G;                         // dots per warp per tile
+    static constexpr int R = tr_out<NV, 16>();
+    static constexpr int R2 = (NV + 31) / 32;
+    static constexpr int TILE_BYTES = T * D * ES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int CONSUMERS = NCW * 32;
+    // shared memory layout (offsets from a 1024-byte aligned base)
+    static constexpr int OFF_BAR = NST * STAGE_BYTES;
+    static constexpr int OFF_ABORT = OFF_BAR + 2 * NST * 8;
+    static constexpr int WARP_SCR = align_up<4>(2 * NV + 2 * G); // floats: sc, pscr, mw, aw
+    static constexpr int OFF_WARP = align_up<16>(OFF_ABORT + 16);
+    static constexpr int OFF_ML = align_up<16>(OFF_WARP + NCW * WARP_SCR * 4);
+    static constexpr int OFF_ACC = align_up<16>(OFF_ML + NCW * G * 8);
+    static constexpr int OFF_FIN = align_up<16>(OFF_ACC + G * D * 4);
+    static constexpr int SMEM_USED = OFF_FIN + 2 * G * 4;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;      // slack for the 1024 alignment
+    static_assert(D % 32 == 0 && NCH * EPC == EPL, "row split");
+    static_assert(T % NCW == 0 && NV % 4 == 0, "tile split");
+    static_assert(T <= 256 && D <= 256, "TMA box limits");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(WARP_SCR % 4 == 0 && NV % 4 == 0, "16-byte aligned per-warp scratch");
+    static_assert(TILE_BYTES % 128 == 0, "TMA destination alignment");
+};
+
+template <typename DT, int D, int G, int T, int NCW, int NST>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1)
+    gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap,
+                     const __grid_constant__ SplitParams p)
+{
+    using K = GqaKernel<DT, D, G, T, NCW, NST>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + K::OFF_BAR);
+    uint64_t *empty = full + NST;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::OFF_ABORT);
+    float2 *sm_ml = reinterpret_cast<float2 *>(smem + K::OFF_ML);
+    float *sm_acc = reinterpret_cast<float *>(smem + K::OFF_ACC);
+    float *sm_fin = reinterpret_cast<float *>(smem + K::OFF_FIN);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const ItemTable &it = p.items;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, NCW);
+        }
+        *abort_flag = 0;
+        if (blockIdx.x == 0) *p.status = 0;
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) sm_acc[i] = 0.f;
+    __syncthreads();
+
+    if (warp == NCW) {
+        // ------------------------------- producer -------------------------------
+        if (lane == 0) {
+            tma_prefetch_map(&kmap);
+            tma_prefetch_map(&vmap);
+            const uint64_t pol = l2_evict_first_policy();
+            int last_parity[NST];
+#pragma unroll
+            for (int s = 0; s < NST; ++s) last_parity[s] = -1;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < it.n_items; item += gridDim.x) {
+                int b, kvh, s;
+                decode_item(it, item, b, kvh, s);
+                const int p0 = s * it.chunk[b];
+                const int p1 = min(it.seq_lens[b], p0 + it.chunk[b]);
+                for (int t0 = p0; t0 < p1; t0 += T) {
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!(p.flags & DA_FLAG_TEST_NO_TMA)) {
+                        uint8_t *dst = smem + stage * K::STAGE_BYTES;
+                        mbar_arrive_expect_tx(full + stage, K::STAGE_BYTES);
+                        tma_load_4d(dst, &kmap, full + stage, 0, kvh, t0, b, pol);
+                        tma_load_4d(dst + K::TILE_BYTES, &vmap, full + stage, 0, kvh, t0, b, pol);
+#pragma unroll
+                        for (int x = 0; x < NST; ++x)
+                            if (x == stage) last_parity[x] = (int)phase;
+                    }
+                    if (++stage == NST) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicCAS(p.status, 0, kStatusTimeoutGqa);
+            }
+            // Nothing may be in flight when the CTA exits: wait (bounded) for the
+            // last copy issued into every stage.
+            volatile int never = 0;
+#pragma unroll
+            for (int s = 0; s < NST; ++s)
+                if (last_parity[s] >= 0)
+                    (void)mbar_wait_bounded(full + s, (uint32_t)last_parity[s], p.timeout_ns,
+                                            &never);
+        }
+        return;
+    }
+
+    // --------------------------------- consumers ---------------------------------
+    float *scr = reinterpret_cast<float *>(smem + K::OFF_WARP) + warp * K::WARP_SCR;
+    float *sc = scr;               // [NV] scores (log2 units), masked
+    float *pscr = scr + K::NV;     // [NV] probabilities
+    float *mw = pscr + K::NV;      // [G] running max of this warp
+    float *aw = mw + G;            // [G] last rescale factors
+    const int tbase = tr_base<K::NV, 16>(lane);
+    const bool twriter = tr_writer<K::NV, 16>(lane);
+
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int item = blockIdx.x; item < it.n_items; item += gridDim.x) {
+        int b, kvh, s;
+        decode_item(it, item, b, kvh, s);
+        const int p0 = s * it.chunk[b];
+        const int p1 = min(it.seq_lens[b], p0 + it.chunk[b]);
+
+        // q for the G heads of this group, pre-scaled into log2 units
+        float q[G][K::EPL];
+        const float *qb = p.q + ((size_t)b * p.n_heads + (size_t)kvh * G) * D;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int c = 0; c < K::NCH; ++c)
+#pragma unroll
+                for (int e = 0; e < K::EPC; e += 4) {
+                    float4 x = *reinterpret_cast<const float4 *>(qb + h * D +
+                                                                 (c * 32 + lane) * K::EPC + e);
+                    q[h][c * K::EPC + e + 0] = x.x * p.scale_log2;
+                    q[h][c * K::EPC + e + 1] = x.y * p.scale_log2;
+                    q[h][c * K::EPC + e + 2] = x.z * p.scale_log2;
+                    q[h][c * K::EPC + e + 3] = x.w * p.scale_log2;
+                }
+        float acc[G][K::EPL];
+        float m[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            m[h] = kNeutralM;
+#pragma unroll
+            for (int e = 0; e < K::EPL; ++e) acc[h][e] = 0.f;
+        }
+        float l_lane[K::R2];
+#pragma unroll
+        for (int k = 0; k < K::R2; ++k) l_lane[k] = 0.f;
+        if (lane < G) mw[lane] = kNeutralM;
+        __syncwarp();
+
+        bool aborted = false;
+        for (int t0 = p0; t0 < p1; t0 += T) {
+            if (!mbar_wait_bounded(full + stage, phase, p.timeout_ns, abort_flag)) {
+                aborted = true;
+                break;
+            }
+            const DT *Kt = reinterpret_cast<const DT *>(smem + stage * K::STAGE_BYTES) +
+                           warp * K::P * D;
+            const DT *Vt = reinterpret_cast<const DT *>(smem + stage * K::STAGE_BYTES +
+                                                        K::TILE_BYTES) +
+                           warp * K::P * D;
+            const int valid = min(min(T, p1 - t0) - warp * K::P, K::P);
+            if (valid > 0) {
+                // ---- scores: P rows x G heads, partial over this lane's elements
+                float dv[K::NV];
+#pragma unroll
+                for (int i = 0; i < K::NV; ++i) dv[i] = 0.f;
+#pragma unroll
+                for (int r = 0; r < K::P; ++r)
+#pragma unroll
+                    for (int c = 0; c < K::NCH; ++c) {
+                        float kf[K::EPC];
+                        Chunk<DT, K::EPC>::load(Kt + r * D + (c * 32 + lane) * K::EPC, kf);
+#pragma unroll
+                        for (int h = 0; h < G; ++h)
+#pragma unroll
+                            for (int e = 0; e < K::EPC; ++e)
+                                dv[r * G + h] = fmaf(q[h][c * K::EPC + e], kf[e], dv[r * G + h]);
+                    }
+                tr_reduce<K::NV, 16>(dv, lane);
+#pragma unroll
+                for (int r = 0; r < K::R; ++r) {
+                    const int idx = tbase + r;
+                    const float sv = (idx / G < valid) ? dv[r] : -INFINITY;
+                    if (twriter) sc[idx] = sv;
+                }
+                __syncwarp();
+                // ---- running max per head (every lane computes it redundantly)
+                float tmax[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) tmax[h] = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < K::NV / 4; ++i) {
+                    const float4 x = reinterpret_cast<const float4 *>(sc)[i];
+                    tmax[(4 * i + 0) % G] = fmaxf(tmax[(4 * i + 0) % G], x.x);
+                    tmax[(4 * i + 1) % G] = fmaxf(tmax[(4 * i + 1) % G], x.y);
+                    tmax[(4 * i + 2) % G] = fmaxf(tmax[(4 * i + 2) % G], x.z);
+                    tmax[(4 * i + 3) % G] = fmaxf(tmax[(4 * i + 3) % G], x.w);
+                }
+                bool changed = false;
+#pragma unroll
+                for (int h = 0; h < G; ++h) changed |= tmax[h] > m[h];
+                if (changed) { // warp-uniform: every lane holds the same m and tmax
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float mn = fmaxf(m[h], tmax[h]);
+                        const float alpha = ex2(m[h] - mn);
+                        m[h] = mn;
+#pragma unroll
+                        for (int e = 0; e < K::EPL; ++e) acc[h][e] *= alpha;
+                        if (lane == h) {
+                            mw[h] = mn;
+                            aw[h] = alpha;
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < K::R2; ++k) {
+                        const int idx = lane + 32 * k;
+                        if (idx < K::NV) l_lane[k] *= aw[idx % G];
+                    }
+                }
+                // ---- probabilities, one (row, head) pair per lane
+#pragma unroll
+                for (int k = 0; k < K::R2; ++k) {
+                    const int idx = lane + 32 * k;
+                    if (idx < K::NV) {
+                        const float pv = ex2(sc[idx] - mw[idx % G]);
+                        pscr[idx] = pv;
+                        l_lane[k] += pv;
+                    }
+                }
+                __syncwarp();
+                // ---- acc += p * v over the valid rows
+#pragma unroll
+                for (int r = 0; r < K::P; ++r) {
+                    if (r < valid) {
+                        float pw[G];
+                        if constexpr (G % 4 == 0) {
+#pragma unroll
+                            for (int h = 0; h < G; h += 4) {
+                                const float4 x =
+                                    *reinterpret_cast<const float4 *>(pscr + r * G + h);
+                                pw[h] = x.x; pw[h + 1] = x.y; pw[h + 2] = x.z; pw[h + 3] = x.w;
+                            }
+                        } else if constexpr (G % 2 == 0) {
+#pragma unroll
+                            for (int h = 0; h < G; h += 2) {
+                                const float2 x =
+                                    *reinterpret_cast<const float2 *>(pscr + r * G + h);
+                                pw[h] = x.x; pw[h + 1] = x.y;
+                            }
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < G; ++h) pw[h] = pscr[r * G + h];
+                        }
+#pragma unroll
+                        for (int c = 0; c < K::NCH; ++c) {
+                            float vf[K::EPC];
+                            Chunk<DT, K::EPC>::load(Vt + r * D + (c * 32 + lane) * K::EPC, vf);
+#pragma unroll
+                            for (int h = 0; h < G; ++h)
+#pragma unroll
+                                for (int e = 0; e < K::EPC; ++e)
+                                    acc[h][c * K::EPC + e] =
+                                        fmaf(pw[h], vf[e], acc[h][c * K::EPC + e]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + stage);
+            if (++stage == NST) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (aborted) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0, kStatusTimeoutGqa);
+        }
+        // Barrier A (always taken): the OR makes the abort decision uniform.
+        if (named_bar_or(1, K::CONSUMERS, aborted || *abort_flag)) break;
+
+        // ---- merge the NCW warp states of this item ----
+        // per-warp l per head from the per-lane partial sums
+#pragma unroll
+        for (int k = 0; k < K::R2; ++k) {
+            const int idx = lane + 32 * k;
+            if (idx < K::NV) pscr[idx] = l_lane[k];
+        }
+        __syncwarp();
+        if (lane < G) {
+            float lw = 0.f;
+#pragma unroll
+            for (int r = 0; r < K::P; ++r) lw += pscr[r * G + lane];
+            sm_ml[warp * G + lane] = make_float2(mw[lane], lw);
+        }
+        named_bar_sync(1, K::CONSUMERS); // B
+        {
+            float f[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float M = kNeutralM;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm_ml[w * G + h].x);
+                f[h] = ex2(m[h] - M);
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int c = 0; c < K::NCH; ++c)
+#pragma unroll
+                    for (int e = 0; e < K::EPC; ++e)
+                        atomicAdd(sm_acc + h * D + (c * 32 + lane) * K::EPC + e,
+                                  acc[h][c * K::EPC + e] * f[h]);
+            if (warp == 0 && lane < G) {
+                float M = kNeutralM;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm_ml[w * G + lane].x);
+                float L = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) {
+                    const float2 x = sm_ml[w * G + lane];
+                    L += x.y * ex2(x.x - M);
+                }
+                sm_fin[lane] = M;
+                sm_fin[G + lane] = L;
+            }
+        }
+        named_bar_sync(1, K::CONSUMERS); // C
+        {
+            const size_t slot = (size_t)it.split_base[b] + s;
+            const size_t row0 = slot * p.n_heads + (size_t)kvh * G;
+            float4 *dst = reinterpret_cast<float4 *>(p.acc + row0 * D);
+            float4 *src = reinterpret_cast<float4 *>(sm_acc);
+            for (int i = threadIdx.x; i < G * D / 4; i += K::CONSUMERS) {
+                dst[i] = src[i];
+                src[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (threadIdx.x < G) {
+                const float M = sm_fin[threadIdx.x], L = sm_fin[G + threadIdx.x];
+                p.ml[row0 + threadIdx.x] = make_float2(L > 0.f ? M * kLn2 : kNeutralM, L);
+            }
+        }
+    }
+    if (threadIdx.x == 0) griddep_launch_dependents();
+}
+
+} // namespace skv

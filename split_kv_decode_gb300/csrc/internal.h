@@ -1,0 +1,87 @@
+// Internal declarations shared by the host side of the library (api.cpp,
+// plan.cpp) and the kernel translation units. Not part of the C ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "split_kv_decode.h"
+
+namespace skv {
+
+// Workspace layout (all offsets from the workspace base, bytes):
+//   [0, 256)                status header; int32 status word at offset 0
+//   [256, 256 + ml_bytes)   float2 (m, l) per (slot, query head)
+//   then                    float acc[slot][n_heads][v_dim]
+// A slot is one split of one sequence: slot = split_base[b] + s.
+constexpr int64_t kWsHeader = 256;
+
+inline int64_t ws_ml_offset() { return kWsHeader; }
+inline int64_t ws_acc_offset(int64_t total_splits, int n_heads)
+{
+    int64_t ml = total_splits * n_heads * 8;
+    return kWsHeader + ((ml + 255) / 256) * 256;
+}
+inline int64_t ws_total(int64_t total_splits, int n_heads, int v_dim)
+{
+    return ws_acc_offset(total_splits, n_heads) + total_splits * n_heads * v_dim * 4;
+}
+
+// Status word codes written by kernels (low byte = da_status_t, next byte = kernel).
+constexpr int kStatusTimeoutGqa = DA_ETIMEOUT | (DA_KERNEL_GQA_TMA << 8);
+constexpr int kStatusTimeoutMla = DA_ETIMEOUT | (DA_KERNEL_MLA_TC << 8);
+
+// Per-launch description of the work items shared by the split kernels.
+struct ItemTable {
+    int32_t batch;
+    int32_t n_items;
+    int32_t n_kv_heads;
+    int32_t seq_lens[DA_MAX_BATCH];
+    int32_t chunk[DA_MAX_BATCH];
+    int32_t split_base[DA_MAX_BATCH + 1];
+};
+
+struct SplitParams {
+    const float *q;          // [B][Hq][Dk]
+    float2 *ml;              // workspace (m, l) per (slot, head)
+    float *acc;              // workspace acc per (slot, head, Dv)
+    int *status;             // workspace status word
+    int32_t n_heads;
+    float scale_log2;        // scale * log2(e)
+    uint64_t timeout_ns;
+    int32_t flags;
+    ItemTable items;
+};
+
+struct CombineParams {
+    const float2 *ml;
+    const float *acc;
+    void *out;
+    int32_t n_heads;
+    int32_t v_dim;
+    int32_t batch;
+    int32_t n_splits[DA_MAX_BATCH];
+    int32_t split_base[DA_MAX_BATCH];
+};
+
+// Launchers (return cudaError_t of the launch).
+struct GqaLaunch {
+    int kv_dtype, head_dim, group;      // selects the instantiation
+    int grid;
+    cudaStream_t stream;
+};
+cudaError_t launch_gqa_split(const GqaLaunch &L, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                             const SplitParams &p);
+// Static configuration of a GQA instantiation (tile rows, CTAs per SM, smem).
+struct GqaConfig {
+    int tile;
+    int ctas_per_sm;
+    int smem_bytes;
+    int threads;
+};
+bool gqa_config(int kv_dtype, int head_dim, int group, GqaConfig *cfg);
+
+cudaError_t launch_combine(int out_dtype, int v_dim, const CombineParams &p, int grid_x,
+                           int grid_y, cudaStream_t stream, bool pdl);
+
+} // namespace skv

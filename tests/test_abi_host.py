@@ -1,0 +1,224 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every function include/split_kv_decode.h declares, its structs have the
+C layout, the planner keeps its invariants, and bad arguments are refused
+before anything touches a device."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+from split_kv_decode_gb300 import _native as N
+from split_kv_decode_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "split_kv_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*(decode_attn_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in N.SIGNATURES, f"binding lacks {n}"
+
+
+def test_struct_layout_matches_the_c_compiler():
+    src = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "split_kv_decode.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(da_args_t), sizeof(da_plan_t),
+         offsetof(da_args_t, k_batch_stride), offsetof(da_args_t, scale),
+         offsetof(da_plan_t, seq_lens), offsetof(da_plan_t, workspace_bytes),
+         offsetof(da_plan_t, est_cost));
+  return 0;
+}
+"""
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        open(c, "w").write(src)
+        exe = os.path.join(d, "t")
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                              check=True).stdout.split()]
+    want = [ctypes.sizeof(N.DaArgs), ctypes.sizeof(N.DaPlan), N.DaArgs.k_batch_stride.offset,
+            N.DaArgs.scale.offset, N.DaPlan.seq_lens.offset, N.DaPlan.workspace_bytes.offset,
+            N.DaPlan.est_cost.offset]
+    assert got == want
+
+
+def args(batch=1, hq=16, hkv=4, d=256, dv=None, cap=262144, dt=N.DA_F16, out=N.DA_F32,
+         force=0, layout="pos"):
+    a = N.DaArgs()
+    a.batch, a.n_heads, a.n_kv_heads, a.head_dim = batch, hq, hkv, d
+    a.v_dim = d if dv is None else dv
+    a.capacity = cap
+    if layout == "pos":
+        a.k_pos_stride = a.v_pos_stride = hkv * d
+        a.k_head_stride = a.v_head_stride = d
+    else:
+        a.k_pos_stride = a.v_pos_stride = d
+        a.k_head_stride = a.v_head_stride = cap * d
+    a.k_batch_stride = a.v_batch_stride = cap * hkv * d
+    a.kv_dtype, a.out_dtype = dt, out
+    a.scale = 1.0 / math.sqrt(d)
+    a.force_splits = force
+    return a
+
+
+def plan(lib, a, lens, sms=152):
+    p = N.DaPlan()
+    arr = (ctypes.c_int32 * len(lens))(*lens)
+    rc = lib.decode_attn_plan(ctypes.byref(a), ctypes.cast(arr, ctypes.c_void_p), sms,
+                              ctypes.byref(p))
+    return rc, p
+
+
+def check_invariants(a, p, lens, sms):
+    G = a.n_heads // a.n_kv_heads
+    assert p.batch == a.batch and p.kernel == N.DA_KERNEL_GQA_TMA
+    base = 0
+    for b, L in enumerate(lens):
+        assert p.seq_lens[b] == L
+        assert p.chunk[b] % p.tile == 0 and p.chunk[b] >= p.tile
+        assert p.n_splits[b] == -(-L // p.chunk[b])                 # ceil
+        assert (p.n_splits[b] - 1) * p.chunk[b] < L                  # no empty split
+        assert p.split_base[b] == base
+        base += p.n_splits[b]
+    assert p.total_splits == base
+    assert p.n_items == base * a.n_kv_heads
+    assert 1 <= p.grid <= min(p.n_items, sms * p.ctas_per_sm)
+    assert p.workspace_bytes >= base * a.n_heads * (a.v_dim + 2) * 4
+    assert G * a.n_kv_heads == a.n_heads
+
+
+@pytest.mark.parametrize("L", [1, 5, 33, 37, 64, 65, 4096, 4097, 8192, 12289, 20000, 151552,
+                               262144])
+def test_plan_invariants_single_sequence(lib, L):
+    a = args()
+    rc, p = plan(lib, a, [L])
+    assert rc == 0, N.load().decode_attn_last_error()
+    check_invariants(a, p, [L], 152)
+
+
+def test_plan_fills_every_sm_at_long_context(lib):
+    # 4 KV heads x splits >= 152 CTAs: the split budget is on the product
+    for hkv, hq in ((4, 16), (2, 8), (8, 32), (1, 8)):
+        a = args(hq=hq, hkv=hkv)
+        rc, p = plan(lib, a, [151552])
+        assert rc == 0
+        assert p.grid >= 148                   # tile granularity may leave an SM or two idle
+        # one balanced wave: makespan within 2% of the even share plus one tile
+        even = 151552 * hkv / 152
+        assert p.est_cost <= even * 1.02 + 2 * p.tile
+
+
+def test_plan_budget_follows_heads(lib):
+    # fewer KV heads -> more splits per head (the "Attention at 128k" §5.1 trap)
+    r8, p8 = plan(lib, args(hq=32, hkv=8), [65536])
+    r2, p2 = plan(lib, args(hq=8, hkv=2), [65536])
+    assert r8 == 0 and r2 == 0
+    assert p2.n_splits[0] > p8.n_splits[0]
+    assert p8.grid >= 148 and p2.grid >= 148
+
+
+def test_plan_ragged_batch_is_balanced(lib):
+    lens = [1024 + (i * 40961) % 130000 for i in range(32)]
+    a = args(batch=32, hq=32, hkv=8, d=128, dt=N.DA_BF16, cap=max(lens))
+    rc, p = plan(lib, a, lens)
+    assert rc == 0
+    check_invariants(a, p, lens, 152)
+    even = sum(lens) * 8 / 152
+    assert p.est_cost <= even * 1.10 + 2 * p.tile
+
+
+def test_plan_forced_splits(lib):
+    a = args(force=7)
+    rc, p = plan(lib, a, [4097])
+    assert rc == 0
+    check_invariants(a, p, [4097], 152)
+    assert p.n_splits[0] == 7
+    a = args(force=1000)                      # capped so that no split is empty
+    rc, p = plan(lib, a, [100])
+    assert rc == 0 and p.n_splits[0] == -(-100 // p.tile)
+
+
+def test_plan_small_sms_count(lib):
+    a = args(batch=4, hq=24, hkv=4, dt=N.DA_F32, cap=131072)
+    lens = [8192, 20480, 61440, 131072]
+    for sms in (1, 7, 152):
+        rc, p = plan(lib, a, lens, sms)
+        assert rc == 0
+        check_invariants(a, p, lens, sms)
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a: setattr(a, "n_heads", 15), N.DA_EINVAL),
+    (lambda a: setattr(a, "batch", 0), N.DA_EINVAL),
+    (lambda a: setattr(a, "batch", 257), N.DA_EINVAL),
+    (lambda a: setattr(a, "kv_dtype", 9), N.DA_EINVAL),
+    (lambda a: setattr(a, "scale", float("nan")), N.DA_EINVAL),
+    (lambda a: setattr(a, "k_pos_stride", 0), N.DA_EINVAL),
+    (lambda a: setattr(a, "head_dim", 96) or setattr(a, "v_dim", 96), N.DA_EUNSUPPORTED),
+    (lambda a: setattr(a, "v_dim", 128), N.DA_EUNSUPPORTED),
+    (lambda a: setattr(a, "k_pos_stride", 1028), N.DA_EUNSUPPORTED),   # 2056 B: not 16-aligned
+])
+def test_plan_rejects_bad_arguments(lib, mutate, status):
+    a = args()
+    mutate(a)
+    rc, _ = plan(lib, a, [4096])
+    assert rc == status
+    assert lib.decode_attn_last_error().decode()
+
+
+def test_plan_rejects_bad_lengths(lib):
+    a = args(cap=4096)
+    assert plan(lib, a, [0])[0] == N.DA_EINVAL
+    assert plan(lib, a, [4097])[0] == N.DA_EINVAL
+    assert "seq_lens" in lib.decode_attn_last_error().decode()
+
+
+def test_run_validates_before_launch(lib):
+    a = args(cap=4096)
+    rc, p = plan(lib, a, [4096])
+    assert rc == 0
+    P = ctypes.c_void_p
+    fake = P(1 << 20)                        # never dereferenced: validation fails first
+    rc = lib.decode_attn_splitk_ex(ctypes.byref(a), ctypes.byref(p), None, fake, fake, fake,
+                                   fake, p.workspace_bytes, None)
+    assert rc == N.DA_EINVAL
+    rc = lib.decode_attn_splitk_ex(ctypes.byref(a), ctypes.byref(p), P(1 << 20 | 8), fake, fake,
+                                   fake, fake, p.workspace_bytes, None)
+    assert rc == N.DA_EINVAL                 # misaligned q
+    rc = lib.decode_attn_splitk_ex(ctypes.byref(a), ctypes.byref(p), fake, fake, fake, fake,
+                                   fake, p.workspace_bytes - 1, None)
+    assert rc == N.DA_ENOSPACE
+    p.n_splits[0] += 1                       # a tampered plan is refused
+    rc = lib.decode_attn_splitk_ex(ctypes.byref(a), ctypes.byref(p), fake, fake, fake, fake,
+                                   fake, p.workspace_bytes, None)
+    assert rc == N.DA_EINVAL and "plan" in lib.decode_attn_last_error().decode()
+
+
+def test_version_and_null_handling(lib):
+    assert b"sm_103a" in lib.decode_attn_version()
+    assert lib.decode_attn_plan(None, None, 152, None) == N.DA_EINVAL
+    assert lib.decode_attn_workspace_bytes(None) == 0
+    assert lib.decode_attn_device_status(None, None) == N.DA_EINVAL
