@@ -235,7 +235,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         if (blockIdx.x == 0) *p.status = 0;
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) sm_acc[i] = 0.f;
     __syncthreads();
 
     if (warp == NCW) {
@@ -496,14 +495,31 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                 for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm_ml[w * G + h].x);
                 f[h] = ex2(m[h] - M);
             }
+            // the warps add in a fixed order (warp 0 stores), so the merged
+            // partial does not depend on timing: runs are bit-reproducible
+            for (int w = 0; w < NCW; ++w) {
+                if (warp == w) {
 #pragma unroll
-            for (int h = 0; h < G; ++h)
+                    for (int h = 0; h < G; ++h)
 #pragma unroll
-                for (int c = 0; c < K::NCH; ++c)
+                        for (int c = 0; c < K::NCH; ++c)
 #pragma unroll
-                    for (int e = 0; e < K::EPC; ++e)
-                        atomicAdd(sm_acc + h * D + (c * 32 + lane) * K::EPC + e,
-                                  acc[h][c * K::EPC + e] * f[h]);
+                            for (int e = 0; e < K::EPC; e += 4) {
+                                float4 *dst4 = reinterpret_cast<float4 *>(
+                                    sm_acc + h * D + (c * 32 + lane) * K::EPC + e);
+                                float4 x = make_float4(acc[h][c * K::EPC + e] * f[h],
+                                                       acc[h][c * K::EPC + e + 1] * f[h],
+                                                       acc[h][c * K::EPC + e + 2] * f[h],
+                                                       acc[h][c * K::EPC + e + 3] * f[h]);
+                                if (w > 0) {
+                                    const float4 y = *dst4;
+                                    x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+                                }
+                                *dst4 = x;
+                            }
+                }
+                named_bar_sync(1, K::CONSUMERS);
+            }
             if (warp == 0 && lane < G) {
                 float M = kNeutralM;
 #pragma unroll
@@ -524,10 +540,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             const size_t row0 = slot * p.n_heads + (size_t)kvh * G;
             float4 *dst = reinterpret_cast<float4 *>(p.acc + row0 * D);
             float4 *src = reinterpret_cast<float4 *>(sm_acc);
-            for (int i = threadIdx.x; i < G * D / 4; i += K::CONSUMERS) {
-                dst[i] = src[i];
-                src[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            for (int i = threadIdx.x; i < G * D / 4; i += K::CONSUMERS) dst[i] = src[i];
             if (threadIdx.x < G) {
                 const float M = sm_fin[threadIdx.x], L = sm_fin[G + threadIdx.x];
                 p.ml[row0 + threadIdx.x] = make_float2(L > 0.f ? M * kLn2 : kNeutralM, L);
