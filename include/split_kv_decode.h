@@ -113,8 +113,9 @@ typedef struct {
 
 /*
  * decode_attn_plan -- choose the kernel and the split of the context.
- * Pure host code (Kernel-Level page: "a host-side plan inspects the batch's
- * length distribution and decides tile partitioning and load balance").
+ * Pure host code: the plan step of the plan/run split described in "The
+ * Kernel Level", where the host looks at the lengths of the batch and fixes
+ * how the work is partitioned and balanced before anything runs.
  * The split count follows aprender issue 3725 §2 (chunk = ceil(L / S),
  * n_splits = ceil(L / chunk), so no split is ever empty) with the budget taken
  * on the product (sequences x KV heads x splits), as "Attention at 128k"
@@ -183,6 +184,36 @@ int decode_attn_splitk(const float *q, const float *k_cache, const float *v_cach
  * kernel), or DA_ECUDA if the synchronisation itself failed.
  */
 int decode_attn_device_status(void *workspace, da_stream_t stream);
+
+/*
+ * decode_attn_splitk_noalloc -- decode_attn_splitk_ex for callers that cannot
+ * allocate device memory. The pages have no counterpart to it.
+ *
+ * Some callers cannot call cudaMalloc: code that runs while the device must
+ * not synchronise (cudaMalloc can), hosts whose memory manager owns all device
+ * memory and forbids raw allocations, and plugins that get no allocator handle.
+ * This entry point takes no workspace: the partials live in a file-scope
+ * device array of 16 MiB inside the library, which every GPU that loads the
+ * library keeps until the process exits. It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   - Same arguments and behaviour as decode_attn_splitk_ex minus the
+ *     workspace; the caller still passes q, the caches and out.
+ *   - Returns DA_ENOSPACE, with a message naming the limit, when
+ *     plan->workspace_bytes exceeds 16 MiB (at most 16 MiB / (4 * (v_dim + 2))
+ *     (query head, split) partials).
+ *   - The first call on a device looks the array up once with
+ *     cudaGetSymbolAddress (with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents: calls that overlap on the GPU (other streams, other threads)
+ *     race and corrupt each other's partials. Serialise them.
+ *   - A timed-out in-kernel wait is reported by decode_attn_device_status on a
+ *     workspace pointer only; this entry point's status word is not reachable
+ *     from the host, so use decode_attn_splitk_ex where that matters.
+ */
+int decode_attn_splitk_noalloc(const da_args_t *args, const da_plan_t *plan, const float *q,
+                               const void *k_cache, const void *v_cache, void *out,
+                               da_stream_t stream);
 
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char *decode_attn_last_error(void);

@@ -15,10 +15,10 @@
  *     w_j  = exp(s_j - m),   Z = sum_j w_j
  *     out[b,h,e] = sum_j w_j * V[b,j,kv,e] / Z               e = 0 .. Dv-1
  *
- * i.e. softmax(q K^T * scale) V, the quantity that split-KV decoding reaches
- * "exactly up to floating-point reassociation" (Attention at 128k: Split Over
- * Context, section 2; The Kernel Level: Attention and MoE, "Decode Starves
- * the SMs"). The two-pass stable form follows the float64 two-pass CPU
+ * i.e. softmax(q K^T * scale) V. Split-KV decoding computes this same
+ * quantity; only the order of the floating-point additions changes
+ * (Attention at 128k: Split Over Context, section 2; The Kernel Level:
+ * Attention and MoE, "Decode Starves the SMs"). The two-pass stable form follows the float64 two-pass CPU
  * reference described in section 6 of the first page.
  *
  * A second entry point runs the split-KV method itself in double:

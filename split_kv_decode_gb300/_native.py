@@ -66,6 +66,8 @@ SIGNATURES = {
     "decode_attn_splitk": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_float, _P, _P]),
     "decode_attn_device_status": (ctypes.c_int, [_P, _P]),
+    "decode_attn_splitk_noalloc": (ctypes.c_int, [ctypes.POINTER(DaArgs), ctypes.POINTER(DaPlan),
+                                                  _P, _P, _P, _P, _P]),
     "decode_attn_last_error": (ctypes.c_char_p, []),
     "decode_attn_release": (None, []),
     "decode_attn_version": (ctypes.c_char_p, []),

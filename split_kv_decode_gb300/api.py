@@ -117,6 +117,17 @@ def decode_attn_splitk(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                                        _stream(stream)))
 
 
+def decode_attn_splitk_noalloc(args: N.DaArgs, plan: N.DaPlan, q: torch.Tensor,
+                               k_cache: torch.Tensor, v_cache: torch.Tensor, out: torch.Tensor,
+                               stream=None) -> None:
+    """decode_attn_splitk_ex without a workspace: the partials go to a 16 MiB
+    array inside the library (for callers that cannot allocate). Calls that
+    overlap on the GPU share that array and race."""
+    _check(N.load().decode_attn_splitk_noalloc(ctypes.byref(args), ctypes.byref(plan), _ptr(q),
+                                               _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                               _stream(stream)))
+
+
 def decode_attn_device_status(workspace: torch.Tensor, stream=None) -> None:
     _check(N.load().decode_attn_device_status(_ptr(workspace), _stream(stream)))
 

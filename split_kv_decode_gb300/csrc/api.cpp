@@ -300,6 +300,11 @@ std::mutex g_ws_mu;
 std::vector<std::pair<void *, size_t>> g_ws;
 
 } // namespace
+
+// Lets other translation units of the library report through
+// decode_attn_last_error().
+int set_error(int code, const char *phase, const char *msg) { return fail(code, phase, "%s", msg); }
+
 } // namespace skv
 
 using namespace skv;
