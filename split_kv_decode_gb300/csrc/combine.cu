@@ -4,11 +4,12 @@
 // ("Attention at 128k: Split Over Context", §2; aprender issue 3725 design
 // note §2). A neutral partial (l = 0, m = -1e30) gets weight 0.
 //
-// One CTA per (query head, sequence). Threads are laid out as Dv/4 lanes over
-// the value width (float4 each) times NG groups over the splits; the groups'
-// sums meet in shared memory. Launched with programmatic stream
-// serialization: the CTAs may start while the split kernel drains and wait in
-// griddepcontrol.wait until its partials are visible.
+// One CTA per (query head, sequence, 128 value columns); 8 warps. Each warp
+// loads the acc vectors of its own splits (s = warp, warp + 8, ...) first,
+// then computes m and l over all splits itself (lanes stride the splits, warp
+// shuffles reduce), so the only block-wide step is the final sum of the 8
+// warps' vectors. Launched with programmatic stream serialization: the CTAs
+// may start while the split kernel drains and wait in griddepcontrol.wait.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -18,7 +19,9 @@
 namespace skv {
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineWChunk = 1024; // split weights staged per pass
+constexpr int kCombineWarps = kCombineThreads / 32;
+constexpr int kCombineCols = 128;   // value columns per CTA (one float4 per lane)
+constexpr int kCombinePrefetch = 8; // acc vectors per lane loaded before the weights
 
 template <typename OT> __device__ __forceinline__ void store4(OT *p, float4 v);
 template <> __device__ __forceinline__ void store4<float>(float *p, float4 v)
@@ -42,92 +45,87 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 
     *reinterpret_cast<uint2 *>(p) = u;
 }
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red)
+__device__ __forceinline__ void fma4(float4 &a, float w, const float4 &v)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float x = __shfl_xor_sync(0xffffffffu, v, o);
-        v = is_max ? fmaxf(v, x) : v + x;
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    v = red[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-    return v;
+    a.x = fmaf(w, v.x, a.x);
+    a.y = fmaf(w, v.y, a.y);
+    a.z = fmaf(w, v.z, a.z);
+    a.w = fmaf(w, v.w, a.w);
 }
 
 template <typename OT>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const __grid_constant__ CombineParams p)
 {
-    __shared__ float wts[kCombineWChunk];
-    __shared__ float red[kCombineThreads / 32];
-    __shared__ __align__(16) float part[kCombineThreads * 4];
+    __shared__ __align__(16) float4 part[kCombineWarps][32];
 
     griddep_wait();
 
     const int h = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.n_splits[b];
     const size_t slot0 = (size_t)p.split_base[b];
-    const int nlane = p.v_dim / 4;                  // threads across the value width
-    const int ng = kCombineThreads / nlane;         // groups across the splits
-    const int e4 = threadIdx.x % nlane, g = threadIdx.x / nlane;
+    const int col = blockIdx.z * kCombineCols + lane * 4;
+    const bool live = col < p.v_dim;
+    const float2 *ml = p.ml + slot0 * p.n_heads + h;         // stride n_heads per split
+    const float *acc = p.acc + (slot0 * p.n_heads + h) * p.v_dim + col;
+    const size_t acc_stride = (size_t)p.n_heads * p.v_dim;
 
-    // pass 1: m = max_i m_i
-    float mx = kNeutralM;
-    for (int i = threadIdx.x; i < S; i += blockDim.x)
-        mx = fmaxf(mx, p.ml[(slot0 + i) * p.n_heads + h].x);
-    const float M = block_reduce(mx, true, red);
-
-    // pass 2: weights, the merged l, and the weighted sum of acc
-    float lsum = 0.f;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < S; c0 += kCombineWChunk) {
-        const int cn = min(kCombineWChunk, S - c0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < cn; i += blockDim.x) {
-            const float2 x = p.ml[(slot0 + c0 + i) * p.n_heads + h];
-            const float w = ex2((x.x - M) * kLog2e);
-            wts[i] = w;
-            lsum += w * x.y;
-        }
-        __syncthreads();
-        if (g < ng) {
-            for (int i = g; i < cn; i += ng) {
-                const float w = wts[i];
-                const float4 v = *reinterpret_cast<const float4 *>(
-                    p.acc + ((slot0 + c0 + i) * p.n_heads + h) * p.v_dim + e4 * 4);
-                a.x = fmaf(w, v.x, a.x);
-                a.y = fmaf(w, v.y, a.y);
-                a.z = fmaf(w, v.z, a.z);
-                a.w = fmaf(w, v.w, a.w);
-            }
-        }
+    // acc vectors of this warp's first splits, in flight while m and l are formed
+    float4 pv[kCombinePrefetch];
+#pragma unroll
+    for (int i = 0; i < kCombinePrefetch; ++i) {
+        const int sp = warp + kCombineWarps * i;
+        pv[i] = (live && sp < S)
+                    ? __ldg(reinterpret_cast<const float4 *>(acc + (size_t)sp * acc_stride))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float L = block_reduce(lsum, false, red);
-    reinterpret_cast<float4 *>(part)[threadIdx.x] = a;
+    // m = max_i m_i and l = sum_i e^{m_i - m} l_i, by every warp for itself
+    float M = kNeutralM;
+    for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, __ldg(&ml[(size_t)sp * p.n_heads].x));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int sp = lane; sp < S; sp += 32) {
+        const float2 x = __ldg(&ml[(size_t)sp * p.n_heads]);
+        L = fmaf(x.y, ex2((x.x - M) * kLog2e), L);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kCombinePrefetch; ++i) {
+        const int sp = warp + kCombineWarps * i;
+        if (sp < S) fma4(a, ex2((__ldg(&ml[(size_t)sp * p.n_heads].x) - M) * kLog2e), pv[i]);
+    }
+    for (int sp = warp + kCombineWarps * kCombinePrefetch; sp < S; sp += kCombineWarps) {
+        const float w = ex2((__ldg(&ml[(size_t)sp * p.n_heads].x) - M) * kLog2e);
+        if (live)
+            fma4(a, w, __ldg(reinterpret_cast<const float4 *>(acc + (size_t)sp * acc_stride)));
+    }
+    part[warp][lane] = a;
     __syncthreads();
-    if (threadIdx.x < nlane) {
-        float4 t = reinterpret_cast<float4 *>(part)[threadIdx.x];
-        for (int gg = 1; gg < ng; ++gg) {
-            const float4 u = reinterpret_cast<float4 *>(part)[gg * nlane + threadIdx.x];
+    if (warp == 0 && live) {
+        float4 t = part[0][lane];
+#pragma unroll
+        for (int w = 1; w < kCombineWarps; ++w) {
+            const float4 u = part[w][lane];
             t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
         }
         const float inv = 1.f / L;
         t.x *= inv; t.y *= inv; t.z *= inv; t.w *= inv;
-        OT *out = reinterpret_cast<OT *>(p.out) + ((size_t)b * p.n_heads + h) * p.v_dim;
-        store4<OT>(out + threadIdx.x * 4, t);
+        OT *out = reinterpret_cast<OT *>(p.out) + ((size_t)b * p.n_heads + h) * p.v_dim + col;
+        store4<OT>(out, t);
     }
 }
 
 cudaError_t launch_combine(int out_dtype, int v_dim, const CombineParams &p, int grid_x,
                            int grid_y, cudaStream_t stream, bool pdl)
 {
-    if (v_dim % 4 != 0 || v_dim / 4 > kCombineThreads) return cudaErrorInvalidValue;
+    if (v_dim % 4 != 0) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_x, grid_y, 1);
+    cfg.gridDim = dim3(grid_x, grid_y, (v_dim + kCombineCols - 1) / kCombineCols);
     cfg.blockDim = dim3(kCombineThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -9,21 +9,37 @@ namespace skv {
 constexpr int pow2_floor(int x) { return x < 2 ? 1 : 2 * pow2_floor(x / 2); }
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
-// Tile geometry of one (storage bytes, head_dim, group) instantiation:
-//   * 7 consumer warps and one producer warp (8 warps: two per SM
-//     sub-partition, so the 255-register ceiling applies), one CTA per SM;
-//   * rows per warp per tile P: a power of two, at most a 64 KB stage
-//     (K tile + V tile) and within the register budget below; then as many
-//     stages as fit in 192 KB;
-//   * register budget per consumer lane: q and acc (2*G*EPL floats) plus the
-//     P*G partial dots must stay under 176 floats.
+// Tile geometry of one (storage bytes, head_dim, group) instantiation.
+//
+// The consumers are latency-bound (shuffle and shared-load chains per tile),
+// so more consumer warps per SM help as long as their registers fit:
+//   * preferred: 11 consumer warps + 1 producer (12 warps per SM, 3 per
+//     sub-partition: a 168-register ceiling); used when the estimated
+//     register need 2*G*EPL (q, acc) + P*G (partial dots) + 64 fits with at
+//     least 2 rows per warp and a stage of at most 48 KB;
+//   * otherwise 7 consumer warps + 1 producer (8 warps: 255-register ceiling)
+//     with rows per warp P under a 176-float budget and a stage of at most
+//     64 KB;
+//   * then as many stages (2..6) as fit in 180 KB of shared memory.
+// P (rows per warp per tile) is a power of two.
+constexpr int gqa_reg_est(int P, int G, int EPL) { return 2 * G * EPL + P * G + 64; }
+
 template <int ES, int D, int G> struct GqaGeom {
-    static constexpr int NCW = 7;
     static constexpr int EPL = D / 32;
-    static constexpr int T_STAGE = 32768 / (D * ES);
-    static constexpr int P = pow2_floor(cmin(T_STAGE / NCW, (176 - 2 * G * EPL) / G));
+    static constexpr int P11 = pow2_floor(cmin((168 - 64 - 2 * G * EPL) / G > 0
+                                                   ? (168 - 64 - 2 * G * EPL) / G
+                                                   : 0,
+                                               49152 / (2 * 11 * D * ES)));
+    static constexpr bool WIDE = (168 - 64 - 2 * G * EPL) / G >= 2 && P11 >= 2 &&
+                                 (P11 * G) % 4 == 0;
+    static constexpr int NCW = WIDE ? 11 : 7;
+    static constexpr int P = WIDE ? P11
+                                  : pow2_floor(cmin(65536 / (2 * 7 * D * ES), (176 - 2 * G * EPL) / G));
     static constexpr int T = P * NCW;
-    static constexpr int NST = 196608 / (2 * T * D * ES);
+    static constexpr int STAGE = 2 * T * D * ES;
+    static constexpr int NST = cmin(6, 184320 / STAGE);
+    static_assert(NST >= 2, "at least two stages");
+    static_assert(!WIDE || gqa_reg_est(P, G, EPL) <= 168, "register estimate");
 };
 
 template <typename DT, int D, int G> struct GqaInst {
