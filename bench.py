@@ -40,6 +40,7 @@ WORKLOADS = {
     "gqa8x2_f32_L4096": ("gqa_8x2", None),
     "gqa24x4_f32_b4": ("gqa_24x4", None),
     "ragged32_bf16": ("ragged_32", None),
+    "mla96_f32_L131072": ("mla_96", None),
 }
 DEFAULT = "gqa16x4_f16_L151552"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gqa_split_traffic.txt")

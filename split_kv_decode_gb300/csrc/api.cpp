@@ -6,6 +6,7 @@
 // is reported with the phase that raised it ("Attention at 128k" §5.3: poll
 // per phase so a bad launch is reported where it happened, not at some later
 // collective).
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -106,17 +107,33 @@ int check_args(const da_args_t *a)
 
 struct KernelChoice {
     int kernel;
-    int tile;
+    int tile;        // planner quantum: chunks are multiples of it
     int ctas_per_sm;
+    int cluster;     // CTAs that share one work item
 };
 
 int select_kernel(const da_args_t *a, KernelChoice *kc)
 {
     const int G = a->n_heads / a->n_kv_heads;
     const int es = dtype_size(a->kv_dtype);
-    if (a->head_dim == 576 && a->v_dim == 512 && a->n_kv_heads == 1)
-        return fail(DA_EUNSUPPORTED, "plan",
-                    "MLA shape (576/512 latent): the tensor-core MLA kernel is not in this build");
+    if (a->head_dim == 576 && a->v_dim == 512 && a->n_kv_heads == 1) {
+        if (a->kv_dtype != DA_F32)
+            return fail(DA_EUNSUPPORTED, "plan", "the MLA kernel reads an f32 latent cache");
+        if (!mla_supported_heads(a->n_heads))
+            return fail(DA_EUNSUPPORTED, "plan", "the MLA kernel serves 32, 64 or 96 query heads");
+        if (a->k_pos_stride < 576 || (a->k_pos_stride * 4) % 16 ||
+            (a->batch > 1 && (a->k_batch_stride * 4) % 16))
+            return fail(DA_EUNSUPPORTED, "plan",
+                        "MLA latent rows need >= 576 elements and 16-byte aligned strides");
+        if (a->v_pos_stride != a->k_pos_stride || (a->batch > 1 && a->v_batch_stride != a->k_batch_stride))
+            return fail(DA_EUNSUPPORTED, "plan",
+                        "MLA values must be the first 512 columns of the key rows (same strides)");
+        kc->kernel = DA_KERNEL_MLA_TC;
+        kc->tile = 16;
+        kc->ctas_per_sm = 1;
+        kc->cluster = 2;
+        return DA_OK;
+    }
     if (a->head_dim != a->v_dim)
         return fail(DA_EUNSUPPORTED, "plan", "GQA kernel needs v_dim == head_dim (got %d, %d)",
                     a->head_dim, a->v_dim);
@@ -136,6 +153,7 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
     kc->kernel = DA_KERNEL_GQA_TMA;
     kc->tile = cfg.tile;
     kc->ctas_per_sm = cfg.ctas_per_sm;
+    kc->cluster = 1;
     return DA_OK;
 }
 
@@ -210,7 +228,8 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
         base += pl->n_splits[b];
         items += (int64_t)pl->n_splits[b] * a->n_kv_heads;
     }
-    if (pl->total_splits != base || pl->n_items != items || pl->grid < 1 || pl->grid > items)
+    if (pl->total_splits != base || pl->n_items != items || pl->grid < kc->cluster ||
+        pl->grid > items * kc->cluster || pl->grid % kc->cluster)
         return fail(DA_EINVAL, "plan", "inconsistent plan totals");
     if (pl->workspace_bytes != ws_total(pl->total_splits, a->n_heads, a->v_dim))
         return fail(DA_EINVAL, "plan", "inconsistent workspace size");
@@ -219,9 +238,45 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
+               const void *v, void *ws, cudaStream_t st)
+{
+    if (k != v)
+        return fail(DA_EUNSUPPORTED, "split",
+                    "MLA values must be the first 512 columns of the key rows: pass the same "
+                    "buffer as k_cache and v_cache");
+    MlaParams p;
+    std::memset(&p, 0, sizeof p);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    p.q = q;
+    p.cache = static_cast<const float *>(k);
+    p.pos_stride = a->k_pos_stride;
+    p.batch_stride = a->batch > 1 ? a->k_batch_stride : 0;
+    p.ml = reinterpret_cast<float2 *>(w + ws_ml_offset());
+    p.acc = reinterpret_cast<float *>(w + ws_acc_offset(pl->total_splits, a->n_heads));
+    p.status = reinterpret_cast<int *>(w);
+    p.n_heads = a->n_heads;
+    p.scale_log2 = a->scale * 1.4426950408889634f;
+    p.timeout_ns = (uint64_t)(a->timeout_us > 0 ? a->timeout_us : 2000000) * 1000ull;
+    p.flags = a->flags;
+    p.items.batch = a->batch;
+    p.items.n_items = pl->n_items;
+    p.items.n_kv_heads = 1;
+    for (int b = 0; b < a->batch; ++b) {
+        p.items.seq_lens[b] = pl->seq_lens[b];
+        p.items.chunk[b] = pl->chunk[b];
+        p.items.split_base[b] = pl->split_base[b];
+    }
+    p.items.split_base[a->batch] = pl->total_splits;
+    cudaError_t e = launch_mla_split(pl->grid, st, p);
+    if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
+    return DA_OK;
+}
+
 int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
                  const void *v, void *ws, cudaStream_t st)
 {
+    if (pl->kernel == DA_KERNEL_MLA_TC) return launch_mla(a, pl, q, k, v, ws, st);
     SplitParams p;
     std::memset(&p, 0, sizeof p);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -332,7 +387,7 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
             return fail(DA_ECUDA, "plan", "SM count query failed: %s", cudaGetErrorString(e));
     }
     PlanOut po;
-    const int slots = num_sms * kc.ctas_per_sm;
+    const int slots = std::max(1, num_sms * kc.ctas_per_sm / kc.cluster);
     const int prc = plan_splits(lens, a->batch, a->n_kv_heads, kc.tile, slots, a->force_splits,
                                 1 << 22, &po);
     if (prc == 1) return fail(DA_EINVAL, "plan", "invalid lengths");
@@ -342,7 +397,7 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
     plan->num_sms = num_sms;
     plan->ctas_per_sm = kc.ctas_per_sm;
     plan->tile = kc.tile;
-    plan->grid = po.grid;
+    plan->grid = po.grid * kc.cluster;
     plan->n_items = po.n_items;
     plan->batch = a->batch;
     int64_t base = 0;

@@ -53,6 +53,27 @@ struct SplitParams {
     ItemTable items;
 };
 
+struct MlaParams {
+    const float *q;          // [B][Hq][576]
+    const float *cache;      // latent rows: element (b, pos, d) at b*batch_stride + pos*pos_stride + d
+    int64_t pos_stride;      // elements between positions (>= 576)
+    int64_t batch_stride;    // elements between sequences
+    float2 *ml;              // workspace (m, l) per (slot, head)
+    float *acc;              // workspace acc per (slot, head, 512)
+    int *status;             // workspace status word
+    int32_t n_heads;
+    float scale_log2;        // scale * log2(e)
+    uint64_t timeout_ns;
+    int32_t flags;
+    ItemTable items;         // n_kv_heads = 1
+};
+
+// MLA tensor-core split kernel: heads per CTA = n_heads / 2 (a 2-CTA cluster
+// shares every tile); supported n_heads: 32, 64, 96.
+bool mla_supported_heads(int n_heads);
+int mla_smem_bytes(int n_heads);
+cudaError_t launch_mla_split(int grid, cudaStream_t stream, const MlaParams &p);
+
 struct CombineParams {
     const float2 *ml;
     const float *acc;

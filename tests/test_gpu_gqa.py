@@ -69,14 +69,6 @@ def test_ragged_32_bf16_full_size_sampled():
     check_sampled(W.named("ragged_32"), per_batch=1)
 
 
-def test_mla_shape_is_refused_until_its_kernel_exists():
-    case = W.named("mla_96", seq_len=256)
-    q, k, v = to_device(case)
-    with pytest.raises(A.DecodeAttnError) as e:
-        A.DecodeAttention(q, k, v, case.seq_lens.tolist(), case.scale, v_dim=512)
-    assert e.value.status == N.DA_EUNSUPPORTED
-
-
 # ---------------------------------------------------------------------------
 # boundary lengths and geometries (aprender issue 3725 §4 device tests;
 # "Attention at 128k" §6: 12289 and 20000; gpuflight: odd length 33)

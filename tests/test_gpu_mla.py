@@ -1,0 +1,105 @@
+"""GPU parity of the MLA-as-MQA path (tcgen05 split kernel + combine) against the
+oracle, through the C ABI.
+
+Tolerance. The tensor-core path rounds q (scaled), the latent rows and the
+probabilities to bf16 and accumulates in f32. On the 131072-position workload
+the output averages so many rows that the error is about 1e-5 of max|V|, inside
+the f32 bar (2e-4). With few attended positions the bf16 rounding of a single
+value row (up to 2^-9 of it) shows directly, so short contexts are held to the
+bound that follows from that arithmetic: 5e-3 of max|V| (the bf16 bar).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from split_kv_decode_gb300 import _native as N
+from split_kv_decode_gb300 import api as A
+from split_kv_decode_gb300 import workloads as W
+from tests.gpu_util import errors, oracle_rows, run, sample_pairs, to_device
+
+pytestmark = pytest.mark.gpu
+
+F32_BAR = 2e-4
+BF16_BAR = 5e-3
+
+
+def mla_case(lens, heads=96, seed=2000, cap=None):
+    return W.make_case("mla", batch=len(lens), n_heads=heads, n_kv_heads=1, head_dim=576,
+                       v_dim=512, seq_lens=lens, kv_dtype="f32", scale=1 / math.sqrt(576.0),
+                       seed=seed, std=0.5, shared_kv=True, capacity=cap)
+
+
+def check(case, bar, **kw):
+    got, da = run(case, **kw)
+    assert da.plan.kernel == N.DA_KERNEL_MLA_TC
+    assert np.all(np.isfinite(got))
+    worst, rel = errors(case, got, oracle_rows(case))
+    assert worst <= bar, (worst, rel)
+    return got, da, worst, rel
+
+
+def test_mla_96_heads_L131072_sampled_f32_bar():
+    case = W.named("mla_96")
+    got, da = run(case)
+    assert da.plan.kernel == N.DA_KERNEL_MLA_TC
+    pairs = sample_pairs(case, per_batch=8)
+    worst, rel = errors(case, got, oracle_rows(case, pairs=pairs), pairs)
+    print(f"MLA L=131072: max|err|/max|V| {worst:.2e}, relL2 {rel:.2e}")
+    assert worst <= F32_BAR
+
+
+@pytest.mark.parametrize("L", [4096, 20000])
+def test_mla_96_heads_full_output_f32_bar(L):
+    check(mla_case([L], seed=2001 + L), F32_BAR)
+
+
+@pytest.mark.parametrize("L", [1, 5, 33, 127, 128, 129, 255, 1000])
+def test_mla_short_contexts(L):
+    check(mla_case([L], seed=3000 + L), BF16_BAR)
+
+
+@pytest.mark.parametrize("heads", [32, 64])
+def test_mla_fewer_heads(heads):
+    check(mla_case([3000], heads=heads, seed=4000 + heads), F32_BAR)
+
+
+def test_mla_batch_of_sequences_with_poisoned_tails():
+    case = mla_case([700, 5000, 129], seed=5000, cap=5100)
+    assert torch.isnan(case.k[0, 700:]).all()
+    check(case, BF16_BAR)
+
+
+def test_mla_forced_splits_smaller_than_a_tile():
+    case = mla_case([2500], seed=5100)
+    for s in (1, 7, 40, 157):
+        got, da, worst, rel = check(case, F32_BAR * 5, force_splits=s)
+
+
+def test_mla_poisoned_workspace_and_determinism():
+    case = mla_case([9000], seed=5200)
+    a, _, _, _ = check(case, F32_BAR, poison_ws=True)
+    b, _ = run(case)
+    assert np.array_equal(a, b)
+
+
+def test_mla_needs_the_values_inside_the_key_rows():
+    case = mla_case([300], seed=5300)
+    q, k, _ = to_device(case)
+    v = k.clone()
+    with pytest.raises(A.DecodeAttnError) as e:
+        run(case, dev=(q, k, v))
+    assert e.value.status == N.DA_EUNSUPPORTED
+
+
+def test_mla_timed_out_wait_is_reported_and_the_context_survives():
+    case = mla_case([1000], seed=5400)
+    q, k, v = to_device(case)
+    da = A.DecodeAttention(q, k, v, [1000], case.scale, v_dim=512,
+                           flags=N.DA_FLAG_TEST_NO_TMA, timeout_us=2000)
+    da(q, k, v)
+    with pytest.raises(A.DecodeAttnError) as e:
+        A.decode_attn_device_status(da.workspace)
+    assert e.value.status == N.DA_ETIMEOUT and "mla" in e.value.message
+    check(case, BF16_BAR)
