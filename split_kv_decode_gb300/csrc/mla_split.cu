@@ -4,40 +4,50 @@
 // one shared 576-wide latent row per position (512 latent + 64 rope columns),
 // and the values are the first 512 columns of the same rows ("Attention at
 // 128k", §1.1 and §4; "The Kernel Level", absorbed MLA decode). With 96 heads
-// against one shared latent the per-tile work is a real dense contraction:
-//     S^T[pos][h] = sum_d K[pos][d] * Q[h][d]        (M = 128 positions, K = 576)
-//     O^T[e][h]  += sum_pos V[pos][e] * P[pos][h]     (M = 512 in 4 blocks of 128)
-// so both products run on the tensor cores (bf16 operands, f32 accumulation
-// in TMEM), and each latent byte is read from HBM once for all heads.
+// against one shared latent, every tile is a real dense contraction:
+//     S[h][pos]  = sum_d Q[h][d] * K[pos][d]          (M = heads, N = 64 positions, K = 576)
+//     O^T[e][h] += sum_pos V[pos][e] * P[h][pos]      (M = 512 in 4 blocks of 128, N = heads)
+// Both products run on the tensor cores (bf16 operands, f32 accumulation in
+// TMEM), and each latent byte is read from HBM once for all heads.
 //
 // Work split: a cluster of two CTAs (on two SMs) takes a work item, a
 // contiguous slice of one sequence's context (split over context, "Attention at
-// 128k" §2). Both CTAs walk the slice in tiles of 128 positions. CTA r:
-//   * converts rows [64r, 64r + 64) of every tile from f32 to bf16 into its own
-//     shared memory and ships them to the peer CTA with a bulk shared-memory copy,
-//     so the tile is read from HBM once and converted once;
+// 128k" §2), and walks it in tiles of 64 positions. CTA r:
+//   * converts rows [32r, 32r + 32) of every tile from f32 to bf16 into its own
+//     shared memory and ships them to the peer CTA with bulk shared-memory
+//     copies, so every row is read from HBM once and converted once;
 //   * owns query heads [r*N, r*N + N), N = n_heads / 2: their bf16 Q (scale and
-//     log2 e folded in), their S^T and O^T in its TMEM, their partials.
-// Roles inside a CTA (9 warps: three per SM sub-partition at most, so a
-// thread may hold up to 168 registers):
-//   warps 0-3  softmax and epilogue: thread p owns TMEM lane p (tile position p);
-//   warps 4-7  converters (f32 -> bf16 with 128-bit loads, 3 chunks in flight),
-//              16 rows (two swizzle atoms) of the CTA's half-tile each;
-//   warp 8     TMEM allocation and the single thread that issues the MMAs.
-// The tile buffer is 9 chunks of [128 positions][64 columns] bf16 in the
-// 128-byte-swizzled K-major layout: each chunk is an A operand of the QK
-// product (positions x 64 columns of K) and, read MN-major, half an M block of
-// the PV product (64 value columns x positions). A chunk is freed (for the next
-// tile) as soon as both CTAs' MMAs are done with it, so conversion of tile t+1
-// overlaps the softmax and PV of tile t.
+//     log2 e folded in), S and O^T in its TMEM, and their partials.
+// The tile buffer is double-buffered (two slots of nine 64-column chunks,
+// 128-byte-swizzled, K-major), so the converters fill tile t+1 while the
+// tensor core and the softmax work on tile t. A chunk is the B operand of the
+// QK product (64 positions x 64 columns) and, read MN-major, half an M block
+// of the PV product (64 value columns x 64 positions).
 //
-// Softmax in the transposed layout: a head's scores lie across the 128 lanes,
-// so the exact per-tile max would need a cross-lane reduction per head. The
-// running reference max m of each head is instead kept lazily: it is set from
-// the first tile of an item and only moved (with the rescale of l and of the
-// head's O^T column) when a score exceeds it by more than 2^8. Any reference
-// value gives the same partial after normalisation; bounding the exponent keeps
-// every 2^(s - m) <= 256, so nothing overflows.
+// Roles (14 warps):
+//   warps 0-3   softmax and epilogue. S uses the 64-row TMEM layout, in which
+//               head h sits in lane 32*(h/16) + h%16; so thread (w, l < 16) owns
+//               head 16w + l: its 64 scores, running max m and sum l stay in
+//               registers, and its probability row is one 128-byte row of P.
+//               All 128 threads (one per TMEM lane) read O^T in the epilogue.
+//   warps 4-11  converters: 4 rows each, 8 chunks of 128-bit loads in flight.
+//               They only store and arrive on a barrier: no proxy fence, so
+//               their loads stay in flight across tiles.
+//   warp 12     TMEM allocation and the one thread that issues the MMAs; it
+//               issues QK(t) before PV(t-1), so QK overlaps the softmax.
+//   warp 13     publisher: once the converters have stored a tile half, it
+//               makes the stores visible to the async proxy (one fence per
+//               tile, on the synchronisation path from the stores to the
+//               tensor core and to the bulk copies), ships the half to the peer
+//               CTA as nine 4 KB bulk copies and releases the tile to the MMA.
+// Q has N real rows; the 64-row MMA reads 64 rows from each Q chunk, so rows
+// N..63 alias the next chunk (or slack). Those rows give S rows that no thread
+// reads.
+//
+// The running max is moved lazily: a head's reference m changes only when a
+// tile holds a score above m + 8 (log2 units), so P <= 2^8 and l, O^T cannot
+// overflow, and O^T (whose column h spans all lanes) is rescaled only then.
+// Any reference gives the same partial after normalisation.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -48,49 +58,43 @@ namespace {
 
 constexpr int kDk = 576;
 constexpr int kDv = 512;
-constexpr int kTile = 128;               // positions per tile = MMA M
-constexpr int kChunks = 9;               // 64-column chunks of a latent row (8 value + rope)
-constexpr int kChunkBytes = kTile * 128; // 16 KB
+constexpr int kTile = 64;                         // positions per tile = QK N
+constexpr int kChunks = 9;                        // 64-column chunks of a latent row
+constexpr int kChunkBytes = kTile * 128;          // 8 KB
+constexpr int kSlotBytes = kChunks * kChunkBytes; // 72 KB
 constexpr int kSoftWarps = 4;
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = 8;
+constexpr int kRowsPerConv = 32 / kConvWarps;     // rows of the half-tile per converter warp
 constexpr int kMmaWarp = kSoftWarps + kConvWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
-constexpr int kPF = 3;                   // converter chunks in flight
-constexpr float kTau = 8.f;              // lazy-rescale threshold (log2 units)
-constexpr int kRope = 8;                 // index of the rope chunk
-
-// chunk processed at step ci of a tile: the rope chunk first (it is freed as
-// soon as QK is done), then the value chunks in order
-__device__ __forceinline__ int chunk_at(int ci) { return ci == 0 ? kRope : ci - 1; }
-
-__host__ __device__ constexpr int tmem_cols_for(int N)
-{
-    return 5 * N <= 32 ? 32 : 5 * N <= 64 ? 64 : 5 * N <= 128 ? 128 : 5 * N <= 256 ? 256 : 512;
-}
+constexpr int kPubWarp = kMmaWarp + 1;
+constexpr int kThreads = (kPubWarp + 1) * 32;
+constexpr int kPF = 8;                            // converter chunks in flight
+constexpr float kTau = 8.f;                       // lazy-rescale threshold (log2 units)
+constexpr int kPeerTx = kChunks * kConvWarps * kRowsPerConv * 128; // bytes the peer ships per tile
 
 template <int N> struct Layout {
-    static constexpr int KV = 0;                            // 9 x 16 KB tile chunks
-    static constexpr int QCH = N * 128;                     // bytes of one Q chunk
-    static constexpr int Q = KV + kChunks * kChunkBytes;    // 9 Q chunks
-    static constexpr int PT = Q + kChunks * QCH;            // P^T: 2 sub-chunks of 64 positions
+    static constexpr int TILE = 0;                          // 2 slots x 72 KB
+    static constexpr int QCH = N * 128;                     // one Q chunk (N rows)
+    static constexpr int Q = TILE + 2 * kSlotBytes;
+    static constexpr int QEND = Q + kChunks * QCH + (kTile * 128 - QCH); // 64-row reads stay inside
+    static constexpr int PT = (QEND + 1023) / 1024 * 1024;  // P: 2 slots of N rows x 128 B
     static constexpr int BAR = PT + 2 * QCH;
-    static constexpr int NBAR = 27;
+    static constexpr int NBAR = 20;
     static constexpr int MISC = BAR + NBAR * 8;             // tmem base, abort flag
-    static constexpr int MREF = (MISC + 16 + 15) / 16 * 16; // float m_ref[N]
-    static constexpr int SCR = MREF + N * 4;                // float scratch[4][N]
-    static constexpr int USED = SCR + kSoftWarps * N * 4;
+    static constexpr int ALPHA = (MISC + 16 + 15) / 16 * 16; // float alpha[N]
+    static constexpr int USED = ALPHA + N * 4;
     static constexpr int ALLOC = USED + 1024;
-    static constexpr int TMEM_COLS = tmem_cols_for(N);
-    static constexpr int S_COL = 0;
-    static constexpr int O_COL = N;                         // O^T block j at O_COL + j*N
+    static constexpr int O_COL = 128;                       // O^T block j at O_COL + j*N
+    static constexpr int TMEM_COLS = O_COL + 4 * N <= 256 ? 256 : 512;
     static_assert(N % 16 == 0 && N >= 16 && N <= 48, "heads per CTA");
     static_assert(QCH % 1024 == 0 && Q % 1024 == 0 && PT % 1024 == 0, "swizzle atoms");
     static_assert(ALLOC <= 232448, "shared memory");
 };
 
-// barrier indices
-constexpr int B_FULL = 0, B_EMPTY = 9, B_SFULL = 18, B_SFREE = 19, B_PFULL = 20, B_PFREE = 21,
-              B_OREADY = 22, B_OFREE = 23, B_DRAIN = 24, B_QFULL = 25, B_QFREE = 26;
+// barrier indices (slot-indexed ones take +slot)
+constexpr int B_FULL = 0, B_EMPTY = 2, B_SFULL = 4, B_SFREE = 6, B_PFULL = 8, B_PFREE = 10,
+              B_PVDONE = 12, B_OREADY = 13, B_OFREE = 14, B_QFULL = 15, B_QFREE = 16,
+              B_DRAIN = 17, B_CONV = 18; // B_CONV + slot: local converters have stored their rows
 
 // byte offset of (row, byte) in a region of 128-byte rows with 128-byte swizzle
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t byte)
@@ -138,23 +142,25 @@ __device__ __forceinline__ Item get_item(const ItemTable &it, int item)
     return x;
 }
 
-// Sequence of (item, tile, chunk) units one converter walks through.
+// The (item, tile, chunk) units of a cluster's work, in order; gt counts tiles.
 struct Cursor {
-    int item, t, ci;
+    int item, t, c, gt;
     Item x;
     bool done;
     __device__ __forceinline__ void start(const ItemTable &it, int first)
     {
         item = first;
         t = 0;
-        ci = 0;
+        c = 0;
+        gt = 0;
         done = item >= it.n_items;
         if (!done) x = get_item(it, item);
     }
     __device__ __forceinline__ void next(const ItemTable &it, int stride)
     {
-        if (++ci == kChunks) {
-            ci = 0;
+        if (++c == kChunks) {
+            c = 0;
+            ++gt;
             if (++t == x.ntiles) {
                 t = 0;
                 item += stride;
@@ -162,6 +168,11 @@ struct Cursor {
                 if (!done) x = get_item(it, item);
             }
         }
+    }
+    __device__ __forceinline__ void next_tile(const ItemTable &it, int stride)
+    {
+        c = kChunks - 1;
+        next(it, stride);
     }
 };
 
@@ -186,8 +197,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + LY::BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + LY::MISC + 4);
-    float *m_ref = reinterpret_cast<float *>(sm + LY::MREF);
-    float *scr = reinterpret_cast<float *>(sm + LY::SCR);
+    float *alpha_sm = reinterpret_cast<float *>(sm + LY::ALPHA);
     const uint32_t sm_base = smem_u32(sm);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -199,19 +209,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     volatile int never = 0;
 
     if (threadIdx.x == 0) {
-        for (int c = 0; c < kChunks; ++c) {
-            mbar_init(bar + B_FULL + c, kConvWarps);
-            mbar_init(bar + B_EMPTY + c, 2);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar + B_FULL + s, 1);
+            mbar_init(bar + B_CONV + s, kConvWarps);
+            mbar_init(bar + B_EMPTY + s, 2);
+            mbar_init(bar + B_SFULL + s, 1);
+            mbar_init(bar + B_SFREE + s, kSoftWarps);
+            mbar_init(bar + B_PFULL + s, kSoftWarps);
+            mbar_init(bar + B_PFREE + s, 1);
         }
-        mbar_init(bar + B_SFULL, 1);
-        mbar_init(bar + B_SFREE, kSoftWarps);
-        mbar_init(bar + B_PFULL, kSoftWarps);
-        mbar_init(bar + B_PFREE, 1);
+        mbar_init(bar + B_PVDONE, 1);
         mbar_init(bar + B_OREADY, 1);
         mbar_init(bar + B_OFREE, kSoftWarps);
-        mbar_init(bar + B_DRAIN, 1);
         mbar_init(bar + B_QFULL, kConvWarps);
         mbar_init(bar + B_QFREE, 1);
+        mbar_init(bar + B_DRAIN, 1);
         *abort_flag = 0;
         if (blockIdx.x == 0) *p.status = 0;
         fence_mbar_init();
@@ -226,30 +238,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp >= kSoftWarps && warp < kMmaWarp) {
         // =============================== converters ===============================
         const int cw = warp - kSoftWarps;
-        const uint32_t row0 = rank * 64 + cw * 16; // this warp's 16 rows of every tile
-        uint32_t eph = 0;                         // per-chunk empty parity bits
-        uint32_t qph = 0;                         // q_free parity
+        const uint32_t row0 = rank * 32 + cw * kRowsPerConv; // this warp's rows of every tile
+        const int trow = lane >> 3, q8 = lane & 7;            // this lane's row and 8 columns
+        uint32_t eph = 0, qph = 0;
         bool ok = true;
-        const bool no_copy = (p.flags & DA_FLAG_TEST_NO_TMA) != 0;
-        float4 ld[kPF][4][2];
+        float4 ld[kPF][2];
         Cursor ahead, cur;
         ahead.start(it, cluster);
         cur.start(it, cluster);
-        auto issue = [&](const Cursor &u, float4 (&r)[4][2]) {
-            const int c = chunk_at(u.ci);
-            const float *base = p.cache + (size_t)u.x.b * p.batch_stride;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int task = lane + 32 * k, row = task >> 3, q8 = task & 7;
-                const int pos = u.x.p0 + u.t * kTile + (int)row0 + row;
-                if (pos < u.x.p1) {
-                    const float4 *src = reinterpret_cast<const float4 *>(
-                        base + (size_t)pos * p.pos_stride + c * 64 + q8 * 8);
-                    r[k][0] = __ldg(src);
-                    r[k][1] = __ldg(src + 1);
-                } else {
-                    r[k][0] = r[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+        auto issue = [&](const Cursor &u, float4 (&r)[2]) {
+            const int pos = u.x.p0 + u.t * kTile + (int)row0 + trow;
+            if (pos < u.x.p1) {
+                // lane q8 takes floats [4*q8, 4*q8 + 4) and [32 + 4*q8, 36 + 4*q8) of the
+                // chunk: each load instruction reads whole 128-byte halves of 4 rows
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    p.cache + (size_t)u.x.b * p.batch_stride + (size_t)pos * p.pos_stride +
+                    u.c * 64 + q8 * 4);
+                r[0] = __ldg(src);
+                r[1] = __ldg(src + 8);
+            } else {
+                r[0] = r[1] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         };
 #pragma unroll
@@ -266,149 +274,156 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     issue(ahead, ld[(u + kPF - 1) % kPF]);
                     ahead.next(it, nclusters);
                 }
-                if (cur.t == 0 && cur.ci == 0) {
-                    // a new item: this CTA's heads of q (scale and log2 e folded in),
-                    // once the previous item's QK products are done with Q
-                    if (!mbar_wait_bounded(bar + B_QFREE, qph ^ 1u, p.timeout_ns, abort_flag)) {
+                const int slot = cur.gt & 1;
+                if (cur.c == 0) {
+                    if (cur.t == 0) {
+                        // a new item: this CTA's heads of q (scale and log2 e folded
+                        // in), once the previous item's QK products are done with Q
+                        if (!mbar_wait_bounded(bar + B_QFREE, qph ^ 1u, p.timeout_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        qph ^= 1u;
+                        const float *qb = p.q + ((size_t)cur.x.b * p.n_heads + hbase) * kDk;
+                        for (int task = cw * 32 + lane; task < N * 72; task += kConvWarps * 32) {
+                            const int h = task / 72, g = task % 72, c = g >> 3, j = g & 7;
+                            const float4 a = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + g * 8));
+                            const float4 b = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + g * 8 + 4));
+                            const float sc = p.scale_log2;
+                            uint4 v;
+                            v.x = pack_bf16(a.x * sc, a.y * sc);
+                            v.y = pack_bf16(a.z * sc, a.w * sc);
+                            v.z = pack_bf16(b.x * sc, b.y * sc);
+                            v.w = pack_bf16(b.z * sc, b.w * sc);
+                            sts_v4(sm_base + LY::Q + c * LY::QCH + sw128(h, j * 16), v.x, v.y, v.z, v.w);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar + B_QFULL);
+                    }
+                    // the slot is free once both CTAs' MMAs are done with its last tile
+                    if (!mbar_wait_bounded(bar + B_EMPTY + slot, ((eph >> slot) & 1u) ^ 1u,
+                                           p.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    qph ^= 1u;
-                    const float *qb = p.q + ((size_t)cur.x.b * p.n_heads + hbase) * kDk;
-                    for (int task = cw * 32 + lane; task < N * 72; task += kConvWarps * 32) {
-                        const int h = task / 72, q8 = task % 72, c = q8 >> 3, j = q8 & 7;
-                        const float4 a = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + q8 * 8));
-                        const float4 b = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + q8 * 8 + 4));
-                        const float sc = p.scale_log2;
-                        uint4 v;
-                        v.x = pack_bf16(a.x * sc, a.y * sc);
-                        v.y = pack_bf16(a.z * sc, a.w * sc);
-                        v.z = pack_bf16(b.x * sc, b.y * sc);
-                        v.w = pack_bf16(b.z * sc, b.w * sc);
-                        *reinterpret_cast<uint4 *>(sm + LY::Q + c * LY::QCH + sw128(h, j * 16)) = v;
-                    }
-                    fence_proxy_async_smem();
+                    eph ^= 1u << slot;
+                }
+                uint4 pk;
+                pk.x = pack_bf16(ld[u][0].x, ld[u][0].y);
+                pk.y = pack_bf16(ld[u][0].z, ld[u][0].w);
+                pk.z = pack_bf16(ld[u][1].x, ld[u][1].y);
+                pk.w = pack_bf16(ld[u][1].z, ld[u][1].w);
+                // (under DA_FLAG_TEST_NO_TMA the publisher ships nothing; the
+                // converters run unchanged: a flag test here slows the loop)
+                const uint32_t chunk = sm_base + LY::TILE + slot * kSlotBytes + cur.c * kChunkBytes;
+                sts_v2(chunk + sw128(row0 + trow, q8 * 8), pk.x, pk.y);
+                sts_v2(chunk + sw128(row0 + trow, 64 + q8 * 8), pk.z, pk.w);
+                if (cur.c == kChunks - 1) {
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar + B_QFULL);
-                }
-                const int c = chunk_at(cur.ci);
-                uint4 pk[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 a = ld[u][k][0], b = ld[u][k][1];
-                    pk[k].x = pack_bf16(a.x, a.y);
-                    pk[k].y = pack_bf16(a.z, a.w);
-                    pk[k].z = pack_bf16(b.x, b.y);
-                    pk[k].w = pack_bf16(b.z, b.w);
-                }
-                if (!mbar_wait_bounded(bar + B_EMPTY + c, ((eph >> c) & 1u) ^ 1u, p.timeout_ns,
-                                       abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                eph ^= 1u << c;
-                if (!no_copy) {
-                    uint8_t *chunk = sm + LY::KV + c * kChunkBytes;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int task = lane + 32 * k, row = task >> 3, q8 = task & 7;
-                        *reinterpret_cast<uint4 *>(chunk + sw128(row0 + row, q8 * 16)) = pk[k];
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const uint32_t src = sm_base + LY::KV + c * kChunkBytes + row0 * 128;
-                        bulk_copy_to_cta(map_to_rank(src, peer), src, 2048,
-                                         map_to_rank(smem_u32(bar + B_FULL + c), peer));
-                        if (cw == 0) mbar_arrive_expect_tx(bar + B_FULL + c, 8 * 1024);
-                        else mbar_arrive(bar + B_FULL + c);
-                    }
+                    if (lane == 0) mbar_arrive(bar + B_CONV + slot);
                 }
                 cur.next(it, nclusters);
             }
         }
         if (!ok) raise_abort(abort_flag, abort_peer, p.status);
-        // every commit (local and the peer's) that targets this CTA's empty
-        // barriers has landed once each chunk has been released once more
+        // every commit (local and the peer's) aimed at this CTA's empty barriers
+        // has landed once each slot has been released once more
         const uint64_t lim = *abort_flag ? 1000000ull : p.timeout_ns;
-        for (int c = 0; c < kChunks; ++c)
-            (void)mbar_wait_bounded(bar + B_EMPTY + c, ((eph >> c) & 1u) ^ 1u, lim, &never);
+        for (int s = 0; s < 2; ++s)
+            (void)mbar_wait_bounded(bar + B_EMPTY + s, ((eph >> s) & 1u) ^ 1u, lim, &never);
     } else if (warp == kMmaWarp) {
         // ============================ MMA issue (1 thread) ============================
         if (lane == 0) {
-            constexpr uint32_t IDESC_QK = idesc_bf16_f32(kTile, N, 0, 0);
-            constexpr uint32_t IDESC_PV = idesc_bf16_f32(kTile, N, 1, 0);
+            constexpr uint32_t IDESC_QK = idesc_bf16_f32(64, kTile, 0, 0);
+            constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, N, 1, 0);
             uint32_t fph = 0, sph = 0, pph = 0, oph = 0, qph = 0;
-            bool ok = true, first_item = true;
-            for (int item = cluster; ok && item < it.n_items; item += nclusters) {
-                const Item x = get_item(it, item);
-                if (!mbar_wait_bounded(bar + B_QFULL, qph, p.timeout_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                qph ^= 1u;
-                for (int t = 0; ok && t < x.ntiles; ++t) {
-                    // S^T = K_tile . Q^T (wait until the softmax has read the previous S^T)
-                    if (!mbar_wait_bounded(bar + B_SFREE, sph ^ 1u, p.timeout_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    sph ^= 1u;
-                    for (int ci = 0; ci < kChunks; ++ci) {
-                        const int c = chunk_at(ci);
-                        if (!mbar_wait_bounded(bar + B_FULL + c, (fph >> c) & 1u, p.timeout_ns,
-                                               abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        fph ^= 1u << c;
+            bool ok = true, q_ready = false;
+            // Two cursors over this cluster's tiles: the next QK product and the
+            // next PV product (never ahead of the QK cursor). Each turn issues
+            // whichever is ready, so PV(t) goes out as soon as P(t) is written
+            // and QK(t+1) as soon as the tile is in, in either order.
+            Cursor qk, pv;
+            qk.start(it, cluster);
+            pv.start(it, cluster);
+            int items_pv = 0;
+            uint64_t last = global_ns();
+            while (!pv.done) {
+                bool progress = false;
+                if (pv.gt < qk.gt) {
+                    // O^T += V^T . P^T once P is written (and, at an item's first
+                    // tile, once the previous item's epilogue has read O^T)
+                    const int slot = pv.gt & 1;
+                    const bool first = pv.t == 0;
+                    if (mbar_test(bar + B_PFULL + slot, (pph >> slot) & 1u) &&
+                        (!first || items_pv == 0 || mbar_test(bar + B_OFREE, oph))) {
+                        pph ^= 1u << slot;
+                        if (first && items_pv > 0) oph ^= 1u;
+                        if (first) ++items_pv;
                         tc_fence_after();
-                        const uint32_t a0 = sm_base + LY::KV + c * kChunkBytes;
-                        const uint32_t b0 = sm_base + LY::Q + c * LY::QCH;
+                        const uint64_t vd = smem_desc_sw128(sm_base + LY::TILE + slot * kSlotBytes,
+                                                            kChunkBytes, 1024);
+                        const uint64_t pd =
+                            smem_desc_sw128(sm_base + LY::PT + slot * LY::QCH, 16, 1024);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc_mma_bf16(tmem + LY::S_COL, smem_desc_sw128(a0 + k * 32, 16, 1024),
-                                        smem_desc_sw128(b0 + k * 32, 16, 1024), IDESC_QK,
-                                        (ci | k) != 0);
-                        if (c == kRope) tc_commit_mc(bar + B_EMPTY + kRope, 3);
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc_mma_bf16(tmem + LY::O_COL + j * N,
+                                            vd + (uint64_t)((2 * j * kChunkBytes + k * 2048) >> 4),
+                                            pd + (uint64_t)((k * 32) >> 4), IDESC_PV,
+                                            (first && k == 0) ? 0u : 1u);
+                        tc_commit_mc(bar + B_EMPTY + slot, 3);
+                        tc_commit(bar + B_PFREE + slot);
+                        tc_commit(bar + B_PVDONE);
+                        if (pv.t == pv.x.ntiles - 1) tc_commit(bar + B_OREADY);
+                        progress = true;
+                        pv.next_tile(it, nclusters);
                     }
-                    if (!ok) break;
-                    tc_commit(bar + B_SFULL);
-                    if (t == x.ntiles - 1) tc_commit(bar + B_QFREE);
-                    // O^T += V^T . P^T once the softmax has written P^T
-                    if (!mbar_wait_bounded(bar + B_PFULL, pph, p.timeout_ns, abort_flag)) {
+                }
+                if (!qk.done) {
+                    // S = Q . K_tile^T once Q of the item is in, the tile is full
+                    // and the softmax has released this S slot
+                    const int slot = qk.gt & 1;
+                    if (!q_ready && mbar_test(bar + B_QFULL, qph)) {
+                        qph ^= 1u;
+                        q_ready = true;
+                    }
+                    if (q_ready && mbar_test(bar + B_FULL + slot, (fph >> slot) & 1u) &&
+                        mbar_test(bar + B_SFREE + slot, ((sph >> slot) & 1u) ^ 1u)) {
+                        fph ^= 1u << slot;
+                        sph ^= 1u << slot;
+                        tc_fence_after();
+                        // descriptors advance by adding (byte offset >> 4) to the start field
+                        const uint64_t qd = smem_desc_sw128(sm_base + LY::Q, 16, 1024);
+                        const uint64_t kd =
+                            smem_desc_sw128(sm_base + LY::TILE + slot * kSlotBytes, 16, 1024);
+#pragma unroll
+                        for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc_mma_bf16(tmem + slot * kTile,
+                                            qd + (uint64_t)((c * LY::QCH + k * 32) >> 4),
+                                            kd + (uint64_t)((c * kChunkBytes + k * 32) >> 4),
+                                            IDESC_QK, (c | k) != 0);
+                        tc_commit(bar + B_SFULL + slot);
+                        if (qk.t == qk.x.ntiles - 1) {
+                            tc_commit(bar + B_QFREE);
+                            q_ready = false;
+                        }
+                        progress = true;
+                        qk.next_tile(it, nclusters);
+                    }
+                }
+                if (progress) {
+                    last = global_ns();
+                } else {
+                    if (*abort_flag || global_ns() - last > p.timeout_ns) {
                         ok = false;
                         break;
                     }
-                    pph ^= 1u;
-                    if (t == 0 && !first_item) {
-                        // the epilogue of the previous item has read O^T
-                        if (!mbar_wait_bounded(bar + B_OFREE, oph, p.timeout_ns, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        oph ^= 1u;
-                    }
-                    tc_fence_after();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t a0 = sm_base + LY::KV + (2 * j) * kChunkBytes;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const uint32_t bk = sm_base + LY::PT + (k >> 2) * LY::QCH + (k & 3) * 32;
-                            tc_mma_bf16(tmem + LY::O_COL + j * N,
-                                        smem_desc_sw128(a0 + k * 2048, kChunkBytes, 1024),
-                                        smem_desc_sw128(bk, 16, 1024), IDESC_PV,
-                                        (t > 0 || k > 0) ? 1u : 0u);
-                        }
-                        tc_commit_mc(bar + B_EMPTY + 2 * j, 3);
-                        tc_commit_mc(bar + B_EMPTY + 2 * j + 1, 3);
-                    }
-                    tc_commit(bar + B_PFREE);
+                    __nanosleep(32);
                 }
-                if (!ok) break;
-                tc_commit(bar + B_OREADY);
-                first_item = false;
             }
             if (!ok) raise_abort(abort_flag, abort_peer, p.status);
             // no MMA may be in flight when TMEM is freed
@@ -416,119 +431,139 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             (void)mbar_wait_bounded(bar + B_DRAIN, 0, p.timeout_ns, &never);
         }
         __syncwarp();
+    } else if (warp == kPubWarp) {
+        // ======================= publisher (1 thread per CTA) =======================
+        if (lane == 0 && !(p.flags & DA_FLAG_TEST_NO_TMA)) {
+            uint32_t cph = 0;
+            bool ok = true;
+            int gt = 0;
+            for (int item = cluster; ok && item < it.n_items; item += nclusters) {
+                const Item x = get_item(it, item);
+                for (int t = 0; t < x.ntiles; ++t, ++gt) {
+                    const int slot = gt & 1;
+                    if (!mbar_wait_bounded(bar + B_CONV + slot, (cph >> slot) & 1u, p.timeout_ns,
+                                           abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    cph ^= 1u << slot;
+                    // the converters' stores, acquired through B_CONV, become visible to
+                    // the async proxy (the bulk copies here, the MMAs after B_FULL)
+                    fence_proxy_async_smem();
+                    const uint32_t half = LY::TILE + slot * kSlotBytes + rank * 32 * 128;
+                    const uint32_t peer_full = map_to_rank(smem_u32(bar + B_FULL + slot), peer);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        const uint32_t src = sm_base + half + c * kChunkBytes;
+                        bulk_copy_to_cta(map_to_rank(src, peer), src, 32 * 128, peer_full);
+                    }
+                    mbar_arrive_expect_tx(bar + B_FULL + slot, kPeerTx);
+                }
+            }
+            if (!ok) raise_abort(abort_flag, abort_peer, p.status);
+        }
+        __syncwarp();
     } else {
         // ========================= softmax and epilogue (warps 0-3) ========================
-        const int tid = threadIdx.x; // 0..127 = TMEM lane = tile position
+        const int tid = threadIdx.x;            // TMEM lane of the epilogue rows
+        const int h = 16 * warp + lane;         // head of this lane in the 64-row S layout
+        const bool owner = lane < 16 && h < N;
         const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-        uint32_t sph = 0, pph = 0, oph = 0;
-        for (int item = cluster; item < it.n_items; item += nclusters) {
+        uint32_t sph = 0, ppf = 0, oph = 0;
+        int gt = 0;
+        bool ab = false;
+        for (int item = cluster; !ab && item < it.n_items; item += nclusters) {
             const Item x = get_item(it, item);
-            float l[N];
-#pragma unroll
-            for (int h = 0; h < N; ++h) l[h] = 0.f;
-            if (tid < N) m_ref[tid] = -INFINITY;
-            named_bar_sync(2, 128);
-            bool ab = false;
-            for (int t = 0; t < x.ntiles; ++t) {
-                bool okw = mbar_wait_bounded(bar + B_SFULL, sph, p.timeout_ns, abort_flag);
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < x.ntiles; ++t, ++gt) {
+                const int slot = gt & 1;
+                bool okw = mbar_wait_bounded(bar + B_SFULL + slot, (sph >> slot) & 1u,
+                                             p.timeout_ns, abort_flag);
                 if (bar_or(2, 128, !okw)) {
                     ab = true;
                     break;
                 }
-                sph ^= 1u;
+                sph ^= 1u << slot;
                 tc_fence_after();
-                const int pos = x.p0 + t * kTile + tid;
-                const bool valid = pos < x.p1;
-                // pass 1: does any score outgrow its head's reference max?
-                bool ex = false;
+                const int nvalid = min(kTile, x.p1 - (x.p0 + t * kTile));
+                const uint32_t scol = tl + slot * kTile;
+                // the tile max of this thread's head over the valid positions
+                float tm = -INFINITY;
 #pragma unroll
-                for (int g = 0; g < N / 16; ++g) {
+                for (int g = 0; g < 4; ++g) {
                     float sg[16];
-                    tmem_ld16(tl + LY::S_COL + 16 * g, sg);
+                    tmem_ld16(scol + 16 * g, sg);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) ex |= valid && sg[i] > m_ref[16 * g + i] + kTau;
+                    for (int i = 0; i < 16; ++i)
+                        if (16 * g + i < nvalid) tm = fmaxf(tm, sg[i]);
                 }
-                okw = mbar_wait_bounded(bar + B_PFREE, pph ^ 1u, p.timeout_ns, abort_flag);
-                if (bar_or(2, 128, !okw)) {
-                    ab = true;
-                    break;
-                }
-                pph ^= 1u;
+                const bool ex = owner && tm > m + kTau;
                 if (bar_or(2, 128, ex)) {
-                    // move the reference max of the heads that outgrew it
-#pragma unroll
-                    for (int g = 0; g < N / 16; ++g) {
-                        float sg[16];
-                        tmem_ld16(tl + LY::S_COL + 16 * g, sg);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float v = valid ? sg[i] : -INFINITY;
-#pragma unroll
-                            for (int o = 16; o > 0; o >>= 1)
-                                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                            if (lane == 0) scr[warp * N + 16 * g + i] = v;
+                    // move the reference of the heads that outgrew it; rescale l and O^T
+                    const float mn = ex ? tm : m;
+                    const float alpha = (mn == m) ? 1.f : (m == -INFINITY ? 0.f : ex2(m - mn));
+                    if (owner) alpha_sm[h] = alpha;
+                    l *= alpha;
+                    m = mn;
+                    if (t > 0) {
+                        // PV(t-1) is done with O^T before it is rescaled
+                        okw = mbar_wait_bounded(bar + B_PVDONE, (uint32_t)(gt - 1) & 1u,
+                                                p.timeout_ns, abort_flag);
+                        named_bar_sync(2, 128);
+                        if (bar_or(2, 128, !okw)) {
+                            ab = true;
+                            break;
                         }
-                    }
-                    named_bar_sync(2, 128);
+                        tc_fence_after();
 #pragma unroll
-                    for (int g = 0; g < N / 16; ++g) {
-                        float alpha[16];
+                        for (int j = 0; j < 4; ++j)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int h = 16 * g + i;
-                            const float tm = fmaxf(fmaxf(scr[h], scr[N + h]),
-                                                   fmaxf(scr[2 * N + h], scr[3 * N + h]));
-                            const float mo = m_ref[h];
-                            const float mn = tm > mo + kTau ? tm : mo;
-                            alpha[i] = (mn == mo) ? 1.f : (mo == -INFINITY ? 0.f : ex2(mo - mn));
-                            l[h] *= alpha[i];
-                        }
-                        if (t > 0) {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
+                            for (int g = 0; g < N / 16; ++g) {
                                 float o[16];
                                 tmem_ld16(tl + LY::O_COL + j * N + 16 * g, o);
                                 tmem_wait_ld();
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) o[i] *= alpha[i];
+                                for (int i = 0; i < 16; ++i) o[i] *= alpha_sm[16 * g + i];
                                 tmem_st16(tl + LY::O_COL + j * N + 16 * g, o);
                             }
-                            tmem_wait_st();
-                        }
+                        tmem_wait_st();
                     }
-                    named_bar_sync(2, 128); // every thread has used the old m_ref
-                    if (tid < N) {
-                        const float tm = fmaxf(fmaxf(scr[tid], scr[N + tid]),
-                                               fmaxf(scr[2 * N + tid], scr[3 * N + tid]));
-                        if (tm > m_ref[tid] + kTau) m_ref[tid] = tm;
-                    }
-                    named_bar_sync(2, 128);
+                    named_bar_sync(2, 128); // alpha_sm is read before it is rewritten
                 }
-                // pass 2: P^T[h][pos] = 2^(s - m_ref) in bf16, K-major (positions contiguous)
-                uint8_t *pt = sm + LY::PT + (tid >> 6) * LY::QCH;
-                const uint32_t pb = (uint32_t)(tid & 63) * 2;
+                // P row of this head: 2^(s - m) in bf16, once PV(t-2) is done with the slot
+                okw = mbar_wait_bounded(bar + B_PFREE + slot, ((ppf >> slot) & 1u) ^ 1u,
+                                        p.timeout_ns, abort_flag);
+                if (bar_or(2, 128, !okw)) {
+                    ab = true;
+                    break;
+                }
+                ppf ^= 1u << slot;
+                const uint32_t prow = sm_base + LY::PT + slot * LY::QCH;
 #pragma unroll
-                for (int g = 0; g < N / 16; ++g) {
+                for (int g = 0; g < 4; ++g) {
                     float sg[16];
-                    tmem_ld16(tl + LY::S_COL + 16 * g, sg);
+                    tmem_ld16(scol + 16 * g, sg);
                     tmem_wait_ld();
+                    if (owner) {
+                        uint32_t w[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int h = 16 * g + i;
-                        const float pv = valid ? ex2(sg[i] - m_ref[h]) : 0.f;
-                        l[h] += pv;
-                        *reinterpret_cast<__nv_bfloat16 *>(pt + sw128(h, pb)) =
-                            __float2bfloat16_rn(pv);
+                        for (int i = 0; i < 16; i += 2) {
+                            const float p0 = (16 * g + i < nvalid) ? ex2(sg[i] - m) : 0.f;
+                            const float p1 = (16 * g + i + 1 < nvalid) ? ex2(sg[i + 1] - m) : 0.f;
+                            l += p0 + p1;
+                            w[i >> 1] = pack_bf16(p0, p1);
+                        }
+                        sts_v4(prow + sw128(h, 32 * g), w[0], w[1], w[2], w[3]);
+                        sts_v4(prow + sw128(h, 32 * g + 16), w[4], w[5], w[6], w[7]);
                     }
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar + B_SFREE);
-                    mbar_arrive(bar + B_PFULL);
+                    mbar_arrive(bar + B_SFREE + slot);
+                    mbar_arrive(bar + B_PFULL + slot);
                 }
             }
             if (ab) break;
@@ -537,15 +572,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (bar_or(2, 128, !okw)) break;
             oph ^= 1u;
             tc_fence_after();
-#pragma unroll
-            for (int h = 0; h < N; ++h) {
-                float v = l[h];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) scr[warp * N + h] = v;
-            }
-            const size_t slot = (size_t)it.split_base[x.b] + x.s;
-            const size_t row0 = slot * p.n_heads + hbase;
+            const size_t slot_id = (size_t)it.split_base[x.b] + x.s;
+            const size_t row0 = slot_id * p.n_heads + hbase;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -560,12 +588,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar + B_OFREE);
-            named_bar_sync(2, 128);
-            if (tid < N) {
-                const float L = scr[tid] + scr[N + tid] + scr[2 * N + tid] + scr[3 * N + tid];
-                p.ml[row0 + tid] = make_float2(L > 0.f ? m_ref[tid] * kLn2 : kNeutralM, L);
-            }
-            named_bar_sync(2, 128);
+            if (owner) p.ml[row0 + h] = make_float2(l > 0.f ? m * kLn2 : kNeutralM, l);
         }
     }
 
