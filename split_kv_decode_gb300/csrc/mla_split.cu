@@ -30,11 +30,13 @@
 //               head 16w + l: its 64 scores, running max m and sum l stay in
 //               registers, and its probability row is one 128-byte row of P.
 //               All 128 threads (one per TMEM lane) read O^T in the epilogue.
-//   warps 4-11  converters: 4 rows each, 8 chunks of 128-bit loads in flight.
+//   warps 4-11  converters: 4 rows each; a whole tile row (nine 64-column chunks)
+//               of 128-bit loads in flight per lane.
 //               They only store and arrive on a barrier: no proxy fence, so
 //               their loads stay in flight across tiles.
 //   warp 12     TMEM allocation and the one thread that issues the MMAs; it
-//               issues QK(t) before PV(t-1), so QK overlaps the softmax.
+//               polls both products and issues whichever is ready: QK(t+1)
+//               once the tile is in, PV(t) once P(t) is written.
 //   warp 13     publisher: once the converters have stored a tile half, it
 //               makes the stores visible to the async proxy (one fence per
 //               tile, on the synchronisation path from the stores to the
@@ -68,7 +70,6 @@ constexpr int kRowsPerConv = 32 / kConvWarps;     // rows of the half-tile per c
 constexpr int kMmaWarp = kSoftWarps + kConvWarps;
 constexpr int kPubWarp = kMmaWarp + 1;
 constexpr int kThreads = (kPubWarp + 1) * 32;
-constexpr int kPF = 8;                            // converter chunks in flight
 constexpr float kTau = 8.f;                       // lazy-rescale threshold (log2 units)
 constexpr int kPeerTx = kChunks * kConvWarps * kRowsPerConv * 128; // bytes the peer ships per tile
 
@@ -240,91 +241,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int cw = warp - kSoftWarps;
         const uint32_t row0 = rank * 32 + cw * kRowsPerConv; // this warp's rows of every tile
         const int trow = lane >> 3, q8 = lane & 7;            // this lane's row and 8 columns
+        // lane q8 takes floats [4*q8, 4*q8 + 4) and [32 + 4*q8, 36 + 4*q8) of each
+        // 64-column chunk: each load instruction reads whole 128-byte halves of 4 rows
+        const uint32_t off_lo = sw128(row0 + trow, q8 * 8), off_hi = sw128(row0 + trow, 64 + q8 * 8);
         uint32_t eph = 0, qph = 0;
         bool ok = true;
-        float4 ld[kPF][2];
-        Cursor ahead, cur;
-        ahead.start(it, cluster);
-        cur.start(it, cluster);
-        auto issue = [&](const Cursor &u, float4 (&r)[2]) {
-            const int pos = u.x.p0 + u.t * kTile + (int)row0 + trow;
-            if (pos < u.x.p1) {
-                // lane q8 takes floats [4*q8, 4*q8 + 4) and [32 + 4*q8, 36 + 4*q8) of the
-                // chunk: each load instruction reads whole 128-byte halves of 4 rows
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    p.cache + (size_t)u.x.b * p.batch_stride + (size_t)pos * p.pos_stride +
-                    u.c * 64 + q8 * 4);
-                r[0] = __ldg(src);
-                r[1] = __ldg(src + 8);
-            } else {
-                r[0] = r[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        // A whole tile of this lane's row (9 chunks) is in flight in registers:
+        // the loads of tile t+1 go out as the stores of tile t free the registers,
+        // and the unrolled body has no branch. Rows past the item's end are
+        // loaded from its last row and stored as zeros (the cache may hold
+        // anything there; the zero rows keep the PV product finite).
+        float4 ld[kChunks][2];
+        auto row_src = [&](const Cursor &u) {
+            const int pos = min(u.x.p0 + u.t * kTile + (int)row0 + trow, u.x.p1 - 1);
+            return reinterpret_cast<const float4 *>(p.cache + (size_t)u.x.b * p.batch_stride +
+                                                    (size_t)pos * p.pos_stride + q8 * 4);
         };
+        Cursor cur;
+        cur.start(it, cluster);
+        if (!cur.done) {
+            const float4 *src = row_src(cur);
 #pragma unroll
-        for (int k = 0; k < kPF - 1; ++k)
-            if (!ahead.done) {
-                issue(ahead, ld[k]);
-                ahead.next(it, nclusters);
+            for (int c = 0; c < kChunks; ++c) {
+                ld[c][0] = ldg_stream_v4(src + 16 * c);
+                ld[c][1] = ldg_stream_v4(src + 16 * c + 8);
             }
-        while (ok && !cur.done) {
+        }
+        while (!cur.done) {
+            Cursor nxt = cur;
+            nxt.next_tile(it, nclusters);
+            const int slot = cur.gt & 1;
+            if (cur.t == 0) {
+                // a new item: this CTA's heads of q (scale and log2 e folded in),
+                // once the previous item's QK products are done with Q
+                if (!mbar_wait_bounded(bar + B_QFREE, qph ^ 1u, p.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                qph ^= 1u;
+                const float *qb = p.q + ((size_t)cur.x.b * p.n_heads + hbase) * kDk;
+                for (int task = cw * 32 + lane; task < N * 72; task += kConvWarps * 32) {
+                    const int h = task / 72, g = task % 72, c = g >> 3, j = g & 7;
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + g * 8));
+                    const float4 b = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + g * 8 + 4));
+                    const float sc = p.scale_log2;
+                    sts_v4(sm_base + LY::Q + c * LY::QCH + sw128(h, j * 16),
+                           pack_bf16(a.x * sc, a.y * sc), pack_bf16(a.z * sc, a.w * sc),
+                           pack_bf16(b.x * sc, b.y * sc), pack_bf16(b.z * sc, b.w * sc));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar + B_QFULL);
+            }
+            // the slot is free once both CTAs' MMAs are done with its last tile
+            if (!mbar_wait_bounded(bar + B_EMPTY + slot, ((eph >> slot) & 1u) ^ 1u, p.timeout_ns,
+                                   abort_flag)) {
+                ok = false;
+                break;
+            }
+            eph ^= 1u << slot;
+            const bool valid = cur.x.p0 + cur.t * kTile + (int)row0 + trow < cur.x.p1;
+            // after the last tile the loads re-read this tile's row (never used)
+            const float4 *nsrc = nxt.done ? row_src(cur) : row_src(nxt);
+            const uint32_t tile = sm_base + LY::TILE + slot * kSlotBytes;
+            // (under DA_FLAG_TEST_NO_TMA the publisher ships nothing; the
+            // converters run unchanged)
 #pragma unroll
-            for (int u = 0; u < kPF; ++u) {
-                if (!ok || cur.done) break;
-                if (!ahead.done) {
-                    issue(ahead, ld[(u + kPF - 1) % kPF]);
-                    ahead.next(it, nclusters);
-                }
-                const int slot = cur.gt & 1;
-                if (cur.c == 0) {
-                    if (cur.t == 0) {
-                        // a new item: this CTA's heads of q (scale and log2 e folded
-                        // in), once the previous item's QK products are done with Q
-                        if (!mbar_wait_bounded(bar + B_QFREE, qph ^ 1u, p.timeout_ns, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        qph ^= 1u;
-                        const float *qb = p.q + ((size_t)cur.x.b * p.n_heads + hbase) * kDk;
-                        for (int task = cw * 32 + lane; task < N * 72; task += kConvWarps * 32) {
-                            const int h = task / 72, g = task % 72, c = g >> 3, j = g & 7;
-                            const float4 a = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + g * 8));
-                            const float4 b = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + g * 8 + 4));
-                            const float sc = p.scale_log2;
-                            uint4 v;
-                            v.x = pack_bf16(a.x * sc, a.y * sc);
-                            v.y = pack_bf16(a.z * sc, a.w * sc);
-                            v.z = pack_bf16(b.x * sc, b.y * sc);
-                            v.w = pack_bf16(b.z * sc, b.w * sc);
-                            sts_v4(sm_base + LY::Q + c * LY::QCH + sw128(h, j * 16), v.x, v.y, v.z, v.w);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar + B_QFULL);
-                    }
-                    // the slot is free once both CTAs' MMAs are done with its last tile
-                    if (!mbar_wait_bounded(bar + B_EMPTY + slot, ((eph >> slot) & 1u) ^ 1u,
-                                           p.timeout_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    eph ^= 1u << slot;
-                }
-                uint4 pk;
-                pk.x = pack_bf16(ld[u][0].x, ld[u][0].y);
-                pk.y = pack_bf16(ld[u][0].z, ld[u][0].w);
-                pk.z = pack_bf16(ld[u][1].x, ld[u][1].y);
-                pk.w = pack_bf16(ld[u][1].z, ld[u][1].w);
-                // (under DA_FLAG_TEST_NO_TMA the publisher ships nothing; the
-                // converters run unchanged: a flag test here slows the loop)
-                const uint32_t chunk = sm_base + LY::TILE + slot * kSlotBytes + cur.c * kChunkBytes;
-                sts_v2(chunk + sw128(row0 + trow, q8 * 8), pk.x, pk.y);
-                sts_v2(chunk + sw128(row0 + trow, 64 + q8 * 8), pk.z, pk.w);
-                if (cur.c == kChunks - 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar + B_CONV + slot);
-                }
-                cur.next(it, nclusters);
+            for (int c = 0; c < kChunks; ++c) {
+                const uint32_t a0 = pack_bf16(ld[c][0].x, ld[c][0].y);
+                const uint32_t a1 = pack_bf16(ld[c][0].z, ld[c][0].w);
+                const uint32_t b0 = pack_bf16(ld[c][1].x, ld[c][1].y);
+                const uint32_t b1 = pack_bf16(ld[c][1].z, ld[c][1].w);
+                sts_v2(tile + c * kChunkBytes + off_lo, valid ? a0 : 0u, valid ? a1 : 0u);
+                sts_v2(tile + c * kChunkBytes + off_hi, valid ? b0 : 0u, valid ? b1 : 0u);
+                ld[c][0] = ldg_stream_v4(nsrc + 16 * c);
+                ld[c][1] = ldg_stream_v4(nsrc + 16 * c + 8);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + B_CONV + slot);
+            cur = nxt;
         }
         if (!ok) raise_abort(abort_flag, abort_peer, p.status);
         // every commit (local and the peer's) aimed at this CTA's empty barriers
@@ -487,17 +482,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int nvalid = min(kTile, x.p1 - (x.p0 + t * kTile));
                 const uint32_t scol = tl + slot * kTile;
-                // the tile max of this thread's head over the valid positions
+                // this thread's head: its 64 scores (one TMEM round trip) and
+                // their max over the valid positions
+                float sc[kTile];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) tmem_ld16(scol + 16 * g, sc + 16 * g);
+                tmem_wait_ld();
                 float tm = -INFINITY;
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    float sg[16];
-                    tmem_ld16(scol + 16 * g, sg);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (16 * g + i < nvalid) tm = fmaxf(tm, sg[i]);
-                }
+                for (int i = 0; i < kTile; ++i)
+                    if (i < nvalid) tm = fmaxf(tm, sc[i]);
                 const bool ex = owner && tm > m + kTau;
                 if (bar_or(2, 128, ex)) {
                     // move the reference of the heads that outgrew it; rescale l and O^T
@@ -530,6 +524,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tmem_wait_st();
                     }
                     named_bar_sync(2, 128); // alpha_sm is read before it is rewritten
+                    // the scores are not held across this rare path: read them again
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) tmem_ld16(scol + 16 * g, sc + 16 * g);
+                    tmem_wait_ld();
                 }
                 // P row of this head: 2^(s - m) in bf16, once PV(t-2) is done with the slot
                 okw = mbar_wait_bounded(bar + B_PFREE + slot, ((ppf >> slot) & 1u) ^ 1u,
@@ -540,17 +538,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 ppf ^= 1u << slot;
                 const uint32_t prow = sm_base + LY::PT + slot * LY::QCH;
+                if (owner) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    float sg[16];
-                    tmem_ld16(scol + 16 * g, sg);
-                    tmem_wait_ld();
-                    if (owner) {
+                    for (int g = 0; g < 4; ++g) {
                         uint32_t w[8];
 #pragma unroll
                         for (int i = 0; i < 16; i += 2) {
-                            const float p0 = (16 * g + i < nvalid) ? ex2(sg[i] - m) : 0.f;
-                            const float p1 = (16 * g + i + 1 < nvalid) ? ex2(sg[i + 1] - m) : 0.f;
+                            const float p0 = (16 * g + i < nvalid) ? ex2(sc[16 * g + i] - m) : 0.f;
+                            const float p1 =
+                                (16 * g + i + 1 < nvalid) ? ex2(sc[16 * g + i + 1] - m) : 0.f;
                             l += p0 + p1;
                             w[i >> 1] = pack_bf16(p0, p1);
                         }

@@ -35,6 +35,17 @@ __device__ __forceinline__ void sts_v4(uint32_t saddr, uint32_t a, uint32_t b, u
                  : "memory");
 }
 
+// 128-bit read-only global load, not cached in L1, kept in program order with
+// the other volatile asm (a prefetch issued early stays early)
+__device__ __forceinline__ float4 ldg_stream_v4(const float4 *p)
+{
+    float4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // ---- mbarrier -------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
