@@ -43,7 +43,9 @@ WORKLOADS = {
     "mla96_f32_L131072": ("mla_96", None),
 }
 DEFAULT = "gqa16x4_f16_L151552"
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gqa_split_traffic.txt")
+# the split kernel each workload runs, and the arithmetic type it computes in
+KERNEL = {"mla96_f32_L131072": ("mla_split_kernel", "bf16")}
+DEFAULT_KERNEL = ("gqa_split_kernel", "f32")
 
 
 def dist_env():
@@ -61,26 +63,33 @@ def load_peaks():
         return 6800.0, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel):
+    """Hash of the sources a split kernel is compiled from (its own files plus
+    the shared PTX helpers and internal header)."""
     import hashlib
     h = hashlib.sha256()
     src = os.path.join(ROOT, "split_kv_decode_gb300", "csrc")
+    own = "gqa" if kernel.startswith("gqa") else "mla"
     for f in sorted(os.listdir(src)):
-        if f.startswith("gqa") or f in ("ptx.cuh", "internal.h"):
+        if f.startswith(own) or f in ("ptx.cuh", "internal.h"):
             h.update(open(os.path.join(src, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def traffic_file(kernel, workload):
+    return os.path.join(ROOT, "profiles", f"{kernel.replace('_kernel', '')}_{workload}.traffic.txt")
+
+
+def profiled_traffic(kernel, workload):
     """Per-launch DRAM bytes of the split kernel from the committed ncu summary,
     or None if there is none for this workload or the kernel changed since."""
     try:
-        lines = open(PROFILE_TRAFFIC).read().splitlines()
+        lines = open(traffic_file(kernel, workload)).read().splitlines()
     except OSError:
         return None
     kv = dict(l.split(":", 1) for l in lines if ":" in l and not l.startswith("#"))
     kv = {k.strip(): v.strip() for k, v in kv.items()}
-    if kv.get("workload") != workload or kv.get("kernel_source_hash") != kernel_source_hash():
+    if kv.get("workload") != workload or kv.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     try:
         return int(float(kv["traffic_bytes_per_launch"]))
@@ -327,12 +336,13 @@ def main():
     peak, peak_src = load_peaks()
     achieved = case.kv_bytes / (split_mean * 1e-6) / 1e9
     kv_gbs_step = case.kv_bytes / (statistics.mean(step_us) * 1e-6) / 1e9
+    kernel, arith = KERNEL.get(args.workload, DEFAULT_KERNEL)
 
     line = {
         "metric": "decode-attention us/layer-step (and KV GB/s)", "value": round(value, 2),
         "unit": "us/layer-step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(value / 1e3, 5), "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": arith, "data": "synthetic",
         "config": workload_config(args.workload, case),
         "kv_gbs": round(kv_gbs_step, 1),
         "hbm_frac_of_8tbs": round(kv_gbs_step / 8000.0, 4),
@@ -342,8 +352,8 @@ def main():
                  "chunk": plan.chunk[0], "n_splits": plan.n_splits[0]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(args.workload),
-                     "kernel": "gqa_split_kernel", "peak_source": peak_src,
+                     "traffic": profiled_traffic(kernel, args.workload),
+                     "kernel": kernel, "peak_source": peak_src,
                      "bytes_per_launch": case.kv_bytes},
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
