@@ -144,6 +144,8 @@ int64_t decode_attn_workspace_bytes(const da_plan_t *plan);
  *               one pointer must never serve two devices). Contents need no
  *               initialisation.
  * Validation before any launch: DA_EINVAL / DA_EUNSUPPORTED / DA_ENOSPACE.
+ * The MLA kernel (head_dim 576, v_dim 512, one KV head) needs an f32 cache,
+ * 32, 64 or 96 heads, and k_cache == v_cache; otherwise DA_EUNSUPPORTED.
  * A failed launch: DA_ELAUNCH, message names the phase ("split"/"combine").
  * Asynchronous: a timed-out wait inside the kernel is reported later by
  * decode_attn_device_status().

@@ -241,10 +241,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
                const void *v, void *ws, cudaStream_t st)
 {
-    if (k != v)
-        return fail(DA_EUNSUPPORTED, "split",
-                    "MLA values must be the first 512 columns of the key rows: pass the same "
-                    "buffer as k_cache and v_cache");
+    (void)v; // the same buffer as k (checked with the arguments)
     MlaParams p;
     std::memset(&p, 0, sizeof p);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -340,13 +337,15 @@ int launch_combine_phase(const da_args_t *a, const da_plan_t *pl, const void *ws
     return DA_OK;
 }
 
-int check_buffers(const da_args_t *a, const float *q, const void *k, const void *v,
-                  const void *out)
+int check_buffers(int kernel, const float *q, const void *k, const void *v, const void *out)
 {
     if (!q || !k || !v || !out) return fail(DA_EINVAL, "args", "a tensor pointer is NULL");
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
         return fail(DA_EINVAL, "args", "q, caches and out must be 16-byte aligned");
-    (void)a;
+    if (kernel == DA_KERNEL_MLA_TC && k != v)
+        return fail(DA_EUNSUPPORTED, "args",
+                    "MLA values must be the first 512 columns of the key rows: pass the same "
+                    "buffer as k_cache and v_cache");
     return DA_OK;
 }
 
@@ -431,7 +430,7 @@ int decode_attn_splitk_ex(const da_args_t *a, const da_plan_t *plan, const float
     KernelChoice kc;
     rc = check_plan(a, plan, &kc);
     if (rc) return rc;
-    rc = check_buffers(a, q, k, v, out);
+    rc = check_buffers(kc.kernel, q, k, v, out);
     if (rc) return rc;
     if (!ws || !aligned(ws, 256))
         return fail(DA_EINVAL, "args", "workspace must be non-NULL and 256-byte aligned");

@@ -222,3 +222,88 @@ def test_version_and_null_handling(lib):
     assert lib.decode_attn_plan(None, None, 152, None) == N.DA_EINVAL
     assert lib.decode_attn_workspace_bytes(None) == 0
     assert lib.decode_attn_device_status(None, None) == N.DA_EINVAL
+
+
+def mla_args(batch=1, hq=96, cap=131072, dt=N.DA_F32):
+    a = N.DaArgs()
+    a.batch, a.n_heads, a.n_kv_heads, a.head_dim, a.v_dim = batch, hq, 1, 576, 512
+    a.capacity = cap
+    a.k_pos_stride = a.v_pos_stride = 576
+    a.k_head_stride = a.v_head_stride = 576
+    a.k_batch_stride = a.v_batch_stride = cap * 576
+    a.kv_dtype, a.out_dtype = dt, N.DA_F32
+    a.scale = 1.0 / 24
+    return a
+
+
+def check_mla_invariants(a, p, lens, sms):
+    assert p.kernel == N.DA_KERNEL_MLA_TC and p.tile == 16 and p.ctas_per_sm == 1
+    base = 0
+    for b, L in enumerate(lens):
+        assert p.chunk[b] % 16 == 0
+        assert p.n_splits[b] == -(-L // p.chunk[b]) and (p.n_splits[b] - 1) * p.chunk[b] < L
+        assert p.split_base[b] == base
+        base += p.n_splits[b]
+    assert p.total_splits == base and p.n_items == base      # one KV head: item = split
+    # a work item is one 2-CTA cluster: the grid is whole clusters, one CTA per SM
+    assert p.grid % 2 == 0 and 2 <= p.grid <= 2 * p.n_items
+    assert p.grid <= max(2, sms - sms % 2)
+    assert p.workspace_bytes >= base * a.n_heads * (a.v_dim + 2) * 4
+
+
+@pytest.mark.parametrize("hq", [32, 64, 96])
+def test_mla_plan_one_cluster_per_sm_pair(lib, hq):
+    a = mla_args(hq=hq)
+    rc, p = plan(lib, a, [131072])
+    assert rc == 0, lib.decode_attn_last_error()
+    check_mla_invariants(a, p, [131072], 152)
+    assert p.grid == 152 and p.n_items == 76        # one balanced wave of 76 clusters
+
+
+@pytest.mark.parametrize("sms", [2, 3, 7, 148, 152])
+def test_mla_plan_any_sm_count(lib, sms):
+    lens = [700, 5000, 129, 131072]
+    a = mla_args(batch=4)
+    rc, p = plan(lib, a, lens, sms)
+    assert rc == 0
+    check_mla_invariants(a, p, lens, sms)
+
+
+def test_mla_plan_short_context_and_forced_splits(lib):
+    a = mla_args(cap=4096)
+    for L in (1, 15, 16, 17, 4096):
+        rc, p = plan(lib, a, [L])
+        assert rc == 0
+        check_mla_invariants(a, p, [L], 152)
+    a.force_splits = 7
+    rc, p = plan(lib, a, [2500])
+    assert rc == 0 and p.n_splits[0] == 7
+    check_mla_invariants(a, p, [2500], 152)
+
+
+@pytest.mark.parametrize("mutate,msg", [
+    (lambda a: setattr(a, "kv_dtype", N.DA_F16), "f32"),
+    (lambda a: setattr(a, "n_heads", 48), "heads"),
+    (lambda a: setattr(a, "n_heads", 128), "heads"),
+    (lambda a: setattr(a, "k_pos_stride", 575) or setattr(a, "v_pos_stride", 575), "576"),
+    (lambda a: setattr(a, "k_pos_stride", 577) or setattr(a, "v_pos_stride", 577), "aligned"),
+    (lambda a: setattr(a, "v_pos_stride", 1152), "first 512"),
+])
+def test_mla_plan_rejects_unsupported_shapes(lib, mutate, msg):
+    a = mla_args(cap=4096)
+    mutate(a)
+    rc, _ = plan(lib, a, [4096])
+    assert rc == N.DA_EUNSUPPORTED
+    assert msg in lib.decode_attn_last_error().decode()
+
+
+def test_mla_run_needs_one_buffer_for_keys_and_values(lib):
+    a = mla_args(cap=4096)
+    rc, p = plan(lib, a, [4096])
+    assert rc == 0
+    P = ctypes.c_void_p
+    fake, other = P(1 << 20), P(1 << 21)      # never dereferenced: validation fails first
+    rc = lib.decode_attn_splitk_ex(ctypes.byref(a), ctypes.byref(p), fake, fake, other, fake,
+                                   fake, p.workspace_bytes, None)
+    assert rc == N.DA_EUNSUPPORTED
+    assert "same buffer" in lib.decode_attn_last_error().decode()
