@@ -71,7 +71,9 @@ constexpr int kMmaWarp = kSoftWarps + kConvWarps;
 constexpr int kPubWarp = kMmaWarp + 1;
 constexpr int kThreads = (kPubWarp + 1) * 32;
 constexpr float kTau = 8.f;                       // lazy-rescale threshold (log2 units)
-constexpr int kPeerTx = kChunks * kConvWarps * kRowsPerConv * 128; // bytes the peer ships per tile
+constexpr int kGroups = 3;                        // a tile is released to the MMA in 3 chunk groups
+constexpr int kGroupChunks = kChunks / kGroups;
+constexpr int kPeerTx = kGroupChunks * kConvWarps * kRowsPerConv * 128; // bytes the peer ships per group
 
 template <int N> struct Layout {
     static constexpr int TILE = 0;                          // 2 slots x 72 KB
@@ -80,7 +82,7 @@ template <int N> struct Layout {
     static constexpr int QEND = Q + kChunks * QCH + (kTile * 128 - QCH); // 64-row reads stay inside
     static constexpr int PT = (QEND + 1023) / 1024 * 1024;  // P: 2 slots of N rows x 128 B
     static constexpr int BAR = PT + 2 * QCH;
-    static constexpr int NBAR = 20;
+    static constexpr int NBAR = 28;
     static constexpr int MISC = BAR + NBAR * 8;             // tmem base, abort flag
     static constexpr int ALPHA = (MISC + 16 + 15) / 16 * 16; // float alpha[N]
     static constexpr int USED = ALPHA + N * 4;
@@ -93,9 +95,11 @@ template <int N> struct Layout {
 };
 
 // barrier indices (slot-indexed ones take +slot)
-constexpr int B_FULL = 0, B_EMPTY = 2, B_SFULL = 4, B_SFREE = 6, B_PFULL = 8, B_PFREE = 10,
-              B_PVDONE = 12, B_OREADY = 13, B_OFREE = 14, B_QFULL = 15, B_QFREE = 16,
-              B_DRAIN = 17, B_CONV = 18; // B_CONV + slot: local converters have stored their rows
+// B_FULL + kGroups*slot + g: chunk group g of the slot's tile is in (both halves);
+// B_CONV + kGroups*slot + g: this CTA's converters have stored their rows of group g
+constexpr int B_FULL = 0, B_EMPTY = 6, B_SFULL = 8, B_SFREE = 10, B_PFULL = 12, B_PFREE = 14,
+              B_PVDONE = 16, B_OREADY = 17, B_OFREE = 18, B_QFULL = 19, B_QFREE = 20,
+              B_DRAIN = 21, B_CONV = 22;
 
 // byte offset of (row, byte) in a region of 128-byte rows with 128-byte swizzle
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t byte)
@@ -211,8 +215,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar + B_FULL + s, 1);
-            mbar_init(bar + B_CONV + s, kConvWarps);
+            for (int g = 0; g < kGroups; ++g) {
+                mbar_init(bar + B_FULL + kGroups * s + g, 1);
+                mbar_init(bar + B_CONV + kGroups * s + g, kConvWarps);
+            }
             mbar_init(bar + B_EMPTY + s, 2);
             mbar_init(bar + B_SFULL + s, 1);
             mbar_init(bar + B_SFREE + s, kSoftWarps);
@@ -316,9 +322,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 sts_v2(tile + c * kChunkBytes + off_hi, valid ? b0 : 0u, valid ? b1 : 0u);
                 ld[c][0] = ldg_stream_v4(nsrc + 16 * c);
                 ld[c][1] = ldg_stream_v4(nsrc + 16 * c + 8);
+                if (c % kGroupChunks == kGroupChunks - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar + B_CONV + kGroups * slot + c / kGroupChunks);
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar + B_CONV + slot);
             cur = nxt;
         }
         if (!ok) raise_abort(abort_flag, abort_peer, p.status);
@@ -334,6 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, N, 1, 0);
             uint32_t fph = 0, sph = 0, pph = 0, oph = 0, qph = 0;
             bool ok = true, q_ready = false;
+            int qg = 0; // next chunk group of the current QK tile
             // Two cursors over this cluster's tiles: the next QK product and the
             // next PV product (never ahead of the QK cursor). Each turn issues
             // whichever is ready, so PV(t) goes out as soon as P(t) is written
@@ -384,30 +393,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         qph ^= 1u;
                         q_ready = true;
                     }
-                    if (q_ready && mbar_test(bar + B_FULL + slot, (fph >> slot) & 1u) &&
-                        mbar_test(bar + B_SFREE + slot, ((sph >> slot) & 1u) ^ 1u)) {
-                        fph ^= 1u << slot;
-                        sph ^= 1u << slot;
+                    const int fb = kGroups * slot + qg;
+                    if (q_ready && mbar_test(bar + B_FULL + fb, (fph >> fb) & 1u) &&
+                        (qg > 0 || mbar_test(bar + B_SFREE + slot, ((sph >> slot) & 1u) ^ 1u))) {
+                        fph ^= 1u << fb;
+                        if (qg == 0) sph ^= 1u << slot;
                         tc_fence_after();
                         // descriptors advance by adding (byte offset >> 4) to the start field
-                        const uint64_t qd = smem_desc_sw128(sm_base + LY::Q, 16, 1024);
-                        const uint64_t kd =
-                            smem_desc_sw128(sm_base + LY::TILE + slot * kSlotBytes, 16, 1024);
+                        const int c0 = qg * kGroupChunks;
+                        const uint64_t qd =
+                            smem_desc_sw128(sm_base + LY::Q + c0 * LY::QCH, 16, 1024);
+                        const uint64_t kd = smem_desc_sw128(
+                            sm_base + LY::TILE + slot * kSlotBytes + c0 * kChunkBytes, 16, 1024);
 #pragma unroll
-                        for (int c = 0; c < kChunks; ++c)
+                        for (int c = 0; c < kGroupChunks; ++c)
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 tc_mma_bf16(tmem + slot * kTile,
                                             qd + (uint64_t)((c * LY::QCH + k * 32) >> 4),
                                             kd + (uint64_t)((c * kChunkBytes + k * 32) >> 4),
-                                            IDESC_QK, (c | k) != 0);
-                        tc_commit(bar + B_SFULL + slot);
-                        if (qk.t == qk.x.ntiles - 1) {
-                            tc_commit(bar + B_QFREE);
-                            q_ready = false;
-                        }
+                                            IDESC_QK, (qg | c | k) != 0 ? 1u : 0u);
                         progress = true;
-                        qk.next_tile(it, nclusters);
+                        if (++qg == kGroups) {
+                            qg = 0;
+                            tc_commit(bar + B_SFULL + slot);
+                            if (qk.t == qk.x.ntiles - 1) {
+                                tc_commit(bar + B_QFREE);
+                                q_ready = false;
+                            }
+                            qk.next_tile(it, nclusters);
+                        }
                     }
                 }
                 if (progress) {
@@ -436,23 +451,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const Item x = get_item(it, item);
                 for (int t = 0; t < x.ntiles; ++t, ++gt) {
                     const int slot = gt & 1;
-                    if (!mbar_wait_bounded(bar + B_CONV + slot, (cph >> slot) & 1u, p.timeout_ns,
-                                           abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    cph ^= 1u << slot;
-                    // the converters' stores, acquired through B_CONV, become visible to
-                    // the async proxy (the bulk copies here, the MMAs after B_FULL)
-                    fence_proxy_async_smem();
-                    const uint32_t half = LY::TILE + slot * kSlotBytes + rank * 32 * 128;
-                    const uint32_t peer_full = map_to_rank(smem_u32(bar + B_FULL + slot), peer);
+                    for (int g = 0; g < kGroups && ok; ++g) {
+                        const int fb = kGroups * slot + g;
+                        if (!mbar_wait_bounded(bar + B_CONV + fb, (cph >> fb) & 1u, p.timeout_ns,
+                                               abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        cph ^= 1u << fb;
+                        // the converters' stores, acquired through B_CONV, become visible
+                        // to the async proxy (the bulk copies here, the MMAs after B_FULL)
+                        fence_proxy_async_smem();
+                        const uint32_t half = LY::TILE + slot * kSlotBytes + rank * 32 * 128;
+                        const uint32_t peer_full = map_to_rank(smem_u32(bar + B_FULL + fb), peer);
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-                        const uint32_t src = sm_base + half + c * kChunkBytes;
-                        bulk_copy_to_cta(map_to_rank(src, peer), src, 32 * 128, peer_full);
+                        for (int c = g * kGroupChunks; c < (g + 1) * kGroupChunks; ++c) {
+                            const uint32_t src = sm_base + half + c * kChunkBytes;
+                            bulk_copy_to_cta(map_to_rank(src, peer), src, 32 * 128, peer_full);
+                        }
+                        mbar_arrive_expect_tx(bar + B_FULL + fb, kPeerTx);
                     }
-                    mbar_arrive_expect_tx(bar + B_FULL + slot, kPeerTx);
+                    if (!ok) break;
                 }
             }
             if (!ok) raise_abort(abort_flag, abort_peer, p.status);
