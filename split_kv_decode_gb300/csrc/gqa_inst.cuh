@@ -22,29 +22,33 @@ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 //     64 KB;
 //   * then as many stages (2..6) as fit in 180 KB of shared memory.
 // P (rows per warp per tile) is a power of two.
-constexpr int gqa_reg_est(int P, int G, int EPL) { return 2 * G * EPL + P * G + 64; }
+// Rows of 256 bytes (D = 128 in a 16-bit type) are read by half-warps, two rows
+// at a time (LPR = 16 lanes per row, 16-byte loads): twice the q and acc
+// registers per lane (EPL = D / LPR) but half the dot registers per row, so
+// it is used for G <= 4 only.
+constexpr int gqa_reg_est(int PH, int G, int EPL) { return 2 * G * EPL + PH * G + 64; }
 
 template <int ES, int D, int G> struct GqaGeom {
-    static constexpr int EPL = D / 32;
-    static constexpr int P11 = pow2_floor(cmin((168 - 64 - 2 * G * EPL) / G > 0
-                                                   ? (168 - 64 - 2 * G * EPL) / G
-                                                   : 0,
-                                               49152 / (2 * 11 * D * ES)));
-    static constexpr bool WIDE = (168 - 64 - 2 * G * EPL) / G >= 2 && P11 >= 2 &&
-                                 (P11 * G) % 4 == 0;
+    static constexpr int LPR = (D * ES == 256 && G <= 4) ? 16 : 32;
+    static constexpr int RPW = 32 / LPR;
+    static constexpr int EPL = D / LPR;
+    static constexpr int B11 = (168 - 64 - 2 * G * EPL) / G; // dot registers per head
+    static constexpr int P11 = pow2_floor(cmin(B11 > 0 ? RPW * B11 : 0, 49152 / (2 * 11 * D * ES)));
+    static constexpr bool WIDE = B11 >= 2 && P11 >= 2 * RPW && (P11 * G) % 4 == 0;
     static constexpr int NCW = WIDE ? 11 : 7;
-    static constexpr int P = WIDE ? P11
-                                  : pow2_floor(cmin(65536 / (2 * 7 * D * ES), (176 - 2 * G * EPL) / G));
+    static constexpr int P =
+        WIDE ? P11 : pow2_floor(cmin(65536 / (2 * 7 * D * ES), RPW * ((176 - 2 * G * EPL) / G)));
     static constexpr int T = P * NCW;
     static constexpr int STAGE = 2 * T * D * ES;
     static constexpr int NST = cmin(6, 184320 / STAGE);
     static_assert(NST >= 2, "at least two stages");
-    static_assert(!WIDE || gqa_reg_est(P, G, EPL) <= 168, "register estimate");
+    static_assert(P % RPW == 0, "whole row steps");
+    static_assert(!WIDE || gqa_reg_est(P / RPW, G, EPL) <= 168, "register estimate");
 };
 
 template <typename DT, int D, int G> struct GqaInst {
     using Geo = GqaGeom<sizeof(DT), D, G>;
-    using Ker = GqaKernel<DT, D, G, Geo::T, Geo::NCW, Geo::NST>;
+    using Ker = GqaKernel<DT, D, G, Geo::T, Geo::NCW, Geo::NST, Geo::LPR>;
     static void config(GqaConfig *c)
     {
         c->tile = Geo::T;
@@ -55,7 +59,7 @@ template <typename DT, int D, int G> struct GqaInst {
     static cudaError_t launch(int grid, cudaStream_t st, const CUtensorMap &km,
                               const CUtensorMap &vm, const SplitParams &p)
     {
-        auto *fn = gqa_split_kernel<DT, D, G, Geo::T, Geo::NCW, Geo::NST>;
+        auto *fn = gqa_split_kernel<DT, D, G, Geo::T, Geo::NCW, Geo::NST, Geo::LPR>;
         cudaError_t e =
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Ker::SMEM_ALLOC);
         if (e != cudaSuccess) return e;

@@ -20,9 +20,10 @@
 //     online-softmax state (running max m, per-lane partial sums of l, and
 //     acc[G][D] in registers), following the recurrence of "The Kernel
 //     Level", section "But Softmax Wants the Whole Row".
-// At the end of an item the NCW warp states are merged through shared memory
-// with the same rescaling as the combine (m = max m_w, weights e^{m_w - m}),
-// and one un-normalised partial (m, l, acc[D]) per query head is written.
+// At the end of an item the NCW warp states are merged with the same
+// rescaling as the combine (m = max m_w, weights e^{m_w - m}) by a pairwise
+// tree through shared memory, and one un-normalised partial (m, l, acc[D]) per
+// query head is written.
 //
 // Scores are kept in base-2 units: q is pre-multiplied by scale*log2(e) so
 // that e^{s - m} = 2^{s2 - m2}; the stored m is converted back to natural
@@ -173,15 +174,21 @@ __device__ __forceinline__ void decode_item(const ItemTable &it, int item, int &
 
 template <int X> __host__ __device__ constexpr int align_up(int v) { return (v + X - 1) / X * X; }
 
-template <typename DT, int D, int G, int T, int NCW, int NST> struct GqaKernel {
+// LPR (lanes per row) is 32, or 16 when a row is only 256 bytes (D = 128 in a
+// 16-bit type): then the two half-warps read two rows at once, each lane with
+// one 16-byte load per row, and the dot products reduce over 16 lanes.
+template <typename DT, int D, int G, int T, int NCW, int NST, int LPR> struct GqaKernel {
     static constexpr int ES = sizeof(DT);
-    static constexpr int EPL = D / 32;                       // elements per lane per row
+    static constexpr int RPW = 32 / LPR;                     // rows a warp reads at once
+    static constexpr int EPL = D / LPR;                      // elements per lane per row
     static constexpr int CB = (EPL * ES < 16) ? EPL * ES : 16; // bytes per chunk load
     static constexpr int EPC = CB / ES;                      // elements per chunk
     static constexpr int NCH = EPL / EPC;                    // chunks per lane per row
     static constexpr int P = T / NCW;                        // rows per warp per tile
+    static constexpr int PH = P / RPW;                       // row steps per tile
     static constexpr int NV = P * G;                         // dots per warp per tile
-    static constexpr int R = tr_out<NV, 16>();
+    static constexpr int NVL = PH * G;                       // dots per lane group per tile
+    static constexpr int R = tr_out<NVL, LPR / 2>();
     static constexpr int R2 = (NV + 31) / 32;
     static constexpr int TILE_BYTES = T * D * ES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
@@ -193,11 +200,17 @@ template <typename DT, int D, int G, int T, int NCW, int NST> struct GqaKernel {
     static constexpr int WARP_SCR = align_up<4>(2 * NV + 2 * G); // floats: sc, pscr, mw, aw
     static constexpr int OFF_WARP = align_up<16>(OFF_ABORT + 16);
     static constexpr int OFF_ML = align_up<16>(OFF_WARP + NCW * WARP_SCR * 4);
-    static constexpr int OFF_ACC = align_up<16>(OFF_ML + NCW * G * 8);
-    static constexpr int OFF_FIN = align_up<16>(OFF_ACC + G * D * 4);
-    static constexpr int SMEM_USED = OFF_FIN + 2 * G * 4;
+    // merge tree: at distance d the warps w = d (mod 2d) pass their sums to
+    // w - d through slot w / (2d); even and odd levels use separate slot sets
+    static constexpr int tree_slots(int d) { return NCW > d ? (NCW - d + 2 * d - 1) / (2 * d) : 0; }
+    static constexpr int cmax(int a, int b) { return a > b ? a : b; }
+    static constexpr int TREE_EVEN = cmax(tree_slots(1), cmax(tree_slots(4), tree_slots(16)));
+    static constexpr int TREE_ODD = cmax(tree_slots(2), tree_slots(8));
+    static constexpr int OFF_TREE = align_up<16>(OFF_ML + NCW * G * 8);
+    static constexpr int SMEM_USED = OFF_TREE + (TREE_EVEN + TREE_ODD) * G * D * 4;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;      // slack for the 1024 alignment
-    static_assert(D % 32 == 0 && NCH * EPC == EPL, "row split");
+    static_assert(D % LPR == 0 && NCH * EPC == EPL && (LPR == 32 || LPR == 16), "row split");
+    static_assert(P % RPW == 0, "rows per warp split into lane groups");
     static_assert(T % NCW == 0 && NV % 4 == 0, "tile split");
     static_assert(T <= 256 && D <= 256, "TMA box limits");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -205,13 +218,13 @@ template <typename DT, int D, int G, int T, int NCW, int NST> struct GqaKernel {
     static_assert(TILE_BYTES % 128 == 0, "TMA destination alignment");
 };
 
-template <typename DT, int D, int G, int T, int NCW, int NST>
+template <typename DT, int D, int G, int T, int NCW, int NST, int LPR>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ SplitParams p)
 {
-    using K = GqaKernel<DT, D, G, T, NCW, NST>;
+    using K = GqaKernel<DT, D, G, T, NCW, NST, LPR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -219,8 +232,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     uint64_t *empty = full + NST;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::OFF_ABORT);
     float2 *sm_ml = reinterpret_cast<float2 *>(smem + K::OFF_ML);
-    float *sm_acc = reinterpret_cast<float *>(smem + K::OFF_ACC);
-    float *sm_fin = reinterpret_cast<float *>(smem + K::OFF_FIN);
+    float *sm_tree = reinterpret_cast<float *>(smem + K::OFF_TREE);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -296,8 +308,33 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     float *pscr = scr + K::NV;     // [NV] probabilities
     float *mw = pscr + K::NV;      // [G] running max of this warp
     float *aw = mw + G;            // [G] last rescale factors
-    const int tbase = tr_base<K::NV, 16>(lane);
-    const bool twriter = tr_writer<K::NV, 16>(lane);
+    const int half = lane / LPR, sub = lane % LPR; // lane group (row of a step) and lane in it
+    const int tbase = tr_base<K::NVL, LPR / 2>(lane);
+    const bool twriter = tr_writer<K::NVL, LPR / 2>(lane);
+
+    // q for the G heads of an item's group, pre-scaled into log2 units. The
+    // next item's q is loaded right after the last tile of the current one,
+    // so the load overlaps the merge.
+    float q[G][K::EPL];
+    auto load_q = [&](int item) {
+        int qb_b, qb_kvh, qb_s;
+        decode_item(it, item, qb_b, qb_kvh, qb_s);
+        const float *qb = p.q + ((size_t)qb_b * p.n_heads + (size_t)qb_kvh * G) * D;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int c = 0; c < K::NCH; ++c)
+#pragma unroll
+                for (int e = 0; e < K::EPC; e += 4) {
+                    float4 x = *reinterpret_cast<const float4 *>(qb + h * D +
+                                                                 (c * LPR + sub) * K::EPC + e);
+                    q[h][c * K::EPC + e + 0] = x.x * p.scale_log2;
+                    q[h][c * K::EPC + e + 1] = x.y * p.scale_log2;
+                    q[h][c * K::EPC + e + 2] = x.z * p.scale_log2;
+                    q[h][c * K::EPC + e + 3] = x.w * p.scale_log2;
+                }
+    };
+    if (blockIdx.x < it.n_items) load_q(blockIdx.x);
 
     int stage = 0;
     uint32_t phase = 0;
@@ -307,22 +344,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         const int p0 = s * it.chunk[b];
         const int p1 = min(it.seq_lens[b], p0 + it.chunk[b]);
 
-        // q for the G heads of this group, pre-scaled into log2 units
-        float q[G][K::EPL];
-        const float *qb = p.q + ((size_t)b * p.n_heads + (size_t)kvh * G) * D;
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int c = 0; c < K::NCH; ++c)
-#pragma unroll
-                for (int e = 0; e < K::EPC; e += 4) {
-                    float4 x = *reinterpret_cast<const float4 *>(qb + h * D +
-                                                                 (c * 32 + lane) * K::EPC + e);
-                    q[h][c * K::EPC + e + 0] = x.x * p.scale_log2;
-                    q[h][c * K::EPC + e + 1] = x.y * p.scale_log2;
-                    q[h][c * K::EPC + e + 2] = x.z * p.scale_log2;
-                    q[h][c * K::EPC + e + 3] = x.w * p.scale_log2;
-                }
         float acc[G][K::EPL];
         float m[G];
 #pragma unroll
@@ -350,28 +371,31 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                            warp * K::P * D;
             const int valid = min(min(T, p1 - t0) - warp * K::P, K::P);
             if (valid > 0) {
-                // ---- scores: P rows x G heads, partial over this lane's elements
-                float dv[K::NV];
+                // ---- scores: P rows x G heads, partial over this lane's elements;
+                // step r2 reads row r2 * RPW + half
+                float dv[K::NVL];
 #pragma unroll
-                for (int i = 0; i < K::NV; ++i) dv[i] = 0.f;
+                for (int i = 0; i < K::NVL; ++i) dv[i] = 0.f;
 #pragma unroll
-                for (int r = 0; r < K::P; ++r)
+                for (int r2 = 0; r2 < K::PH; ++r2)
 #pragma unroll
                     for (int c = 0; c < K::NCH; ++c) {
                         float kf[K::EPC];
-                        Chunk<DT, K::EPC>::load(Kt + r * D + (c * 32 + lane) * K::EPC, kf);
+                        Chunk<DT, K::EPC>::load(
+                            Kt + (r2 * K::RPW + half) * D + (c * LPR + sub) * K::EPC, kf);
 #pragma unroll
                         for (int h = 0; h < G; ++h)
 #pragma unroll
                             for (int e = 0; e < K::EPC; ++e)
-                                dv[r * G + h] = fmaf(q[h][c * K::EPC + e], kf[e], dv[r * G + h]);
+                                dv[r2 * G + h] = fmaf(q[h][c * K::EPC + e], kf[e], dv[r2 * G + h]);
                     }
-                tr_reduce<K::NV, 16>(dv, lane);
+                tr_reduce<K::NVL, LPR / 2>(dv, lane);
 #pragma unroll
                 for (int r = 0; r < K::R; ++r) {
-                    const int idx = tbase + r;
-                    const float sv = (idx / G < valid) ? dv[r] : -INFINITY;
-                    if (twriter) sc[idx] = sv;
+                    const int idx = tbase + r;                       // (step, head) of this group
+                    const int row = (idx / G) * K::RPW + half;
+                    const float sv = (row < valid) ? dv[r] : -INFINITY;
+                    if (twriter) sc[row * G + idx % G] = sv;
                 }
                 __syncwarp();
                 // ---- running max per head (every lane computes it redundantly)
@@ -420,9 +444,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                     }
                 }
                 __syncwarp();
-                // ---- acc += p * v over the valid rows
+                // ---- acc += p * v over the valid rows (each lane group its own rows)
 #pragma unroll
-                for (int r = 0; r < K::P; ++r) {
+                for (int r2 = 0; r2 < K::PH; ++r2) {
+                    const int r = r2 * K::RPW + half;
                     if (r < valid) {
                         float pw[G];
                         if constexpr (G % 4 == 0) {
@@ -446,7 +471,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
 #pragma unroll
                         for (int c = 0; c < K::NCH; ++c) {
                             float vf[K::EPC];
-                            Chunk<DT, K::EPC>::load(Vt + r * D + (c * 32 + lane) * K::EPC, vf);
+                            Chunk<DT, K::EPC>::load(Vt + r * D + (c * LPR + sub) * K::EPC, vf);
 #pragma unroll
                             for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -470,6 +495,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         }
         // Barrier A (always taken): the OR makes the abort decision uniform.
         if (named_bar_or(1, K::CONSUMERS, aborted || *abort_flag)) break;
+        if (item + (int)gridDim.x < it.n_items) load_q(item + gridDim.x);
+        if constexpr (K::RPW == 2) {
+            // the two lane groups hold the same value columns for different rows
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < K::EPL; ++e)
+                    acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+        }
 
         // ---- merge the NCW warp states of this item ----
         // per-warp l per head from the per-lane partial sums
@@ -487,40 +521,68 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         }
         named_bar_sync(1, K::CONSUMERS); // B
         {
-            float f[G];
+            // every warp rescales its acc to the common max of the item ...
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 float M = kNeutralM;
 #pragma unroll
                 for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm_ml[w * G + h].x);
-                f[h] = ex2(m[h] - M);
+                const float f = ex2(m[h] - M);
+#pragma unroll
+                for (int e = 0; e < K::EPL; ++e) acc[h][e] *= f;
             }
-            // the warps add in a fixed order (warp 0 stores), so the merged
-            // partial does not depend on timing: runs are bit-reproducible
-            for (int w = 0; w < NCW; ++w) {
-                if (warp == w) {
+            // ... and a pairwise tree in a fixed order sums the warps into warp 0,
+            // so the merged partial does not depend on timing (bit-reproducible)
+#pragma unroll
+            for (int d = 1, lvl = 0; d < NCW; d *= 2, ++lvl) {
+                float *set = sm_tree + ((lvl & 1) ? K::TREE_EVEN : 0) * G * D;
+                float *slot = set + (warp / (2 * d)) * G * D;
+                if (warp % (2 * d) == d && half == 0) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int c = 0; c < K::NCH; ++c)
+#pragma unroll
+                            for (int e = 0; e < K::EPC; e += 4)
+                                *reinterpret_cast<float4 *>(slot + h * D + (c * LPR + sub) * K::EPC + e) =
+                                    make_float4(acc[h][c * K::EPC + e], acc[h][c * K::EPC + e + 1],
+                                                acc[h][c * K::EPC + e + 2], acc[h][c * K::EPC + e + 3]);
+                }
+                named_bar_sync(1, K::CONSUMERS);
+                if (warp % (2 * d) == 0 && warp + d < NCW && half == 0) {
 #pragma unroll
                     for (int h = 0; h < G; ++h)
 #pragma unroll
                         for (int c = 0; c < K::NCH; ++c)
 #pragma unroll
                             for (int e = 0; e < K::EPC; e += 4) {
-                                float4 *dst4 = reinterpret_cast<float4 *>(
-                                    sm_acc + h * D + (c * 32 + lane) * K::EPC + e);
-                                float4 x = make_float4(acc[h][c * K::EPC + e] * f[h],
-                                                       acc[h][c * K::EPC + e + 1] * f[h],
-                                                       acc[h][c * K::EPC + e + 2] * f[h],
-                                                       acc[h][c * K::EPC + e + 3] * f[h]);
-                                if (w > 0) {
-                                    const float4 y = *dst4;
-                                    x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-                                }
-                                *dst4 = x;
+                                const float4 y = *reinterpret_cast<const float4 *>(
+                                    slot + h * D + (c * LPR + sub) * K::EPC + e);
+                                acc[h][c * K::EPC + e] += y.x;
+                                acc[h][c * K::EPC + e + 1] += y.y;
+                                acc[h][c * K::EPC + e + 2] += y.z;
+                                acc[h][c * K::EPC + e + 3] += y.w;
                             }
                 }
-                named_bar_sync(1, K::CONSUMERS);
             }
-            if (warp == 0 && lane < G) {
+        }
+        // warp 0 writes the partial: acc from its registers, (m, l) per head
+        if (warp == 0) {
+            const size_t slot_id = (size_t)it.split_base[b] + s;
+            const size_t row0 = slot_id * p.n_heads + (size_t)kvh * G;
+            if (half == 0) {
+                float *dst = p.acc + row0 * D;
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int c = 0; c < K::NCH; ++c)
+#pragma unroll
+                        for (int e = 0; e < K::EPC; e += 4)
+                            *reinterpret_cast<float4 *>(dst + h * D + (c * LPR + sub) * K::EPC + e) =
+                                make_float4(acc[h][c * K::EPC + e], acc[h][c * K::EPC + e + 1],
+                                            acc[h][c * K::EPC + e + 2], acc[h][c * K::EPC + e + 3]);
+            }
+            if (lane < G) {
                 float M = kNeutralM;
 #pragma unroll
                 for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm_ml[w * G + lane].x);
@@ -530,20 +592,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                     const float2 x = sm_ml[w * G + lane];
                     L += x.y * ex2(x.x - M);
                 }
-                sm_fin[lane] = M;
-                sm_fin[G + lane] = L;
-            }
-        }
-        named_bar_sync(1, K::CONSUMERS); // C
-        {
-            const size_t slot = (size_t)it.split_base[b] + s;
-            const size_t row0 = slot * p.n_heads + (size_t)kvh * G;
-            float4 *dst = reinterpret_cast<float4 *>(p.acc + row0 * D);
-            float4 *src = reinterpret_cast<float4 *>(sm_acc);
-            for (int i = threadIdx.x; i < G * D / 4; i += K::CONSUMERS) dst[i] = src[i];
-            if (threadIdx.x < G) {
-                const float M = sm_fin[threadIdx.x], L = sm_fin[G + threadIdx.x];
-                p.ml[row0 + threadIdx.x] = make_float2(L > 0.f ? M * kLn2 : kNeutralM, L);
+                p.ml[row0 + lane] = make_float2(L > 0.f ? M * kLn2 : kNeutralM, L);
             }
         }
     }
