@@ -520,14 +520,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             sm_ml[warp * G + lane] = make_float2(mw[lane], lw);
         }
         named_bar_sync(1, K::CONSUMERS); // B
+        // lane h < G forms the item's max and sum for head h over the warps
+        float Mh = kNeutralM, Lh = 0.f;
+        if (lane < G) {
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) Mh = fmaxf(Mh, sm_ml[w * G + lane].x);
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) {
+                const float2 x = sm_ml[w * G + lane];
+                Lh += x.y * ex2(x.x - Mh);
+            }
+        }
         {
             // every warp rescales its acc to the common max of the item ...
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                float M = kNeutralM;
-#pragma unroll
-                for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm_ml[w * G + h].x);
-                const float f = ex2(m[h] - M);
+                const float f = ex2(m[h] - __shfl_sync(0xffffffffu, Mh, h));
 #pragma unroll
                 for (int e = 0; e < K::EPL; ++e) acc[h][e] *= f;
             }
@@ -582,18 +590,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                                 make_float4(acc[h][c * K::EPC + e], acc[h][c * K::EPC + e + 1],
                                             acc[h][c * K::EPC + e + 2], acc[h][c * K::EPC + e + 3]);
             }
-            if (lane < G) {
-                float M = kNeutralM;
-#pragma unroll
-                for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm_ml[w * G + lane].x);
-                float L = 0.f;
-#pragma unroll
-                for (int w = 0; w < NCW; ++w) {
-                    const float2 x = sm_ml[w * G + lane];
-                    L += x.y * ex2(x.x - M);
-                }
-                p.ml[row0 + lane] = make_float2(L > 0.f ? M * kLn2 : kNeutralM, L);
-            }
+            if (lane < G) p.ml[row0 + lane] = make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
         }
     }
     if (threadIdx.x == 0) griddep_launch_dependents();

@@ -7,9 +7,11 @@
 // "Attention at 128k" §5.1 prescribes, so that the grid fills every SM
 // whatever the batch and head counts. On GB300 the split kernel is
 // persistent (one CTA per SM, static round-robin over the items), so the
-// planner scores each candidate chunk by simulating that assignment and
-// keeps the one with the smallest makespan; ties go to the larger chunk
-// (fewer partials for the combine to read).
+// planner scores each candidate by simulating that assignment and keeps the
+// one with the smallest makespan; near-ties go to fewer items (fewer
+// partials for the combine to read). Candidates are one chunk for the whole
+// batch, or -- for ragged batches -- a chunk per sequence chosen so that all
+// items have about the same length and fill a whole number of waves.
 #include <algorithm>
 #include <cstdint>
 #include <vector>
@@ -22,24 +24,55 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // Makespan (in positions, plus `overhead` per item) of the static round-robin
-// assignment of the items of `chunk` over min(items, slots) CTAs.
-static int64_t simulate(const int32_t *lens, int batch, int hkv, int64_t chunk, int slots,
-                        int64_t overhead, int64_t *n_items_out)
+// assignment of the items (sequence b cut into chunks of chunk[b]; items in
+// the kernel's order: sequence, split, KV head) over min(items, slots) CTAs.
+// Item i goes to CTA i % grid. A sequence's full splits are one contiguous run
+// of equal items, which adds a whole number of items to every CTA plus one
+// more item to a circular range of CTAs (a difference array), so the cost is
+// O(batch * hkv + grid), not O(items).
+static int64_t simulate(const int32_t *lens, int batch, int hkv, const int64_t *chunk, int slots,
+                        int64_t overhead, int64_t *n_items_out, std::vector<int64_t> &diff)
 {
+    int32_t full[DA_MAX_BATCH], rem[DA_MAX_BATCH];
     int64_t items = 0;
-    for (int b = 0; b < batch; ++b) items += ceil_div(lens[b], chunk) * hkv;
+    for (int b = 0; b < batch; ++b) {
+        full[b] = (int32_t)(lens[b] / chunk[b]);               // chunks may exceed 2^31
+        rem[b] = (int32_t)(lens[b] - (int64_t)full[b] * chunk[b]);
+        items += (int64_t)(full[b] + (rem[b] > 0)) * hkv;
+    }
     *n_items_out = items;
     const int64_t grid = std::min<int64_t>(items, slots);
-    std::vector<int64_t> cost((size_t)grid, 0);
-    int64_t item = 0;
-    for (int b = 0; b < batch; ++b) {
-        const int64_t ns = ceil_div(lens[b], chunk);
-        for (int64_t s = 0; s < ns; ++s) {
-            const int64_t len = std::min<int64_t>(chunk, lens[b] - s * chunk);
-            for (int h = 0; h < hkv; ++h, ++item) cost[(size_t)(item % grid)] += len + overhead;
+    const uint32_t g = (uint32_t)grid;
+    diff.assign((size_t)grid + 1, 0);
+    int64_t all = 0;
+    uint32_t st = 0; // (index of the next item) mod grid
+    auto run = [&](int64_t len, int64_t w) { // the next len items, each of cost w
+        const uint64_t q = (uint64_t)len / g;
+        const uint32_t r = (uint32_t)((uint64_t)len - q * g);
+        all += (int64_t)q * w;
+        if (r > 0) {
+            diff[st] += w;
+            if (st + r <= g) {
+                diff[st + r] -= w;
+            } else {
+                diff[g] -= w;
+                diff[0] += w;
+                diff[st + r - g] -= w;
+            }
+            st += r;
+            if (st >= g) st -= g;
         }
+    };
+    for (int b = 0; b < batch; ++b) {
+        run((int64_t)full[b] * hkv, chunk[b] + overhead);
+        if (rem[b] > 0) run(hkv, rem[b] + overhead);
     }
-    return *std::max_element(cost.begin(), cost.end());
+    int64_t best = 0, acc = 0;
+    for (uint32_t c = 0; c < g; ++c) {
+        acc += diff[c];
+        best = std::max(best, all + acc);
+    }
+    return best;
 }
 
 int plan_splits(const int32_t *lens, int batch, int hkv, int tile, int slots, int force_splits,
@@ -48,7 +81,9 @@ int plan_splits(const int32_t *lens, int batch, int hkv, int tile, int slots, in
     if (batch < 1 || batch > DA_MAX_BATCH || hkv < 1 || tile < 1 || slots < 1) return 1;
     for (int b = 0; b < batch; ++b)
         if (lens[b] < 1) return 1;
-    const int64_t overhead = tile; // per-item merge and partial write, in positions
+    // per-item cost in positions: the warps' merge, the partial write and the
+    // wait for the slowest warp take about as long as three tiles
+    const int64_t overhead = 3 * (int64_t)tile;
     if (force_splits > 0) {
         int64_t items = 0, cost = 0;
         for (int b = 0; b < batch; ++b) {
@@ -58,17 +93,10 @@ int plan_splits(const int32_t *lens, int batch, int hkv, int tile, int slots, in
             items += (int64_t)out->n_splits[b] * hkv;
         }
         if (items > max_items) return 2;
-        // cost of the round-robin assignment with per-sequence chunks
+        std::vector<int64_t> ch((size_t)batch), diff;
+        for (int b = 0; b < batch; ++b) ch[(size_t)b] = out->chunk[b];
+        cost = simulate(lens, batch, hkv, ch.data(), slots, overhead, &items, diff);
         const int64_t grid = std::min<int64_t>(items, slots);
-        std::vector<int64_t> c((size_t)grid, 0);
-        int64_t item = 0;
-        for (int b = 0; b < batch; ++b)
-            for (int s = 0; s < out->n_splits[b]; ++s) {
-                const int64_t len =
-                    std::min<int64_t>(out->chunk[b], lens[b] - (int64_t)s * out->chunk[b]);
-                for (int h = 0; h < hkv; ++h, ++item) c[(size_t)(item % grid)] += len + overhead;
-            }
-        cost = *std::max_element(c.begin(), c.end());
         out->n_items = (int32_t)items;
         out->grid = (int32_t)grid;
         out->est_cost = cost;
@@ -79,40 +107,53 @@ int plan_splits(const int32_t *lens, int batch, int hkv, int tile, int slots, in
         total += (int64_t)lens[b] * hkv;
         maxlen = std::max<int64_t>(maxlen, lens[b]);
     }
-    // candidate chunks: the even share of 1..32 waves over all slots, and powers
-    // of two times the tile; every candidate a multiple of the tile
+    // candidates:
+    //  (a) one chunk for every sequence: the even share of w waves over all
+    //      slots (w from 1 to 32), and powers of two times the tile;
+    //  (b) a chunk per sequence: sequence b gets about L_b / target splits, so
+    //      that the items are of about equal length, target = the even share
+    //      of w waves; every chunk a multiple of the tile
+    // candidates live in one flat array, `batch` chunks each
     std::vector<int64_t> cand;
-    for (int w = 1; w <= 32; ++w) cand.push_back(round_up(ceil_div(total, (int64_t)w * slots), tile));
-    for (int64_t c = tile; c < round_up(maxlen, tile) * 2; c *= 2) cand.push_back(c);
-    cand.push_back(round_up(maxlen, tile));
-    std::sort(cand.begin(), cand.end());
-    cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
-    struct Cand { int64_t chunk, cost, items; };
-    std::vector<Cand> ok;
-    int64_t min_cost = -1;
-    for (int64_t c : cand) {
-        int64_t items = 0;
-        const int64_t cost = simulate(lens, batch, hkv, c, slots, overhead, &items);
-        if (items > max_items) continue;
-        ok.push_back({c, cost, items});
-        if (min_cost < 0 || cost < min_cost) min_cost = cost;
-    }
-    // the largest chunk whose makespan is within 0.5% of the best one
-    int64_t best_chunk = -1, best_cost = 0, best_items = 0;
-    for (const Cand &x : ok)
-        if (x.cost * 1000 <= min_cost * 1005 && x.chunk > best_chunk) {
-            best_chunk = x.chunk;
-            best_cost = x.cost;
-            best_items = x.items;
+    cand.reserve((size_t)batch * 96);
+    auto uniform = [&](int64_t c) { cand.insert(cand.end(), (size_t)batch, c); };
+    static const int kWaves[] = {1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16, 20, 24, 28, 32};
+    for (int w : kWaves) uniform(round_up(ceil_div(total, (int64_t)w * slots), tile));
+    for (int64_t c = tile; c < round_up(maxlen, tile) * 2; c *= 2) uniform(c);
+    uniform(round_up(maxlen, tile));
+    if (batch > 1)
+        for (int w : kWaves) {
+            const int64_t target = std::max<int64_t>(tile, ceil_div(total, (int64_t)w * slots));
+            for (int b = 0; b < batch; ++b) {
+                const int64_t ns = std::max<int64_t>(1, (lens[b] + target / 2) / target);
+                cand.push_back(round_up(ceil_div(lens[b], ns), tile));
+            }
         }
-    if (best_chunk < 0) return 2;
-    for (int b = 0; b < batch; ++b) {
-        out->chunk[b] = (int32_t)best_chunk;
-        out->n_splits[b] = (int32_t)ceil_div(lens[b], best_chunk);
+    const size_t n_cand = cand.size() / (size_t)batch;
+    std::vector<int64_t> diff, cost_of(n_cand), items_of(n_cand);
+    int64_t min_cost = -1;
+    for (size_t i = 0; i < n_cand; ++i) {
+        cost_of[i] = simulate(lens, batch, hkv, &cand[i * (size_t)batch], slots, overhead,
+                              &items_of[i], diff);
+        if (items_of[i] > max_items) continue;
+        if (min_cost < 0 || cost_of[i] < min_cost) min_cost = cost_of[i];
     }
-    out->n_items = (int32_t)best_items;
-    out->grid = (int32_t)std::min<int64_t>(best_items, slots);
-    out->est_cost = best_cost;
+    // the fewest items whose makespan is within 0.5% of the best one
+    size_t best = n_cand;
+    for (size_t i = 0; i < n_cand; ++i)
+        if (items_of[i] <= max_items && cost_of[i] * 1000 <= min_cost * 1005 &&
+            (best == n_cand || items_of[i] < items_of[best] ||
+             (items_of[i] == items_of[best] && cost_of[i] < cost_of[best])))
+            best = i;
+    if (best == n_cand) return 2;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t c = cand[best * (size_t)batch + (size_t)b];
+        out->chunk[b] = (int32_t)c;
+        out->n_splits[b] = (int32_t)ceil_div(lens[b], c);
+    }
+    out->n_items = (int32_t)items_of[best];
+    out->grid = (int32_t)std::min<int64_t>(items_of[best], slots);
+    out->est_cost = cost_of[best];
     return 0;
 }
 
