@@ -217,6 +217,56 @@ int decode_attn_splitk_noalloc(const da_args_t *args, const da_plan_t *plan, con
                                const void *k_cache, const void *v_cache, void *out,
                                da_stream_t stream);
 
+/*
+ * Device-side lengths and paged caches for decode_attn_splitk_dev.
+ * "The Kernel Level: Attention and MoE" (llm-serving.xyz lecture 07), sections
+ * "A kernel alone is not a serving system" and the CUDA-graph section: the
+ * kernel indexes K/V through a block table, and the step is captured once and
+ * replayed, so everything that changes per step lives in device memory.
+ *   seq_lens      DEVICE int32[batch], the current length of every sequence,
+ *                 read by the kernel; each is clamped to [1, plan->seq_lens[b]]
+ *                 (make the plan for the largest lengths the launch will see).
+ *                 NULL: the plan's lengths. It must not change while a call
+ *                 that reads it is in flight.
+ *   block_table   DEVICE int32[batch * max_blocks_per_seq], or NULL for the
+ *                 contiguous caches of da_args_t. Entry [b][i] is the pool block
+ *                 that holds positions [i * block_size, (i + 1) * block_size)
+ *                 of sequence b; entries past a sequence's length are not read.
+ *                 With a table, k_cache / v_cache point at pools whose element
+ *                 (block, slot, kv, d) is at base + block * *_block_stride +
+ *                 slot * *_pos_stride + kv * *_head_stride + d (elements);
+ *                 capacity and the batch strides of da_args_t are not used for
+ *                 addressing (capacity must still cover every length).
+ *   block_size    positions per block: a positive multiple of 16.
+ *   num_blocks    blocks in each pool; table entries must be < num_blocks.
+ *   k_block_stride, v_block_stride  elements between blocks (16-byte multiples,
+ *                 at least block_size * pos_stride).
+ */
+typedef struct {
+    const int32_t *seq_lens;
+    const int32_t *block_table;
+    int32_t max_blocks_per_seq;
+    int32_t block_size;
+    int32_t num_blocks;
+    int32_t reserved;           /* 0 */
+    int64_t k_block_stride;
+    int64_t v_block_stride;
+} da_dev_t;
+
+/*
+ * decode_attn_splitk_dev -- decode_attn_splitk_ex with lengths read on the
+ * device and, optionally, paged K/V caches (da_dev_t). It makes no host-side
+ * decision that depends on the current lengths, so a launch captured in a CUDA
+ * graph stays valid while the lengths grow up to the plan's. Splits that start
+ * past a sequence's current length write neutral partials (l = 0). GQA/MQA
+ * kernel only: an MLA shape gets DA_EUNSUPPORTED. Validation before any launch
+ * as in decode_attn_splitk_ex, plus the da_dev_t rules above (DA_EINVAL /
+ * DA_EUNSUPPORTED).
+ */
+int decode_attn_splitk_dev(const da_args_t *args, const da_plan_t *plan, const da_dev_t *dev,
+                           const float *q, const void *k_cache, const void *v_cache, void *out,
+                           void *workspace, size_t workspace_bytes, da_stream_t stream);
+
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char *decode_attn_last_error(void);
 

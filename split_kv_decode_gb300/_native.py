@@ -55,6 +55,15 @@ class DaPlan(ctypes.Structure):
 
 # name -> (restype, argtypes), in header order
 _P = ctypes.c_void_p
+class DaDev(ctypes.Structure):
+    _fields_ = [
+        ("seq_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+        ("max_blocks_per_seq", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("k_block_stride", ctypes.c_int64), ("v_block_stride", ctypes.c_int64),
+    ]
+
+
 SIGNATURES = {
     "decode_attn_plan": (ctypes.c_int, [ctypes.POINTER(DaArgs), _P, ctypes.c_int,
                                         ctypes.POINTER(DaPlan)]),
@@ -68,6 +77,9 @@ SIGNATURES = {
     "decode_attn_device_status": (ctypes.c_int, [_P, _P]),
     "decode_attn_splitk_noalloc": (ctypes.c_int, [ctypes.POINTER(DaArgs), ctypes.POINTER(DaPlan),
                                                   _P, _P, _P, _P, _P]),
+    "decode_attn_splitk_dev": (ctypes.c_int, [ctypes.POINTER(DaArgs), ctypes.POINTER(DaPlan),
+                                              ctypes.POINTER(DaDev), _P, _P, _P, _P, _P,
+                                              ctypes.c_size_t, _P]),
     "decode_attn_last_error": (ctypes.c_char_p, []),
     "decode_attn_release": (None, []),
     "decode_attn_version": (ctypes.c_char_p, []),

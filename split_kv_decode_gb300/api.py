@@ -128,6 +128,61 @@ def decode_attn_splitk_noalloc(args: N.DaArgs, plan: N.DaPlan, q: torch.Tensor,
                                                _stream(stream)))
 
 
+def make_paged_args(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, scale: float,
+                    max_blocks_per_seq: int, *, out_dtype: torch.dtype = torch.float32,
+                    force_splits: int = 0, flags: int = 0, timeout_us: int = 0) -> N.DaArgs:
+    """da_args_t for paged pools [num_blocks, block_size, Hkv, D]: the position and
+    head strides come from the pools, the capacity is max_blocks_per_seq *
+    block_size (the batch strides are not used for addressing)."""
+    if k_pool.dim() != 4 or v_pool.dim() != 4:
+        raise ValueError("pools must be [num_blocks, block_size, Hkv, D]")
+    a = make_args(q, k_pool, v_pool, scale, out_dtype=out_dtype, force_splits=force_splits,
+                  flags=flags, timeout_us=timeout_us)
+    a.capacity = int(max_blocks_per_seq) * k_pool.shape[1]
+    return a
+
+
+def make_dev(*, seq_lens: Optional[torch.Tensor] = None,
+             block_table: Optional[torch.Tensor] = None, k_pool: Optional[torch.Tensor] = None,
+             v_pool: Optional[torch.Tensor] = None) -> N.DaDev:
+    """da_dev_t: device lengths (int32 [B] on the device) and, for paged caches, the
+    block table (int32 [B, max_blocks] on the device) with the pools
+    [num_blocks, block_size, Hkv, D]. The tensors must outlive every launch (and
+    every replay of a captured launch) that uses them."""
+    d = N.DaDev()
+    if seq_lens is not None:
+        if seq_lens.dtype != torch.int32 or not seq_lens.is_cuda:
+            raise TypeError("seq_lens must be an int32 CUDA tensor")
+        d.seq_lens = seq_lens.data_ptr()
+    if block_table is not None:
+        if block_table.dtype != torch.int32 or not block_table.is_cuda or block_table.dim() != 2:
+            raise TypeError("block_table must be a 2-D int32 CUDA tensor")
+        if not block_table.is_contiguous():
+            raise ValueError("block_table must be contiguous")
+        if k_pool is None or v_pool is None:
+            raise ValueError("a block table needs the K and V pools")
+        d.block_table = block_table.data_ptr()
+        d.max_blocks_per_seq = block_table.shape[1]
+        d.block_size = k_pool.shape[1]
+        d.num_blocks = k_pool.shape[0]
+        d.k_block_stride = k_pool.stride(0)
+        d.v_block_stride = v_pool.stride(0)
+    return d
+
+
+def decode_attn_splitk_dev(args: N.DaArgs, plan: N.DaPlan, dev: N.DaDev, q: torch.Tensor,
+                           k_cache: torch.Tensor, v_cache: torch.Tensor, out: torch.Tensor,
+                           workspace: torch.Tensor, stream=None) -> None:
+    """decode_attn_splitk_ex with lengths read on the device and, optionally,
+    paged caches; capturable in a CUDA graph (no host decision depends on the
+    current lengths)."""
+    _check(N.load().decode_attn_splitk_dev(ctypes.byref(args), ctypes.byref(plan),
+                                           ctypes.byref(dev), _ptr(q), _ptr(k_cache),
+                                           _ptr(v_cache), _ptr(out), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
+                                           _stream(stream)))
+
+
 def decode_attn_device_status(workspace: torch.Tensor, stream=None) -> None:
     _check(N.load().decode_attn_device_status(_ptr(workspace), _stream(stream)))
 

@@ -110,6 +110,7 @@ struct KernelChoice {
     int tile;        // planner quantum: chunks are multiples of it
     int ctas_per_sm;
     int cluster;     // CTAs that share one work item
+    int rows_per_warp; // GQA: rows of a tile per consumer warp
 };
 
 int select_kernel(const da_args_t *a, KernelChoice *kc)
@@ -152,6 +153,7 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
                         "cache strides must be multiples of 16 bytes for TMA tiles");
     kc->kernel = DA_KERNEL_GQA_TMA;
     kc->tile = cfg.tile;
+    kc->rows_per_warp = cfg.rows_per_warp;
     kc->ctas_per_sm = cfg.ctas_per_sm;
     kc->cluster = 1;
     return DA_OK;
@@ -205,6 +207,29 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dt, int D, int hkv,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(DA_EUNSUPPORTED, "tma", "cuTensorMapEncodeTiled rejected the cache layout (%d)",
+                    (int)r);
+    return DA_OK;
+}
+
+// 4-D map over a paged pool (d, kv head, slot in block, block) with box
+// (D, 1, rows, 1); a block coordinate past num_blocks reads zeros.
+int encode_pool_map(CUtensorMap *map, const void *base, int dt, int D, int hkv, int block_size,
+                    int num_blocks, int64_t head_st, int64_t pos_st, int64_t block_st, int rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(DA_ECUDA, "tma", "cuTensorMapEncodeTiled is unavailable");
+    const int es = dtype_size(dt);
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)block_size,
+                          (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)(head_st * es), (cuuint64_t)(pos_st * es),
+                             (cuuint64_t)(block_st * es)};
+    cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, tma_dtype(dt), 4, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(DA_EUNSUPPORTED, "tma", "cuTensorMapEncodeTiled rejected the paged pool (%d)",
                     (int)r);
     return DA_OK;
 }
@@ -271,7 +296,8 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
 }
 
 int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
-                 const void *v, void *ws, cudaStream_t st)
+                 const void *v, void *ws, cudaStream_t st, const da_dev_t *dev,
+                 int rows_per_warp)
 {
     if (pl->kernel == DA_KERNEL_MLA_TC) return launch_mla(a, pl, q, k, v, ws, st);
     SplitParams p;
@@ -296,13 +322,31 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     p.items.split_base[a->batch] = pl->total_splits;
 
     CUtensorMap km, vm;
-    int rc = encode_cache_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, a->capacity,
+    int rc;
+    if (dev && dev->block_table) {
+        p.block_table = dev->block_table;
+        p.max_blocks = dev->max_blocks_per_seq;
+        p.block_size = dev->block_size;
+        p.oob_block = dev->num_blocks;
+        rc = encode_pool_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, dev->block_size,
+                             dev->num_blocks, a->k_head_stride, a->k_pos_stride,
+                             dev->k_block_stride, rows_per_warp);
+        if (rc) return rc;
+        rc = encode_pool_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, dev->block_size,
+                             dev->num_blocks, a->v_head_stride, a->v_pos_stride,
+                             dev->v_block_stride, rows_per_warp);
+        if (rc) return rc;
+    } else {
+        rc = encode_cache_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, a->capacity,
                               a->batch, a->k_head_stride, a->k_pos_stride, a->k_batch_stride,
                               pl->tile);
-    if (rc) return rc;
-    rc = encode_cache_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, a->capacity, a->batch,
-                          a->v_head_stride, a->v_pos_stride, a->v_batch_stride, pl->tile);
-    if (rc) return rc;
+        if (rc) return rc;
+        rc = encode_cache_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, a->capacity,
+                              a->batch, a->v_head_stride, a->v_pos_stride, a->v_batch_stride,
+                              pl->tile);
+        if (rc) return rc;
+    }
+    if (dev) p.dev_lens = dev->seq_lens;
 
     const int G = a->n_heads / a->n_kv_heads;
     cudaError_t e;
@@ -441,7 +485,60 @@ int decode_attn_splitk_ex(const da_args_t *a, const da_plan_t *plan, const float
     if (pre != cudaSuccess)
         return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = launch_split(a, plan, q, k, v, ws, st);
+    rc = launch_split(a, plan, q, k, v, ws, st, nullptr, kc.rows_per_warp);
+    if (rc) return rc;
+    if (a->flags & DA_FLAG_NO_COMBINE) return DA_OK;
+    return launch_combine_phase(a, plan, ws, out, st);
+}
+
+int decode_attn_splitk_dev(const da_args_t *a, const da_plan_t *plan, const da_dev_t *dev,
+                           const float *q, const void *k, const void *v, void *out, void *ws,
+                           size_t ws_bytes, da_stream_t stream)
+{
+    int rc = check_args(a);
+    if (rc) return rc;
+    if (!dev) return fail(DA_EINVAL, "args", "dev is NULL");
+    KernelChoice kc;
+    rc = check_plan(a, plan, &kc);
+    if (rc) return rc;
+    if (kc.kernel != DA_KERNEL_GQA_TMA)
+        return fail(DA_EUNSUPPORTED, "args",
+                    "device lengths and paged caches are served by the GQA kernel only");
+    rc = check_buffers(kc.kernel, q, k, v, out);
+    if (rc) return rc;
+    if (dev->seq_lens && !aligned(dev->seq_lens, 4))
+        return fail(DA_EINVAL, "args", "dev->seq_lens must be 4-byte aligned");
+    if (dev->block_table) {
+        const int es = dtype_size(a->kv_dtype);
+        if (!aligned(dev->block_table, 4))
+            return fail(DA_EINVAL, "args", "dev->block_table must be 4-byte aligned");
+        if (dev->block_size < 16 || dev->block_size % 16)
+            return fail(DA_EUNSUPPORTED, "args", "block_size %d: a positive multiple of 16",
+                        dev->block_size);
+        if (dev->max_blocks_per_seq < 1 || dev->num_blocks < 1)
+            return fail(DA_EINVAL, "args", "max_blocks_per_seq and num_blocks must be >= 1");
+        if ((dev->k_block_stride * es) % 16 || (dev->v_block_stride * es) % 16 ||
+            dev->k_block_stride < (int64_t)dev->block_size * a->k_pos_stride ||
+            dev->v_block_stride < (int64_t)dev->block_size * a->v_pos_stride)
+            return fail(DA_EUNSUPPORTED, "args",
+                        "block strides must hold block_size positions and be multiples of 16 "
+                        "bytes");
+        for (int b = 0; b < a->batch; ++b)
+            if ((int64_t)plan->seq_lens[b] > (int64_t)dev->max_blocks_per_seq * dev->block_size)
+                return fail(DA_EINVAL, "args",
+                            "seq_lens[%d] = %d exceeds max_blocks_per_seq x block_size", b,
+                            plan->seq_lens[b]);
+    }
+    if (!ws || !aligned(ws, 256))
+        return fail(DA_EINVAL, "args", "workspace must be non-NULL and 256-byte aligned");
+    if ((int64_t)ws_bytes < plan->workspace_bytes)
+        return fail(DA_ENOSPACE, "args", "workspace %zu bytes < %lld needed", ws_bytes,
+                    (long long)plan->workspace_bytes);
+    cudaError_t pre = cudaGetLastError();
+    if (pre != cudaSuccess)
+        return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    rc = launch_split(a, plan, q, k, v, ws, st, dev, kc.rows_per_warp);
     if (rc) return rc;
     if (a->flags & DA_FLAG_NO_COMBINE) return DA_OK;
     return launch_combine_phase(a, plan, ws, out, st);

@@ -172,6 +172,14 @@ __device__ __forceinline__ void decode_item(const ItemTable &it, int item, int &
     s = t - it.split_base[lo];
 }
 
+// the length an item of sequence b attends over: the plan's, or the current
+// length read on the device, kept within [1, the plan's]
+__device__ __forceinline__ int item_len(const SplitParams &p, int b)
+{
+    const int L = p.items.seq_lens[b];
+    return p.dev_lens ? max(1, min(__ldg(p.dev_lens + b), L)) : L;
+}
+
 template <int X> __host__ __device__ constexpr int align_up(int v) { return (v + X - 1) / X * X; }
 
 // LPR (lanes per row) is 32, or 16 when a row is only 256 bytes (D = 128 in a
@@ -251,41 +259,88 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
 
     if (warp == NCW) {
         // ------------------------------- producer -------------------------------
+        // Lane 0 waits on the stage barriers and issues the copies. For paged
+        // caches the whole warp walks the items and tiles: the lanes hold a
+        // window of 32 consecutive block-table entries of the current sequence
+        // (one coalesced load), and each P-row group of a tile -- one consumer
+        // warp's rows, never straddling a block -- is its own TMA box. For
+        // contiguous caches lane 0 walks alone (one box per tile).
+        const bool paged = p.block_table != nullptr;
+        if (!paged && lane != 0) return;
+        const unsigned mask = paged ? 0xffffffffu : 1u;
         if (lane == 0) {
             tma_prefetch_map(&kmap);
             tma_prefetch_map(&vmap);
-            const uint64_t pol = l2_evict_first_policy();
-            int last_parity[NST];
+        }
+        const uint64_t pol = l2_evict_first_policy();
+        int last_parity[NST];
 #pragma unroll
-            for (int s = 0; s < NST; ++s) last_parity[s] = -1;
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int item = blockIdx.x; ok && item < it.n_items; item += gridDim.x) {
-                int b, kvh, s;
-                decode_item(it, item, b, kvh, s);
-                const int p0 = s * it.chunk[b];
-                const int p1 = min(it.seq_lens[b], p0 + it.chunk[b]);
-                for (int t0 = p0; t0 < p1; t0 += T) {
-                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
-                        ok = false;
-                        break;
+        for (int s = 0; s < NST; ++s) last_parity[s] = -1;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        int win_b = -1, win_lo = 0;
+        int32_t win_entry = 0;
+        for (int item = blockIdx.x; ok && item < it.n_items; item += gridDim.x) {
+            int b, kvh, s;
+            decode_item(it, item, b, kvh, s);
+            const int Lb = item_len(p, b);
+            const int p0 = s * it.chunk[b];
+            const int p1 = min(Lb, p0 + it.chunk[b]);
+            for (int t0 = p0; t0 < p1; t0 += T) {
+                bool got = true;
+                if (lane == 0)
+                    got = mbar_wait_bounded(empty + stage, phase ^ 1u, p.timeout_ns, abort_flag);
+                if (!__shfl_sync(mask, got, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (!(p.flags & DA_FLAG_TEST_NO_TMA)) {
+                    uint8_t *dst = smem + stage * K::STAGE_BYTES;
+                    if (lane == 0) mbar_arrive_expect_tx(full + stage, K::STAGE_BYTES);
+                    if (!paged) {
+                        if (lane == 0) {
+                            tma_load_4d(dst, &kmap, full + stage, 0, kvh, t0, b, pol);
+                            tma_load_4d(dst + K::TILE_BYTES, &vmap, full + stage, 0, kvh, t0, b,
+                                        pol);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int w = 0; w < NCW; ++w) {
+                            const int pos = t0 + w * K::P;
+                            int blk = p.oob_block, slot = 0;
+                            if (pos < Lb) { // warp-uniform
+                                const int idx = pos / p.block_size;
+                                if (b != win_b || idx < win_lo || idx >= win_lo + 32) {
+                                    win_b = b;
+                                    win_lo = idx;
+                                    win_entry = (idx + lane < p.max_blocks)
+                                                    ? p.block_table[(size_t)b * p.max_blocks +
+                                                                    idx + lane]
+                                                    : p.oob_block;
+                                }
+                                blk = __shfl_sync(0xffffffffu, win_entry, idx - win_lo);
+                                slot = pos - idx * p.block_size;
+                            }
+                            if (lane == 0) {
+                                const int off = w * K::P * D * K::ES;
+                                tma_load_4d(dst + off, &kmap, full + stage, 0, kvh, slot, blk, pol);
+                                tma_load_4d(dst + K::TILE_BYTES + off, &vmap, full + stage, 0, kvh,
+                                            slot, blk, pol);
+                            }
+                        }
                     }
-                    if (!(p.flags & DA_FLAG_TEST_NO_TMA)) {
-                        uint8_t *dst = smem + stage * K::STAGE_BYTES;
-                        mbar_arrive_expect_tx(full + stage, K::STAGE_BYTES);
-                        tma_load_4d(dst, &kmap, full + stage, 0, kvh, t0, b, pol);
-                        tma_load_4d(dst + K::TILE_BYTES, &vmap, full + stage, 0, kvh, t0, b, pol);
 #pragma unroll
-                        for (int x = 0; x < NST; ++x)
-                            if (x == stage) last_parity[x] = (int)phase;
-                    }
-                    if (++stage == NST) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    for (int x = 0; x < NST; ++x)
+                        if (x == stage) last_parity[x] = (int)phase;
+                }
+                if (++stage == NST) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
+        }
+        if (lane == 0) {
             if (!ok) {
                 *abort_flag = 1;
                 atomicCAS(p.status, 0, kStatusTimeoutGqa);
@@ -342,7 +397,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         int b, kvh, s;
         decode_item(it, item, b, kvh, s);
         const int p0 = s * it.chunk[b];
-        const int p1 = min(it.seq_lens[b], p0 + it.chunk[b]);
+        const int p1 = min(item_len(p, b), p0 + it.chunk[b]); // p1 <= p0: an empty item
 
         float acc[G][K::EPL];
         float m[G];

@@ -50,6 +50,14 @@ struct SplitParams {
     float scale_log2;        // scale * log2(e)
     uint64_t timeout_ns;
     int32_t flags;
+    // Optional, read on the device (so that one captured launch serves changing
+    // contexts): current lengths (each clamped to [1, items.seq_lens[b]]), and
+    // a block table for paged caches. NULL: the plan's lengths / contiguous caches.
+    const int32_t *dev_lens;
+    const int32_t *block_table; // [batch][max_blocks] pool block of each block_size positions
+    int32_t max_blocks;
+    int32_t block_size;
+    int32_t oob_block;       // a block coordinate past the pool: TMA fills zeros there
     ItemTable items;
 };
 
@@ -99,6 +107,7 @@ struct GqaConfig {
     int ctas_per_sm;
     int smem_bytes;
     int threads;
+    int rows_per_warp; // P: a consumer warp's rows of a tile (the TMA box of a paged cache)
 };
 bool gqa_config(int kv_dtype, int head_dim, int group, GqaConfig *cfg);
 

@@ -45,10 +45,11 @@ def test_struct_layout_matches_the_c_compiler():
 #include <stddef.h>
 #include "split_kv_decode.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(da_args_t), sizeof(da_plan_t),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(da_args_t), sizeof(da_plan_t),
          offsetof(da_args_t, k_batch_stride), offsetof(da_args_t, scale),
          offsetof(da_plan_t, seq_lens), offsetof(da_plan_t, workspace_bytes),
-         offsetof(da_plan_t, est_cost));
+         offsetof(da_plan_t, est_cost), sizeof(da_dev_t), offsetof(da_dev_t, max_blocks_per_seq),
+         offsetof(da_dev_t, num_blocks), offsetof(da_dev_t, v_block_stride));
   return 0;
 }
 """
@@ -61,7 +62,8 @@ int main(void) {
                                               check=True).stdout.split()]
     want = [ctypes.sizeof(N.DaArgs), ctypes.sizeof(N.DaPlan), N.DaArgs.k_batch_stride.offset,
             N.DaArgs.scale.offset, N.DaPlan.seq_lens.offset, N.DaPlan.workspace_bytes.offset,
-            N.DaPlan.est_cost.offset]
+            N.DaPlan.est_cost.offset, ctypes.sizeof(N.DaDev), N.DaDev.max_blocks_per_seq.offset,
+            N.DaDev.num_blocks.offset, N.DaDev.v_block_stride.offset]
     assert got == want
 
 
@@ -370,3 +372,58 @@ def test_plan_is_cheap_enough_for_every_decode_step(lib):
                                     ctypes.byref(p)) == 0
     per_plan = (time.perf_counter() - t0) / 50
     assert per_plan < 1e-3, per_plan
+
+
+def paged_args(batch=2, hq=16, hkv=4, d=256, block_size=64, max_blocks=8, dt=N.DA_F16):
+    a = args(batch=batch, hq=hq, hkv=hkv, d=d, dt=dt, cap=block_size * max_blocks)
+    return a
+
+
+def dev_struct(block_size=64, max_blocks=8, num_blocks=32, pos_stride=4 * 256, table=1 << 22,
+               lens=1 << 23):
+    d = N.DaDev()
+    d.seq_lens = lens
+    d.block_table = table
+    d.max_blocks_per_seq, d.block_size, d.num_blocks = max_blocks, block_size, num_blocks
+    d.k_block_stride = d.v_block_stride = block_size * pos_stride
+    return d
+
+
+@pytest.mark.parametrize("mutate,status,msg", [
+    (lambda d: setattr(d, "block_size", 24), N.DA_EUNSUPPORTED, "multiple of 16"),
+    (lambda d: setattr(d, "block_size", 0), N.DA_EUNSUPPORTED, "multiple of 16"),
+    (lambda d: setattr(d, "num_blocks", 0), N.DA_EINVAL, "num_blocks"),
+    (lambda d: setattr(d, "k_block_stride", 64 * 1024 - 8), N.DA_EUNSUPPORTED, "block strides"),
+    (lambda d: setattr(d, "max_blocks_per_seq", 4), N.DA_EINVAL, "max_blocks_per_seq"),
+    (lambda d: setattr(d, "block_table", (1 << 22) + 2), N.DA_EINVAL, "block_table"),
+    (lambda d: setattr(d, "seq_lens", (1 << 23) + 1), N.DA_EINVAL, "seq_lens"),
+])
+def test_dev_call_validates_before_launch(lib, mutate, status, msg):
+    a = paged_args()
+    rc, p = plan(lib, a, [500, 300])
+    assert rc == 0
+    d = dev_struct()
+    mutate(d)
+    P = ctypes.c_void_p
+    fake = P(1 << 20)                        # never dereferenced: validation fails first
+    rc = lib.decode_attn_splitk_dev(ctypes.byref(a), ctypes.byref(p), ctypes.byref(d), fake,
+                                    fake, fake, fake, fake, p.workspace_bytes, None)
+    assert rc == status
+    assert msg in lib.decode_attn_last_error().decode()
+
+
+def test_dev_call_refuses_mla_and_a_null_extension(lib):
+    a = mla_args(cap=4096)
+    rc, p = plan(lib, a, [4096])
+    assert rc == 0
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    d = N.DaDev()
+    rc = lib.decode_attn_splitk_dev(ctypes.byref(a), ctypes.byref(p), ctypes.byref(d), fake,
+                                    fake, fake, fake, fake, p.workspace_bytes, None)
+    assert rc == N.DA_EUNSUPPORTED and "GQA" in lib.decode_attn_last_error().decode()
+    a = paged_args()
+    rc, p = plan(lib, a, [500, 300])
+    rc = lib.decode_attn_splitk_dev(ctypes.byref(a), ctypes.byref(p), None, fake, fake, fake,
+                                    fake, fake, p.workspace_bytes, None)
+    assert rc == N.DA_EINVAL
