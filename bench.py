@@ -361,12 +361,98 @@ def main():
     }
     if rank == 0 and not args.no_extra:
         line["e2e"] = measure_e2e(case, q, out_dt, dev, stream, args)
+        if kernel == "gqa_split_kernel":
+            line["graph"] = measure_graph(case, q, k, v, out_dt, dev, flush, args)
+            line["paged"] = {f"block_{bs}": measure_paged(case, q, k, v, out_dt, dev, flush, args, bs)
+                             for bs in (64, 256)}
         line["cpu_baseline"] = cpu_baseline(case)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _timed_steps(launch, flush, steps, stream):
+    """Median CUDA-event time (us) of `launch` over `steps` runs, L2 flushed before each."""
+    import torch
+    ts = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) * 1e3 for a, b in ts)
+
+
+def measure_graph(case, q, k, v, out_dt, dev, flush, args):
+    """The step (split + combine) through decode_attn_splitk_dev with the lengths
+    in device memory, captured once in a CUDA graph and replayed: no host work
+    per step."""
+    import torch
+    from split_kv_decode_gb300 import api as A
+    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
+    p = A.decode_attn_plan(a, case.seq_lens.tolist())
+    ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    out = torch.empty(case.batch, case.n_heads, case.v_dim, dtype=out_dt, device=dev)
+    dev_lens = case.seq_lens.to(dev)
+    d = A.make_dev(seq_lens=dev_lens)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            A.decode_attn_splitk_dev(a, p, d, q, k, v, out, ws, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        A.decode_attn_splitk_dev(a, p, d, q, k, v, out, ws, s)
+    n = max(20, min(args.steps, 200))
+    with torch.cuda.stream(s):
+        us = _timed_steps(g.replay, flush, n, s)
+    return {"value": round(us, 2), "unit": "us/layer-step", "steps": n,
+            "what": "split + combine replayed from one CUDA graph, lengths read on the device"}
+
+
+def measure_paged(case, q, k, v, out_dt, dev, flush, args, block_size):
+    """The same step with the caches scattered into pools of `block_size`-position
+    blocks in a random order, read through a block table (decode_attn_splitk_dev).
+    A tile never spans two blocks, so blocks that the tile does not divide cost
+    partial tiles."""
+    import torch
+    from split_kv_decode_gb300 import api as A
+    B, cap, hkv, dk = k.shape
+    nb = -(-cap // block_size)
+    num_blocks = B * nb
+    order = torch.randperm(num_blocks, generator=torch.Generator().manual_seed(5)).to(dev)
+    table = order.view(B, nb).to(torch.int32).contiguous()
+    kp = torch.empty(num_blocks, block_size, hkv, dk, dtype=k.dtype, device=dev)
+    vp = torch.empty(num_blocks, block_size, hkv, v.shape[3], dtype=v.dtype, device=dev)
+    pad = nb * block_size - cap
+    kpad = torch.nn.functional.pad(k, (0, 0, 0, 0, 0, pad)) if pad else k
+    vpad = torch.nn.functional.pad(v, (0, 0, 0, 0, 0, pad)) if pad else v
+    kp[table.view(-1).long()] = kpad.reshape(B * nb, block_size, hkv, dk)
+    vp[table.view(-1).long()] = vpad.reshape(B * nb, block_size, hkv, v.shape[3])
+    del kpad, vpad
+    a = A.make_paged_args(q, kp, vp, case.scale, nb, out_dtype=out_dt)
+    p = A.decode_attn_plan(a, case.seq_lens.tolist())
+    ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    out = torch.empty(case.batch, case.n_heads, case.v_dim, dtype=out_dt, device=dev)
+    d = A.make_dev(block_table=table, k_pool=kp, v_pool=vp)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        A.decode_attn_splitk_dev(a, p, d, q, kp, vp, out, ws, stream)
+    n = max(20, min(args.steps, 200))
+    us = _timed_steps(lambda: A.decode_attn_splitk_dev(a, p, d, q, kp, vp, out, ws, stream),
+                      flush, n, stream)
+    gbs = case.kv_bytes / (us * 1e-6) / 1e9
+    del kp, vp
+    torch.cuda.empty_cache()
+    return {"value": round(us, 2), "unit": "us/layer-step", "steps": n, "block_size": block_size,
+            "kv_gbs": round(gbs, 1),
+            "what": "split + combine with the caches in a pool of blocks, random block order"}
 
 
 def measure_e2e(case, q_dev, out_dt, dev, stream, args):

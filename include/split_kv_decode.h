@@ -237,7 +237,10 @@ int decode_attn_splitk_noalloc(const da_args_t *args, const da_plan_t *plan, con
  *                 slot * *_pos_stride + kv * *_head_stride + d (elements);
  *                 capacity and the batch strides of da_args_t are not used for
  *                 addressing (capacity must still cover every length).
- *   block_size    positions per block: a positive multiple of 16.
+ *   block_size    positions per block: a positive multiple of 16. A tile of the
+ *                 split kernel never spans two blocks, so blocks of 128 or more
+ *                 positions stream at nearly the contiguous rate; smaller
+ *                 blocks cost partial tiles.
  *   num_blocks    blocks in each pool; table entries must be < num_blocks.
  *   k_block_stride, v_block_stride  elements between blocks (16-byte multiples,
  *                 at least block_size * pos_stride).

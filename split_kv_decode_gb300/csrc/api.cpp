@@ -110,7 +110,6 @@ struct KernelChoice {
     int tile;        // planner quantum: chunks are multiples of it
     int ctas_per_sm;
     int cluster;     // CTAs that share one work item
-    int rows_per_warp; // GQA: rows of a tile per consumer warp
 };
 
 int select_kernel(const da_args_t *a, KernelChoice *kc)
@@ -153,7 +152,6 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
                         "cache strides must be multiples of 16 bytes for TMA tiles");
     kc->kernel = DA_KERNEL_GQA_TMA;
     kc->tile = cfg.tile;
-    kc->rows_per_warp = cfg.rows_per_warp;
     kc->ctas_per_sm = cfg.ctas_per_sm;
     kc->cluster = 1;
     return DA_OK;
@@ -212,7 +210,7 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dt, int D, int hkv,
 }
 
 // 4-D map over a paged pool (d, kv head, slot in block, block) with box
-// (D, 1, rows, 1); a block coordinate past num_blocks reads zeros.
+// (D, 1, rows, 1); slots past block_size and blocks past num_blocks read zeros.
 int encode_pool_map(CUtensorMap *map, const void *base, int dt, int D, int hkv, int block_size,
                     int num_blocks, int64_t head_st, int64_t pos_st, int64_t block_st, int rows)
 {
@@ -296,8 +294,7 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
 }
 
 int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
-                 const void *v, void *ws, cudaStream_t st, const da_dev_t *dev,
-                 int rows_per_warp)
+                 const void *v, void *ws, cudaStream_t st, const da_dev_t *dev)
 {
     if (pl->kernel == DA_KERNEL_MLA_TC) return launch_mla(a, pl, q, k, v, ws, st);
     SplitParams p;
@@ -330,11 +327,11 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
         p.oob_block = dev->num_blocks;
         rc = encode_pool_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, dev->block_size,
                              dev->num_blocks, a->k_head_stride, a->k_pos_stride,
-                             dev->k_block_stride, rows_per_warp);
+                             dev->k_block_stride, pl->tile);
         if (rc) return rc;
         rc = encode_pool_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, dev->block_size,
                              dev->num_blocks, a->v_head_stride, a->v_pos_stride,
-                             dev->v_block_stride, rows_per_warp);
+                             dev->v_block_stride, pl->tile);
         if (rc) return rc;
     } else {
         rc = encode_cache_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, a->capacity,
@@ -485,7 +482,7 @@ int decode_attn_splitk_ex(const da_args_t *a, const da_plan_t *plan, const float
     if (pre != cudaSuccess)
         return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = launch_split(a, plan, q, k, v, ws, st, nullptr, kc.rows_per_warp);
+    rc = launch_split(a, plan, q, k, v, ws, st, nullptr);
     if (rc) return rc;
     if (a->flags & DA_FLAG_NO_COMBINE) return DA_OK;
     return launch_combine_phase(a, plan, ws, out, st);
@@ -538,7 +535,7 @@ int decode_attn_splitk_dev(const da_args_t *a, const da_plan_t *plan, const da_d
     if (pre != cudaSuccess)
         return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = launch_split(a, plan, q, k, v, ws, st, dev, kc.rows_per_warp);
+    rc = launch_split(a, plan, q, k, v, ws, st, dev);
     if (rc) return rc;
     if (a->flags & DA_FLAG_NO_COMBINE) return DA_OK;
     return launch_combine_phase(a, plan, ws, out, st);

@@ -55,7 +55,6 @@ template <typename DT, int D, int G> struct GqaInst {
         c->ctas_per_sm = 1;
         c->smem_bytes = Ker::SMEM_ALLOC;
         c->threads = Ker::THREADS;
-        c->rows_per_warp = Ker::P;
     }
     static cudaError_t launch(int grid, cudaStream_t st, const CUtensorMap &km,
                               const CUtensorMap &vm, const SplitParams &p)

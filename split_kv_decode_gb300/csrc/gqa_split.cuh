@@ -31,6 +31,7 @@
 // before the max and skipped in the PV update, so whatever the cache holds
 // there (never-written memory, NaN) cannot leak in.
 #pragma once
+#include <climits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -180,6 +181,23 @@ __device__ __forceinline__ int item_len(const SplitParams &p, int b)
     return p.dev_lens ? max(1, min(__ldg(p.dev_lens + b), L)) : L;
 }
 
+// A tile is T rows, cut at the item's end and, for a paged cache, at the end
+// of its block (a tile never spans two blocks). The next block boundary is
+// tracked from the item's start, so a tile costs no division; contiguous caches
+// have no boundary.
+__device__ __forceinline__ int first_block_end(const SplitParams &p, int p0)
+{
+    return p.block_table ? (p0 / p.block_size + 1) * p.block_size : INT_MAX;
+}
+
+template <int T>
+__device__ __forceinline__ int tile_end(int t0, int p1, int &bend, int bs)
+{
+    const int e = min(min(t0 + T, p1), bend);
+    if (e == bend) bend += bs;
+    return e;
+}
+
 template <int X> __host__ __device__ constexpr int align_up(int v) { return (v + X - 1) / X * X; }
 
 // LPR (lanes per row) is 32, or 16 when a row is only 256 bytes (D = 128 in a
@@ -262,9 +280,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         // Lane 0 waits on the stage barriers and issues the copies. For paged
         // caches the whole warp walks the items and tiles: the lanes hold a
         // window of 32 consecutive block-table entries of the current sequence
-        // (one coalesced load), and each P-row group of a tile -- one consumer
-        // warp's rows, never straddling a block -- is its own TMA box. For
-        // contiguous caches lane 0 walks alone (one box per tile).
+        // (one coalesced load); a tile never spans two blocks (tile_end), so a
+        // tile is still one TMA box of T rows, whose rows past the block are
+        // read as zeros and masked. For contiguous caches lane 0 walks alone.
         const bool paged = p.block_table != nullptr;
         if (!paged && lane != 0) return;
         const unsigned mask = paged ? 0xffffffffu : 1u;
@@ -287,7 +305,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             const int Lb = item_len(p, b);
             const int p0 = s * it.chunk[b];
             const int p1 = min(Lb, p0 + it.chunk[b]);
-            for (int t0 = p0; t0 < p1; t0 += T) {
+            int bend = first_block_end(p, p0);
+            for (int t0 = p0, t1; t0 < p1; t0 = t1) {
+                t1 = tile_end<T>(t0, p1, bend, p.block_size);
                 bool got = true;
                 if (lane == 0)
                     got = mbar_wait_bounded(empty + stage, phase ^ 1u, p.timeout_ns, abort_flag);
@@ -297,38 +317,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                 }
                 if (!(p.flags & DA_FLAG_TEST_NO_TMA)) {
                     uint8_t *dst = smem + stage * K::STAGE_BYTES;
-                    if (lane == 0) mbar_arrive_expect_tx(full + stage, K::STAGE_BYTES);
-                    if (!paged) {
-                        if (lane == 0) {
-                            tma_load_4d(dst, &kmap, full + stage, 0, kvh, t0, b, pol);
-                            tma_load_4d(dst + K::TILE_BYTES, &vmap, full + stage, 0, kvh, t0, b,
-                                        pol);
+                    int c2 = t0, c3 = b; // contiguous: (position, sequence)
+                    if (paged) {         // paged: (slot in block, block)
+                        const int idx = t0 / p.block_size;
+                        if (b != win_b || idx < win_lo || idx >= win_lo + 32) {
+                            win_b = b;
+                            win_lo = idx;
+                            win_entry = (idx + lane < p.max_blocks)
+                                            ? p.block_table[(size_t)b * p.max_blocks + idx + lane]
+                                            : p.oob_block;
                         }
-                    } else {
-#pragma unroll 1
-                        for (int w = 0; w < NCW; ++w) {
-                            const int pos = t0 + w * K::P;
-                            int blk = p.oob_block, slot = 0;
-                            if (pos < Lb) { // warp-uniform
-                                const int idx = pos / p.block_size;
-                                if (b != win_b || idx < win_lo || idx >= win_lo + 32) {
-                                    win_b = b;
-                                    win_lo = idx;
-                                    win_entry = (idx + lane < p.max_blocks)
-                                                    ? p.block_table[(size_t)b * p.max_blocks +
-                                                                    idx + lane]
-                                                    : p.oob_block;
-                                }
-                                blk = __shfl_sync(0xffffffffu, win_entry, idx - win_lo);
-                                slot = pos - idx * p.block_size;
-                            }
-                            if (lane == 0) {
-                                const int off = w * K::P * D * K::ES;
-                                tma_load_4d(dst + off, &kmap, full + stage, 0, kvh, slot, blk, pol);
-                                tma_load_4d(dst + K::TILE_BYTES + off, &vmap, full + stage, 0, kvh,
-                                            slot, blk, pol);
-                            }
-                        }
+                        c3 = __shfl_sync(0xffffffffu, win_entry, idx - win_lo);
+                        c2 = t0 - idx * p.block_size;
+                    }
+                    // rows of the box past the block (or the pool) are read as zeros
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full + stage, K::STAGE_BYTES);
+                        tma_load_4d(dst, &kmap, full + stage, 0, kvh, c2, c3, pol);
+                        tma_load_4d(dst + K::TILE_BYTES, &vmap, full + stage, 0, kvh, c2, c3, pol);
                     }
 #pragma unroll
                     for (int x = 0; x < NST; ++x)
@@ -414,7 +420,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         __syncwarp();
 
         bool aborted = false;
-        for (int t0 = p0; t0 < p1; t0 += T) {
+        int bend = first_block_end(p, p0);
+        for (int t0 = p0, t1; t0 < p1; t0 = t1) {
+            t1 = tile_end<T>(t0, p1, bend, p.block_size);
             if (!mbar_wait_bounded(full + stage, phase, p.timeout_ns, abort_flag)) {
                 aborted = true;
                 break;
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             const DT *Vt = reinterpret_cast<const DT *>(smem + stage * K::STAGE_BYTES +
                                                         K::TILE_BYTES) +
                            warp * K::P * D;
-            const int valid = min(min(T, p1 - t0) - warp * K::P, K::P);
+            const int valid = min(t1 - t0 - warp * K::P, K::P);
             if (valid > 0) {
                 // ---- scores: P rows x G heads, partial over this lane's elements;
                 // step r2 reads row r2 * RPW + half

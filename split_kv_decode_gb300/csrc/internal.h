@@ -107,7 +107,6 @@ struct GqaConfig {
     int ctas_per_sm;
     int smem_bytes;
     int threads;
-    int rows_per_warp; // P: a consumer warp's rows of a tile (the TMA box of a paged cache)
 };
 bool gqa_config(int kv_dtype, int head_dim, int group, GqaConfig *cfg);
 
