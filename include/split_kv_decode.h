@@ -261,9 +261,10 @@ typedef struct {
  * device and, optionally, paged K/V caches (da_dev_t). It makes no host-side
  * decision that depends on the current lengths, so a launch captured in a CUDA
  * graph stays valid while the lengths grow up to the plan's. Splits that start
- * past a sequence's current length write neutral partials (l = 0). GQA/MQA
- * kernel only: an MLA shape gets DA_EUNSUPPORTED. Validation before any launch
- * as in decode_attn_splitk_ex, plus the da_dev_t rules above (DA_EINVAL /
+ * past a sequence's current length write neutral partials (l = 0). Both
+ * kernels: for the MLA shape the pool holds the latent rows once (k_cache ==
+ * v_cache, equal block strides). Validation before any launch as in
+ * decode_attn_splitk_ex, plus the da_dev_t rules above (DA_EINVAL /
  * DA_EUNSUPPORTED).
  */
 int decode_attn_splitk_dev(const da_args_t *args, const da_plan_t *plan, const da_dev_t *dev,

@@ -129,15 +129,17 @@ def decode_attn_splitk_noalloc(args: N.DaArgs, plan: N.DaPlan, q: torch.Tensor,
 
 
 def make_paged_args(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, scale: float,
-                    max_blocks_per_seq: int, *, out_dtype: torch.dtype = torch.float32,
-                    force_splits: int = 0, flags: int = 0, timeout_us: int = 0) -> N.DaArgs:
+                    max_blocks_per_seq: int, *, v_dim: Optional[int] = None,
+                    out_dtype: torch.dtype = torch.float32, force_splits: int = 0,
+                    flags: int = 0, timeout_us: int = 0) -> N.DaArgs:
     """da_args_t for paged pools [num_blocks, block_size, Hkv, D]: the position and
     head strides come from the pools, the capacity is max_blocks_per_seq *
-    block_size (the batch strides are not used for addressing)."""
+    block_size (the batch strides are not used for addressing). For MLA pass the
+    latent pool as both pools and v_dim."""
     if k_pool.dim() != 4 or v_pool.dim() != 4:
         raise ValueError("pools must be [num_blocks, block_size, Hkv, D]")
-    a = make_args(q, k_pool, v_pool, scale, out_dtype=out_dtype, force_splits=force_splits,
-                  flags=flags, timeout_us=timeout_us)
+    a = make_args(q, k_pool, v_pool, scale, v_dim=v_dim, out_dtype=out_dtype,
+                  force_splits=force_splits, flags=flags, timeout_us=timeout_us)
     a.capacity = int(max_blocks_per_seq) * k_pool.shape[1]
     return a
 

@@ -262,7 +262,7 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
-               const void *v, void *ws, cudaStream_t st)
+               const void *v, void *ws, cudaStream_t st, const da_dev_t *dev)
 {
     (void)v; // the same buffer as k (checked with the arguments)
     MlaParams p;
@@ -288,6 +288,15 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
         p.items.split_base[b] = pl->split_base[b];
     }
     p.items.split_base[a->batch] = pl->total_splits;
+    if (dev) {
+        p.dev_lens = dev->seq_lens;
+        if (dev->block_table) {
+            p.block_table = dev->block_table;
+            p.max_blocks = dev->max_blocks_per_seq;
+            p.block_size = dev->block_size;
+            p.block_stride = dev->k_block_stride;
+        }
+    }
     cudaError_t e = launch_mla_split(pl->grid, st, p);
     if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
     return DA_OK;
@@ -296,7 +305,7 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
 int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
                  const void *v, void *ws, cudaStream_t st, const da_dev_t *dev)
 {
-    if (pl->kernel == DA_KERNEL_MLA_TC) return launch_mla(a, pl, q, k, v, ws, st);
+    if (pl->kernel == DA_KERNEL_MLA_TC) return launch_mla(a, pl, q, k, v, ws, st, dev);
     SplitParams p;
     std::memset(&p, 0, sizeof p);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -498,9 +507,11 @@ int decode_attn_splitk_dev(const da_args_t *a, const da_plan_t *plan, const da_d
     KernelChoice kc;
     rc = check_plan(a, plan, &kc);
     if (rc) return rc;
-    if (kc.kernel != DA_KERNEL_GQA_TMA)
+    if (kc.kernel == DA_KERNEL_MLA_TC && dev->block_table &&
+        (dev->v_block_stride != dev->k_block_stride || (dev->k_block_stride * 4) % 16))
         return fail(DA_EUNSUPPORTED, "args",
-                    "device lengths and paged caches are served by the GQA kernel only");
+                    "MLA latent pools: one pool for keys and values (equal block strides, "
+                    "16-byte multiples)");
     rc = check_buffers(kc.kernel, q, k, v, out);
     if (rc) return rc;
     if (dev->seq_lens && !aligned(dev->seq_lens, 4))

@@ -2,7 +2,8 @@
 // (sequence, query head) row,
 //     m = max_i m_i,  w_i = exp(m_i - m),  out = sum_i w_i acc_i / sum_i w_i l_i
 // ("Attention at 128k: Split Over Context", §2; aprender issue 3725 design
-// note §2). A neutral partial (l = 0, m = -1e30) gets weight 0.
+// note §2). A neutral partial (l = 0) gets weight 0 and its acc is not used
+// (an empty split of the MLA kernel leaves it unwritten).
 //
 // One CTA per (query head, sequence, 128 value columns); 8 warps. Each warp
 // loads the acc vectors of its own splits (s = warp, warp + 8, ...) first,
@@ -97,12 +98,16 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
     for (int i = 0; i < kCombinePrefetch; ++i) {
         const int sp = warp + kCombineWarps * i;
-        if (sp < S) fma4(a, ex2((__ldg(&ml[(size_t)sp * p.n_heads].x) - M) * kLog2e), pv[i]);
+        if (sp < S) {
+            const float2 x = __ldg(&ml[(size_t)sp * p.n_heads]);
+            if (x.y > 0.f) fma4(a, ex2((x.x - M) * kLog2e), pv[i]);
+        }
     }
     for (int sp = warp + kCombineWarps * kCombinePrefetch; sp < S; sp += kCombineWarps) {
-        const float w = ex2((__ldg(&ml[(size_t)sp * p.n_heads].x) - M) * kLog2e);
-        if (live)
-            fma4(a, w, __ldg(reinterpret_cast<const float4 *>(acc + (size_t)sp * acc_stride)));
+        const float2 x = __ldg(&ml[(size_t)sp * p.n_heads]);
+        if (live && x.y > 0.f)
+            fma4(a, ex2((x.x - M) * kLog2e),
+                 __ldg(reinterpret_cast<const float4 *>(acc + (size_t)sp * acc_stride)));
     }
     part[warp][lane] = a;
     __syncthreads();

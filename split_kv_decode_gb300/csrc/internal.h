@@ -73,6 +73,14 @@ struct MlaParams {
     float scale_log2;        // scale * log2(e)
     uint64_t timeout_ns;
     int32_t flags;
+    // Optional, as for the GQA kernel: current lengths read on the device, and
+    // a block table over a pool of latent rows (row (block, slot) at
+    // cache + block * block_stride + slot * pos_stride).
+    const int32_t *dev_lens;
+    const int32_t *block_table;
+    int32_t max_blocks;
+    int32_t block_size;
+    int64_t block_stride;
     ItemTable items;         // n_kv_heads = 1
 };
 

@@ -130,8 +130,11 @@ struct Item {
     int b, s, p0, p1, ntiles;
 };
 
-__device__ __forceinline__ Item get_item(const ItemTable &it, int item)
+// item -> (sequence, split, positions [p0, p1), tiles). With lengths read on
+// the device a split may start past its sequence's current end: an empty item.
+__device__ __forceinline__ Item get_item(const MlaParams &p, int item)
 {
+    const ItemTable &it = p.items;
     Item x;
     int lo = 0, hi = it.batch - 1;
     while (lo < hi) {
@@ -142,26 +145,38 @@ __device__ __forceinline__ Item get_item(const ItemTable &it, int item)
     x.b = lo;
     x.s = item - it.split_base[lo];
     x.p0 = x.s * it.chunk[lo];
-    x.p1 = min(it.seq_lens[lo], x.p0 + it.chunk[lo]);
-    x.ntiles = (x.p1 - x.p0 + kTile - 1) / kTile;
+    int L = it.seq_lens[lo];
+    if (p.dev_lens) L = max(1, min(__ldg(p.dev_lens + lo), L));
+    x.p1 = min(L, x.p0 + it.chunk[lo]);
+    x.ntiles = x.p1 > x.p0 ? (x.p1 - x.p0 + kTile - 1) / kTile : 0;
     return x;
 }
 
 // The (item, tile, chunk) units of a cluster's work, in order; gt counts tiles.
+// Empty items have no tiles and are skipped.
 struct Cursor {
     int item, t, c, gt;
     Item x;
     bool done;
-    __device__ __forceinline__ void start(const ItemTable &it, int first)
+    __device__ __forceinline__ void seek(const MlaParams &p, int stride)
+    {
+        for (;;) {
+            done = item >= p.items.n_items;
+            if (done) return;
+            x = get_item(p, item);
+            if (x.ntiles > 0) return;
+            item += stride;
+        }
+    }
+    __device__ __forceinline__ void start(const MlaParams &p, int first, int stride)
     {
         item = first;
         t = 0;
         c = 0;
         gt = 0;
-        done = item >= it.n_items;
-        if (!done) x = get_item(it, item);
+        seek(p, stride);
     }
-    __device__ __forceinline__ void next(const ItemTable &it, int stride)
+    __device__ __forceinline__ void next(const MlaParams &p, int stride)
     {
         if (++c == kChunks) {
             c = 0;
@@ -169,15 +184,14 @@ struct Cursor {
             if (++t == x.ntiles) {
                 t = 0;
                 item += stride;
-                done = item >= it.n_items;
-                if (!done) x = get_item(it, item);
+                seek(p, stride);
             }
         }
     }
-    __device__ __forceinline__ void next_tile(const ItemTable &it, int stride)
+    __device__ __forceinline__ void next_tile(const MlaParams &p, int stride)
     {
         c = kChunks - 1;
-        next(it, stride);
+        next(p, stride);
     }
 };
 
@@ -260,11 +274,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float4 ld[kChunks][2];
         auto row_src = [&](const Cursor &u) {
             const int pos = min(u.x.p0 + u.t * kTile + (int)row0 + trow, u.x.p1 - 1);
+            if (p.block_table) { // paged: the row's block from the table
+                const int idx = pos / p.block_size;
+                const int blk = __ldg(p.block_table + (size_t)u.x.b * p.max_blocks + idx);
+                return reinterpret_cast<const float4 *>(
+                    p.cache + (size_t)blk * p.block_stride +
+                    (size_t)(pos - idx * p.block_size) * p.pos_stride + q8 * 4);
+            }
             return reinterpret_cast<const float4 *>(p.cache + (size_t)u.x.b * p.batch_stride +
                                                     (size_t)pos * p.pos_stride + q8 * 4);
         };
         Cursor cur;
-        cur.start(it, cluster);
+        cur.start(p, cluster, nclusters);
         if (!cur.done) {
             const float4 *src = row_src(cur);
 #pragma unroll
@@ -275,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         while (!cur.done) {
             Cursor nxt = cur;
-            nxt.next_tile(it, nclusters);
+            nxt.next_tile(p, nclusters);
             const int slot = cur.gt & 1;
             if (cur.t == 0) {
                 // a new item: this CTA's heads of q (scale and log2 e folded in),
@@ -348,8 +369,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // whichever is ready, so PV(t) goes out as soon as P(t) is written
             // and QK(t+1) as soon as the tile is in, in either order.
             Cursor qk, pv;
-            qk.start(it, cluster);
-            pv.start(it, cluster);
+            qk.start(p, cluster, nclusters);
+            pv.start(p, cluster, nclusters);
             int items_pv = 0;
             uint64_t last = global_ns();
             while (!pv.done) {
@@ -382,7 +403,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tc_commit(bar + B_PVDONE);
                         if (pv.t == pv.x.ntiles - 1) tc_commit(bar + B_OREADY);
                         progress = true;
-                        pv.next_tile(it, nclusters);
+                        pv.next_tile(p, nclusters);
                     }
                 }
                 if (!qk.done) {
@@ -421,7 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 tc_commit(bar + B_QFREE);
                                 q_ready = false;
                             }
-                            qk.next_tile(it, nclusters);
+                            qk.next_tile(p, nclusters);
                         }
                     }
                 }
@@ -448,7 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             int gt = 0;
             for (int item = cluster; ok && item < it.n_items; item += nclusters) {
-                const Item x = get_item(it, item);
+                const Item x = get_item(p, item);
                 for (int t = 0; t < x.ntiles; ++t, ++gt) {
                     const int slot = gt & 1;
                     for (int g = 0; g < kGroups && ok; ++g) {
@@ -487,7 +508,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int gt = 0;
         bool ab = false;
         for (int item = cluster; !ab && item < it.n_items; item += nclusters) {
-            const Item x = get_item(it, item);
+            const Item x = get_item(p, item);
+            if (x.ntiles == 0) { // an empty item: a neutral partial, no MMA took part
+                const size_t row0 = ((size_t)it.split_base[x.b] + x.s) * p.n_heads + hbase;
+                if (owner) p.ml[row0 + h] = make_float2(kNeutralM, 0.f);
+                continue;
+            }
             float m = -INFINITY, l = 0.f;
             for (int t = 0; t < x.ntiles; ++t, ++gt) {
                 const int slot = gt & 1;

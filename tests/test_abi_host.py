@@ -412,16 +412,21 @@ def test_dev_call_validates_before_launch(lib, mutate, status, msg):
     assert msg in lib.decode_attn_last_error().decode()
 
 
-def test_dev_call_refuses_mla_and_a_null_extension(lib):
+def test_dev_call_needs_one_latent_pool_for_mla_and_an_extension(lib):
     a = mla_args(cap=4096)
     rc, p = plan(lib, a, [4096])
     assert rc == 0
     P = ctypes.c_void_p
-    fake = P(1 << 20)
-    d = N.DaDev()
+    fake, other = P(1 << 20), P(1 << 21)
+    d = dev_struct(block_size=64, max_blocks=64, pos_stride=576)
+    d.v_block_stride = d.k_block_stride + 576 * 4
     rc = lib.decode_attn_splitk_dev(ctypes.byref(a), ctypes.byref(p), ctypes.byref(d), fake,
                                     fake, fake, fake, fake, p.workspace_bytes, None)
-    assert rc == N.DA_EUNSUPPORTED and "GQA" in lib.decode_attn_last_error().decode()
+    assert rc == N.DA_EUNSUPPORTED and "one pool" in lib.decode_attn_last_error().decode()
+    d = dev_struct(block_size=64, max_blocks=64, pos_stride=576)
+    rc = lib.decode_attn_splitk_dev(ctypes.byref(a), ctypes.byref(p), ctypes.byref(d), fake,
+                                    fake, other, fake, fake, p.workspace_bytes, None)
+    assert rc == N.DA_EUNSUPPORTED and "same buffer" in lib.decode_attn_last_error().decode()
     a = paged_args()
     rc, p = plan(lib, a, [500, 300])
     rc = lib.decode_attn_splitk_dev(ctypes.byref(a), ctypes.byref(p), None, fake, fake, fake,

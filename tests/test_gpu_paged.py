@@ -190,3 +190,104 @@ def test_paged_decode_steps_replayed_from_one_cuda_graph():
         torch.cuda.synchronize()
         check_against_oracle(case, lens, out.double().cpu().numpy())
     assert lens == final
+
+
+# ---------------------------------------------------------------------------
+# MLA: one latent pool (values are the first 512 columns of each row)
+# ---------------------------------------------------------------------------
+MLA_F32_BAR, MLA_SHORT_BAR = 2e-4, 5e-3   # as in test_gpu_mla: bf16 operands
+
+
+def mla_case(lens, seed):
+    return W.make_case("mla", batch=len(lens), n_heads=96, n_kv_heads=1, head_dim=576,
+                       v_dim=512, seq_lens=lens, kv_dtype="f32", scale=1 / math.sqrt(576.0),
+                       seed=seed, std=0.5, shared_kv=True)
+
+
+def mla_pool(case, block_size, seed):
+    B, cap = case.k.shape[:2]
+    nb_seq = -(-cap // block_size)
+    num_blocks = B * nb_seq + 3
+    order = torch.randperm(num_blocks, generator=torch.Generator().manual_seed(seed))
+    pool = torch.full((num_blocks, block_size, 1, 576), float("nan"))
+    table = torch.full((B, nb_seq + 1), int(order[-1]), dtype=torch.int32)
+    i = 0
+    for b in range(B):
+        for j in range(nb_seq):
+            blk = int(order[i])
+            i += 1
+            n = min(block_size, cap - j * block_size)
+            pool[blk, :n] = case.k[b, j * block_size:j * block_size + n]
+            table[b, j] = blk
+    return pool, table
+
+
+def run_mla_dev(case, lens_now, pool=None, table=None):
+    q = case.q.cuda()
+    dev_lens = torch.tensor(lens_now, dtype=torch.int32, device="cuda")
+    if pool is None:
+        k = case.k.cuda()
+        a = A.make_args(q, k, k, case.scale, v_dim=512)
+        d = A.make_dev(seq_lens=dev_lens)
+    else:
+        k, tab = pool.cuda(), table.cuda()
+        a = A.make_paged_args(q, k, k, case.scale, tab.shape[1], v_dim=512)
+        d = A.make_dev(seq_lens=dev_lens, block_table=tab, k_pool=k, v_pool=k)
+    p = A.decode_attn_plan(a, case.seq_lens.tolist())
+    assert p.kernel == N.DA_KERNEL_MLA_TC
+    ws = A.new_workspace(p)
+    ws.fill_(0xFF)
+    out = torch.empty(case.batch, 96, 512, device="cuda")
+    A.decode_attn_splitk_dev(a, p, d, q, k, k, out, ws)
+    torch.cuda.synchronize()
+    A.decode_attn_device_status(ws)
+    return out.double().cpu().numpy()
+
+
+def check_mla(case, lens_now, got):
+    ref_case = at_lengths(case, lens_now)
+    worst, rel = errors(ref_case, got, oracle_rows(ref_case))
+    bar = MLA_F32_BAR if min(lens_now) >= 4096 else MLA_SHORT_BAR
+    assert np.all(np.isfinite(got))
+    assert worst <= bar, (worst, rel)
+
+
+def test_mla_device_lengths_leave_empty_splits_neutral():
+    case = mla_case([12000, 5000], seed=640)
+    # the plan cuts 12000 positions into many splits; at 4500 most of them are empty
+    for lens_now in ([4500, 5000], [12000, 4096], [1, 5000]):
+        check_mla(case, lens_now, run_mla_dev(case, lens_now))
+
+
+@pytest.mark.parametrize("block_size", [16, 64, 128])
+def test_mla_paged_latent_pool(block_size):
+    case = mla_case([6000, 4500], seed=650 + block_size)
+    pool, table = mla_pool(case, block_size, seed=block_size)
+    check_mla(case, [6000, 4500], run_mla_dev(case, [6000, 4500], pool, table))
+    check_mla(case, [4200, 4096], run_mla_dev(case, [4200, 4096], pool, table))
+
+
+def test_mla_paged_launch_replayed_from_a_cuda_graph():
+    case = mla_case([8000], seed=660)
+    pool, table = mla_pool(case, 64, seed=1)
+    q = case.q.cuda()
+    k, tab = pool.cuda(), table.cuda()
+    a = A.make_paged_args(q, k, k, case.scale, tab.shape[1], v_dim=512)
+    p = A.decode_attn_plan(a, [8000])
+    ws = A.new_workspace(p)
+    out = torch.empty(1, 96, 512, device="cuda")
+    dev_lens = torch.tensor([5000], dtype=torch.int32, device="cuda")
+    d = A.make_dev(seq_lens=dev_lens, block_table=tab, k_pool=k, v_pool=k)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        A.decode_attn_splitk_dev(a, p, d, q, k, k, out, ws, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        A.decode_attn_splitk_dev(a, p, d, q, k, k, out, ws, s)
+    for L in (5000, 6500, 8000, 4096):
+        dev_lens.fill_(L)
+        g.replay()
+        torch.cuda.synchronize()
+        check_mla(case, [L], out.double().cpu().numpy())
