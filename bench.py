@@ -48,6 +48,18 @@ KERNEL = {"mla96_f32_L131072": ("mla_split_kernel", "bf16")}
 DEFAULT_KERNEL = ("gqa_split_kernel", "f32")
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over the ranks of the default process group (x itself
+    on a single rank): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
         int(os.environ.get("LOCAL_RANK", 0))
@@ -326,11 +338,7 @@ def main():
 
     step_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(args.steps)]
     split_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(args.steps)]
-    total_us = sum(step_us)
-    if world > 1:
-        t = torch.tensor([total_us], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_us = float(t.item())
+    total_us = max_over_ranks(sum(step_us), dev)
     value = total_us / (args.steps * world)                # µs per layer-step, whole job
     split_mean = statistics.mean(split_us)
     peak, peak_src = load_peaks()

@@ -165,6 +165,22 @@ int decode_attn_combine(const da_args_t *args, const da_plan_t *plan, const void
                         void *out, da_stream_t stream);
 
 /*
+ * decode_attn_combine_ranks -- the combine of a context-parallel step (DCP:
+ * "The Kernel Level: Attention and MoE", the split-KV section: the same merge
+ * across GPUs that hold slices of the context). n_ranks ranks each ran
+ * decode_attn_splitk_dev with DA_FLAG_NO_COMBINE and the SAME plan on their
+ * own slice of every sequence (the plan made for the longest slice, the slice
+ * lengths in seq_lens); `workspaces` holds their workspaces back to back, rank
+ * r at r * plan->workspace_bytes (e.g. after an all-gather). Merges, for every
+ * (sequence, query head), the partials of all ranks and splits:
+ *   m = max m_ri, out = sum e^{m_ri - m} acc_ri / sum e^{m_ri - m} l_ri.
+ * n_ranks = 1 is decode_attn_combine. One kernel launch on `stream`.
+ */
+int decode_attn_combine_ranks(const da_args_t *args, const da_plan_t *plan,
+                              const void *workspaces, int n_ranks, void *out,
+                              da_stream_t stream);
+
+/*
  * decode_attn_splitk -- the short form: batch 1, f32 q/K/V/out,
  * v_dim = head_dim, caches laid out [seq_len][n_kv_heads][head_dim]
  * contiguous, scale given.

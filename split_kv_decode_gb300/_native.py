@@ -72,6 +72,8 @@ SIGNATURES = {
                                              _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "decode_attn_combine": (ctypes.c_int, [ctypes.POINTER(DaArgs), ctypes.POINTER(DaPlan), _P,
                                            _P, _P]),
+    "decode_attn_combine_ranks": (ctypes.c_int, [ctypes.POINTER(DaArgs), ctypes.POINTER(DaPlan),
+                                                 _P, ctypes.c_int, _P, _P]),
     "decode_attn_splitk": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_float, _P, _P]),
     "decode_attn_device_status": (ctypes.c_int, [_P, _P]),

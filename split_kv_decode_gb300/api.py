@@ -106,6 +106,15 @@ def decode_attn_combine(args: N.DaArgs, plan: N.DaPlan, workspace: torch.Tensor,
                                         _ptr(out), _stream(stream)))
 
 
+def decode_attn_combine_ranks(args: N.DaArgs, plan: N.DaPlan, workspaces: torch.Tensor,
+                              n_ranks: int, out: torch.Tensor, stream=None) -> None:
+    """Merge the partials of n_ranks ranks that ran the same plan on their slices
+    of the context; `workspaces` holds their workspaces back to back."""
+    _check(N.load().decode_attn_combine_ranks(ctypes.byref(args), ctypes.byref(plan),
+                                              _ptr(workspaces), int(n_ranks), _ptr(out),
+                                              _stream(stream)))
+
+
 def decode_attn_splitk(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                        seq_lens: Sequence[int], n_heads: int, n_kv_heads: int, head_dim: int,
                        scale: float, out: torch.Tensor, stream=None) -> None:

@@ -366,10 +366,13 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
 }
 
 int launch_combine_phase(const da_args_t *a, const da_plan_t *pl, const void *ws, void *out,
-                         cudaStream_t st)
+                         cudaStream_t st, int n_ranks = 1)
 {
     CombineParams c;
     std::memset(&c, 0, sizeof c);
+    c.n_ranks = n_ranks;
+    c.rank_ml = pl->workspace_bytes / 8; // float2 elements between ranks' workspaces
+    c.rank_acc = pl->workspace_bytes / 4;
     const uint8_t *w = static_cast<const uint8_t *>(ws);
     c.ml = reinterpret_cast<const float2 *>(w + ws_ml_offset());
     c.acc = reinterpret_cast<const float *>(w + ws_acc_offset(pl->total_splits, a->n_heads));
@@ -550,6 +553,26 @@ int decode_attn_splitk_dev(const da_args_t *a, const da_plan_t *plan, const da_d
     if (rc) return rc;
     if (a->flags & DA_FLAG_NO_COMBINE) return DA_OK;
     return launch_combine_phase(a, plan, ws, out, st);
+}
+
+int decode_attn_combine_ranks(const da_args_t *a, const da_plan_t *plan, const void *ws,
+                              int n_ranks, void *out, da_stream_t stream)
+{
+    int rc = check_args(a);
+    if (rc) return rc;
+    KernelChoice kc;
+    rc = check_plan(a, plan, &kc);
+    if (rc) return rc;
+    if (n_ranks < 1 || n_ranks > 4096)
+        return fail(DA_EINVAL, "args", "n_ranks %d outside [1, 4096]", n_ranks);
+    if (!ws || !aligned(ws, 256)) return fail(DA_EINVAL, "args", "workspaces misaligned or NULL");
+    if (!out || !aligned(out, 16)) return fail(DA_EINVAL, "args", "out misaligned or NULL");
+    cudaError_t pre = cudaGetLastError();
+    if (pre != cudaSuccess)
+        return fail(DA_ECUDA, "before combine", "pending CUDA error: %s",
+                    cudaGetErrorString(pre));
+    return launch_combine_phase(a, plan, ws, out, reinterpret_cast<cudaStream_t>(stream),
+                                n_ranks);
 }
 
 int decode_attn_combine(const da_args_t *a, const da_plan_t *plan, const void *ws, void *out,

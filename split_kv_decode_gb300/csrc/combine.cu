@@ -5,6 +5,9 @@
 // note §2). A neutral partial (l = 0) gets weight 0 and its acc is not used
 // (an empty split of the MLA kernel leaves it unwritten).
 //
+// For a context-parallel step the partials of several ranks are merged the
+// same way: the (rank, split) pairs of a row are one list.
+//
 // One CTA per (query head, sequence, 128 value columns); 8 warps. Each warp
 // loads the acc vectors of its own splits (s = warp, warp + 8, ...) first,
 // then computes m and l over all splits itself (lanes stride the splits, warp
@@ -65,30 +68,36 @@ __global__ void __launch_bounds__(kCombineThreads)
     const int h = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.n_splits[b];
+    const int SR = S * p.n_ranks;                            // (rank, split) pairs
     const size_t slot0 = (size_t)p.split_base[b];
     const int col = blockIdx.z * kCombineCols + lane * 4;
     const bool live = col < p.v_dim;
-    const float2 *ml = p.ml + slot0 * p.n_heads + h;         // stride n_heads per split
-    const float *acc = p.acc + (slot0 * p.n_heads + h) * p.v_dim + col;
-    const size_t acc_stride = (size_t)p.n_heads * p.v_dim;
+    // pair i = r * S + s: rank r's split s
+    auto ml_of = [&](int i) {
+        const int r = i / S;
+        return __ldg(p.ml + r * p.rank_ml + (slot0 + (i - r * S)) * p.n_heads + h);
+    };
+    auto acc_of = [&](int i) {
+        const int r = i / S;
+        return __ldg(reinterpret_cast<const float4 *>(
+            p.acc + r * p.rank_acc + ((slot0 + (i - r * S)) * p.n_heads + h) * p.v_dim + col));
+    };
 
-    // acc vectors of this warp's first splits, in flight while m and l are formed
+    // acc vectors of this warp's first pairs, in flight while m and l are formed
     float4 pv[kCombinePrefetch];
 #pragma unroll
     for (int i = 0; i < kCombinePrefetch; ++i) {
         const int sp = warp + kCombineWarps * i;
-        pv[i] = (live && sp < S)
-                    ? __ldg(reinterpret_cast<const float4 *>(acc + (size_t)sp * acc_stride))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        pv[i] = (live && sp < SR) ? acc_of(sp) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     // m = max_i m_i and l = sum_i e^{m_i - m} l_i, by every warp for itself
     float M = kNeutralM;
-    for (int sp = lane; sp < S; sp += 32) M = fmaxf(M, __ldg(&ml[(size_t)sp * p.n_heads].x));
+    for (int sp = lane; sp < SR; sp += 32) M = fmaxf(M, ml_of(sp).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
-    for (int sp = lane; sp < S; sp += 32) {
-        const float2 x = __ldg(&ml[(size_t)sp * p.n_heads]);
+    for (int sp = lane; sp < SR; sp += 32) {
+        const float2 x = ml_of(sp);
         L = fmaf(x.y, ex2((x.x - M) * kLog2e), L);
     }
 #pragma unroll
@@ -98,16 +107,14 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
     for (int i = 0; i < kCombinePrefetch; ++i) {
         const int sp = warp + kCombineWarps * i;
-        if (sp < S) {
-            const float2 x = __ldg(&ml[(size_t)sp * p.n_heads]);
+        if (sp < SR) {
+            const float2 x = ml_of(sp);
             if (x.y > 0.f) fma4(a, ex2((x.x - M) * kLog2e), pv[i]);
         }
     }
-    for (int sp = warp + kCombineWarps * kCombinePrefetch; sp < S; sp += kCombineWarps) {
-        const float2 x = __ldg(&ml[(size_t)sp * p.n_heads]);
-        if (live && x.y > 0.f)
-            fma4(a, ex2((x.x - M) * kLog2e),
-                 __ldg(reinterpret_cast<const float4 *>(acc + (size_t)sp * acc_stride)));
+    for (int sp = warp + kCombineWarps * kCombinePrefetch; sp < SR; sp += kCombineWarps) {
+        const float2 x = ml_of(sp);
+        if (live && x.y > 0.f) fma4(a, ex2((x.x - M) * kLog2e), acc_of(sp));
     }
     part[warp][lane] = a;
     __syncthreads();

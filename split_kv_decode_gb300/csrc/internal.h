@@ -22,9 +22,12 @@ inline int64_t ws_acc_offset(int64_t total_splits, int n_heads)
     int64_t ml = total_splits * n_heads * 8;
     return kWsHeader + ((ml + 255) / 256) * 256;
 }
+// rounded to 256 bytes, so that workspaces placed back to back (one per rank
+// of a context-parallel step) keep every region aligned
 inline int64_t ws_total(int64_t total_splits, int n_heads, int v_dim)
 {
-    return ws_acc_offset(total_splits, n_heads) + total_splits * n_heads * v_dim * 4;
+    const int64_t t = ws_acc_offset(total_splits, n_heads) + total_splits * n_heads * v_dim * 4;
+    return (t + 255) / 256 * 256;
 }
 
 // Status word codes written by kernels (low byte = da_status_t, next byte = kernel).
@@ -97,6 +100,11 @@ struct CombineParams {
     int32_t n_heads;
     int32_t v_dim;
     int32_t batch;
+    // partials of n_ranks ranks that ran the same plan, workspaces back to back:
+    // rank r's (m, l) at ml + r * rank_ml, its acc at acc + r * rank_acc
+    int32_t n_ranks;
+    int64_t rank_ml;
+    int64_t rank_acc;
     int32_t n_splits[DA_MAX_BATCH];
     int32_t split_base[DA_MAX_BATCH];
 };
