@@ -89,6 +89,14 @@ typedef struct {
                             so that no split is empty)                         */
     int32_t flags;       /* DA_FLAG_*                                          */
     int32_t timeout_us;  /* bound on every in-kernel wait; 0 = 2 000 000 us    */
+    int32_t q_len;       /* query tokens per sequence; 0 or 1: one. With q_len
+                            > 1 (GQA/MQA only), q is [batch][q_len][n_heads]
+                            [head_dim] and out [batch][q_len][n_heads][v_dim];
+                            token i sits at position L - q_len + i and attends
+                            to positions 0 .. L - q_len + i (causal among the
+                            new tokens, whose K/V rows are in the cache).
+                            (n_heads / n_kv_heads) * q_len must be 1, 2, 4, 6
+                            or 8, and every seq_len >= q_len.                  */
 } da_args_t;
 
 /* A host-side plan (plan/run separation): which kernel, how the context is

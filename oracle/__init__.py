@@ -189,6 +189,28 @@ def attention(q, k, v, seq_lens, scale, *, v_dim=None, pairs=None, threads=1):
     return out if p is not None else out.reshape(shp.batch, shp.n_heads, shp.v_dim)
 
 
+def attention_multi(q, k, v, seq_lens, scale, *, v_dim=None, pairs=None, threads=1):
+    """Several new query tokens per sequence, causal among themselves, in double.
+
+    q: [B, T, Hq, Dk]: the last T positions of each sequence, whose keys and
+    values are already in the cache. Token t sits at position L - T + t and
+    attends to positions 0 .. L - T + t, the causal mask of a decoder block
+    ("Decoder Block 6: Online Attention, the Capstone", Lesson: each query row
+    sees its own prefix), so token t is plain attention over a sequence of
+    length L - T + t + 1 and the oracle forms it that way, token by token.
+    Requires every seq_lens[b] >= T. Returns float64 [B, T, Hq, Dv] (with
+    pairs (b, h): [T, n_pairs, Dv]).
+    """
+    q = q.detach().cpu() if hasattr(q, "detach") else np.asarray(q)
+    T = int(q.shape[1])
+    lens = np.asarray(seq_lens, dtype=np.int64).reshape(-1)
+    if T < 1 or np.any(lens < T):
+        raise ValueError("every sequence needs at least q_len positions")
+    outs = [attention(q[:, t], k, v, (lens - T + 1 + t).astype(np.int32), scale, v_dim=v_dim,
+                      pairs=pairs, threads=threads) for t in range(T)]
+    return np.stack(outs, axis=0 if pairs is not None else 1)
+
+
 def attention_split(q, k, v, seq_lens, scale, n_splits, *, block=64, form=MERGE_ML, flags=0,
                     v_dim=None, pairs=None, return_partials=False):
     """The split-KV method in double: n_splits contiguous segments per row, the

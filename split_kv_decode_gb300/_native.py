@@ -34,6 +34,7 @@ class DaArgs(ctypes.Structure):
         ("kv_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
         ("scale", ctypes.c_float), ("force_splits", ctypes.c_int32),
         ("flags", ctypes.c_int32), ("timeout_us", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
     ]
 
 

@@ -50,13 +50,19 @@ def dtype_code(dt: torch.dtype) -> int:
 def make_args(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float, *,
               v_dim: Optional[int] = None, out_dtype: torch.dtype = torch.float32,
               force_splits: int = 0, flags: int = 0, timeout_us: int = 0) -> N.DaArgs:
-    """Describe q [B, Hq, Dk] and caches [B, cap, Hkv, D] (any element strides)
-    as a da_args_t. For MLA pass the same tensor as both caches and v_dim."""
-    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4:
-        raise ValueError("q must be [B, Hq, D] and caches [B, cap, Hkv, D]")
-    B, Hq, Dk = q.shape
+    """Describe q [B, Hq, Dk] (one token per sequence) or [B, q_len, Hq, Dk]
+    (q_len new tokens, causal among themselves) and caches [B, cap, Hkv, D]
+    (any element strides) as a da_args_t. For MLA pass the same tensor as both
+    caches and v_dim."""
+    if q.dim() not in (3, 4) or k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, D] or [B, q_len, Hq, D] and caches [B, cap, Hkv, D]")
+    if q.dim() == 3:
+        (B, Hq, Dk), q_len = q.shape, 1
+    else:
+        B, q_len, Hq, Dk = q.shape
     a = N.DaArgs()
     a.batch, a.n_heads, a.n_kv_heads, a.head_dim = B, Hq, k_cache.shape[2], Dk
+    a.q_len = q_len
     a.v_dim = int(v_dim) if v_dim is not None else v_cache.shape[3]
     a.capacity = k_cache.shape[1]
     ks, vs = k_cache.stride(), v_cache.stride()
@@ -229,7 +235,9 @@ class DecodeAttention:
 
     def new_out(self, device) -> torch.Tensor:
         a = self.args
-        return torch.empty((a.batch, a.n_heads, a.v_dim), dtype=self.out_dtype, device=device)
+        shape = (a.batch, a.n_heads, a.v_dim) if a.q_len <= 1 else \
+            (a.batch, a.q_len, a.n_heads, a.v_dim)
+        return torch.empty(shape, dtype=self.out_dtype, device=device)
 
     def __call__(self, q, k_cache, v_cache, out=None, stream=None) -> torch.Tensor:
         if out is None:

@@ -77,6 +77,10 @@ bool gqa_config_any(int dt, int D, int G, GqaConfig *cfg)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// query tokens per sequence, and rows (query token, head) of the workspace and out
+int q_len_of(const da_args_t *a) { return a->q_len > 1 ? a->q_len : 1; }
+int rows_of(const da_args_t *a) { return a->n_heads * q_len_of(a); }
+
 int check_args(const da_args_t *a)
 {
     if (!a) return fail(DA_EINVAL, "args", "args is NULL");
@@ -102,6 +106,7 @@ int check_args(const da_args_t *a)
         return fail(DA_EINVAL, "args", "batch strides must be positive when batch > 1");
     if (a->force_splits < 0) return fail(DA_EINVAL, "args", "force_splits < 0");
     if (a->timeout_us < 0) return fail(DA_EINVAL, "args", "timeout_us < 0");
+    if (a->q_len < 0 || a->q_len > 64) return fail(DA_EINVAL, "args", "q_len %d outside [0, 64]", a->q_len);
     return DA_OK;
 }
 
@@ -114,9 +119,12 @@ struct KernelChoice {
 
 int select_kernel(const da_args_t *a, KernelChoice *kc)
 {
-    const int G = a->n_heads / a->n_kv_heads;
+    // the GQA kernel serves the q_len tokens of a group as extra rows
+    const int G = a->n_heads / a->n_kv_heads * q_len_of(a);
     const int es = dtype_size(a->kv_dtype);
     if (a->head_dim == 576 && a->v_dim == 512 && a->n_kv_heads == 1) {
+        if (q_len_of(a) > 1)
+            return fail(DA_EUNSUPPORTED, "plan", "the MLA kernel serves one query token");
         if (a->kv_dtype != DA_F32)
             return fail(DA_EUNSUPPORTED, "plan", "the MLA kernel reads an f32 latent cache");
         if (!mla_supported_heads(a->n_heads))
@@ -140,8 +148,8 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
     GqaConfig cfg;
     if (!gqa_config_any(a->kv_dtype, a->head_dim, G, &cfg))
         return fail(DA_EUNSUPPORTED, "plan",
-                    "no GQA kernel for head_dim %d, group %d, %s KV (head_dim 128 or 256; "
-                    "group 1, 2, 4, 6 or 8)",
+                    "no GQA kernel for head_dim %d, group %d (heads per KV head x q_len), "
+                    "%s KV (head_dim 128 or 256; group 1, 2, 4, 6 or 8)",
                     a->head_dim, G, dtype_name(a->kv_dtype));
     const int64_t st[6] = {a->k_pos_stride, a->k_head_stride, a->v_pos_stride,
                            a->v_head_stride, a->batch > 1 ? a->k_batch_stride : 0,
@@ -242,9 +250,9 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
     int64_t base = 0, items = 0;
     for (int b = 0; b < a->batch; ++b) {
         const int L = pl->seq_lens[b];
-        if (L < 1 || L > a->capacity)
-            return fail(DA_EINVAL, "plan", "seq_lens[%d] = %d outside [1, capacity %d]", b, L,
-                        a->capacity);
+        if (L < q_len_of(a) || L > a->capacity)
+            return fail(DA_EINVAL, "plan", "seq_lens[%d] = %d outside [q_len %d, capacity %d]",
+                        b, L, q_len_of(a), a->capacity);
         if (pl->chunk[b] < 1 || pl->n_splits[b] != ceil_div(L, pl->chunk[b]) ||
             pl->split_base[b] != base)
             return fail(DA_EINVAL, "plan", "inconsistent split table at b = %d", b);
@@ -254,7 +262,7 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
     if (pl->total_splits != base || pl->n_items != items || pl->grid < kc->cluster ||
         pl->grid > items * kc->cluster || pl->grid % kc->cluster)
         return fail(DA_EINVAL, "plan", "inconsistent plan totals");
-    if (pl->workspace_bytes != ws_total(pl->total_splits, a->n_heads, a->v_dim))
+    if (pl->workspace_bytes != ws_total(pl->total_splits, rows_of(a), a->v_dim))
         return fail(DA_EINVAL, "plan", "inconsistent workspace size");
     return DA_OK;
 }
@@ -273,7 +281,7 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
     p.pos_stride = a->k_pos_stride;
     p.batch_stride = a->batch > 1 ? a->k_batch_stride : 0;
     p.ml = reinterpret_cast<float2 *>(w + ws_ml_offset());
-    p.acc = reinterpret_cast<float *>(w + ws_acc_offset(pl->total_splits, a->n_heads));
+    p.acc = reinterpret_cast<float *>(w + ws_acc_offset(pl->total_splits, rows_of(a)));
     p.status = reinterpret_cast<int *>(w);
     p.n_heads = a->n_heads;
     p.scale_log2 = a->scale * 1.4426950408889634f;
@@ -311,9 +319,11 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     uint8_t *w = static_cast<uint8_t *>(ws);
     p.q = q;
     p.ml = reinterpret_cast<float2 *>(w + ws_ml_offset());
-    p.acc = reinterpret_cast<float *>(w + ws_acc_offset(pl->total_splits, a->n_heads));
+    p.acc = reinterpret_cast<float *>(w + ws_acc_offset(pl->total_splits, rows_of(a)));
     p.status = reinterpret_cast<int *>(w);
-    p.n_heads = a->n_heads;
+    p.n_heads = rows_of(a);
+    p.q_len = q_len_of(a);
+    p.hq = a->n_heads;
     p.scale_log2 = a->scale * 1.4426950408889634f;
     p.timeout_ns = (uint64_t)(a->timeout_us > 0 ? a->timeout_us : 2000000) * 1000ull;
     p.flags = a->flags;
@@ -354,7 +364,7 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     }
     if (dev) p.dev_lens = dev->seq_lens;
 
-    const int G = a->n_heads / a->n_kv_heads;
+    const int G = a->n_heads / a->n_kv_heads * q_len_of(a);
     cudaError_t e;
     switch (a->kv_dtype) {
     case DA_F32: e = gqa_launch_f32(a->head_dim, G, pl->grid, st, km, vm, p); break;
@@ -375,16 +385,16 @@ int launch_combine_phase(const da_args_t *a, const da_plan_t *pl, const void *ws
     c.rank_acc = pl->workspace_bytes / 4;
     const uint8_t *w = static_cast<const uint8_t *>(ws);
     c.ml = reinterpret_cast<const float2 *>(w + ws_ml_offset());
-    c.acc = reinterpret_cast<const float *>(w + ws_acc_offset(pl->total_splits, a->n_heads));
+    c.acc = reinterpret_cast<const float *>(w + ws_acc_offset(pl->total_splits, rows_of(a)));
     c.out = out;
-    c.n_heads = a->n_heads;
+    c.n_heads = rows_of(a);
     c.v_dim = a->v_dim;
     c.batch = a->batch;
     for (int b = 0; b < a->batch; ++b) {
         c.n_splits[b] = pl->n_splits[b];
         c.split_base[b] = pl->split_base[b];
     }
-    cudaError_t e = launch_combine(a->out_dtype, a->v_dim, c, a->n_heads, a->batch, st, true);
+    cudaError_t e = launch_combine(a->out_dtype, a->v_dim, c, rows_of(a), a->batch, st, true);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(DA_ELAUNCH, "combine", "%s", cudaGetErrorString(e));
     return DA_OK;
@@ -424,9 +434,9 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
     if (rc) return rc;
     if (!lens || !plan) return fail(DA_EINVAL, "args", "seq_lens or plan is NULL");
     for (int b = 0; b < a->batch; ++b)
-        if (lens[b] < 1 || lens[b] > a->capacity)
-            return fail(DA_EINVAL, "args", "seq_lens[%d] = %d outside [1, capacity %d]", b,
-                        lens[b], a->capacity);
+        if (lens[b] < q_len_of(a) || lens[b] > a->capacity)
+            return fail(DA_EINVAL, "args", "seq_lens[%d] = %d outside [q_len %d, capacity %d]",
+                        b, lens[b], q_len_of(a), a->capacity);
     KernelChoice kc;
     rc = select_kernel(a, &kc);
     if (rc) return rc;
@@ -464,7 +474,7 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
     }
     plan->total_splits = (int32_t)base;
     plan->max_splits = mx;
-    plan->workspace_bytes = ws_total(base, a->n_heads, a->v_dim);
+    plan->workspace_bytes = ws_total(base, rows_of(a), a->v_dim);
     plan->est_cost = po.est_cost;
     return DA_OK;
 }

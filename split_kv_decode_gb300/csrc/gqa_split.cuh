@@ -174,11 +174,11 @@ __device__ __forceinline__ void decode_item(const ItemTable &it, int item, int &
 }
 
 // the length an item of sequence b attends over: the plan's, or the current
-// length read on the device, kept within [1, the plan's]
+// length read on the device, kept within [q_len, the plan's]
 __device__ __forceinline__ int item_len(const SplitParams &p, int b)
 {
     const int L = p.items.seq_lens[b];
-    return p.dev_lens ? max(1, min(__ldg(p.dev_lens + b), L)) : L;
+    return p.dev_lens ? max(p.q_len, min(__ldg(p.dev_lens + b), L)) : L;
 }
 
 // A tile is T rows, cut at the item's end and, for a paged cache, at the end
@@ -373,21 +373,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     const int tbase = tr_base<K::NVL, LPR / 2>(lane);
     const bool twriter = tr_writer<K::NVL, LPR / 2>(lane);
 
-    // q for the G heads of an item's group, pre-scaled into log2 units. The
+    // The G rows of an item are (query token, head) pairs: row j is token
+    // j / Gh and head kvh * Gh + j % Gh of that token, Gh = heads per KV head.
+    // Offsets of row j from the (sequence, group) base, in q and workspace rows:
+    const int Gh = G / p.q_len;
+    auto row_off = [&](int j) { return p.q_len == 1 ? j : (j / Gh) * p.hq + j % Gh; };
+
+    // q for the G rows of an item's group, pre-scaled into log2 units. The
     // next item's q is loaded right after the last tile of the current one,
     // so the load overlaps the merge.
     float q[G][K::EPL];
     auto load_q = [&](int item) {
         int qb_b, qb_kvh, qb_s;
         decode_item(it, item, qb_b, qb_kvh, qb_s);
-        const float *qb = p.q + ((size_t)qb_b * p.n_heads + (size_t)qb_kvh * G) * D;
+        const float *qb = p.q + ((size_t)qb_b * p.n_heads + (size_t)qb_kvh * Gh) * D;
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
             for (int c = 0; c < K::NCH; ++c)
 #pragma unroll
                 for (int e = 0; e < K::EPC; e += 4) {
-                    float4 x = *reinterpret_cast<const float4 *>(qb + h * D +
+                    float4 x = *reinterpret_cast<const float4 *>(qb + (size_t)row_off(h) * D +
                                                                  (c * LPR + sub) * K::EPC + e);
                     q[h][c * K::EPC + e + 0] = x.x * p.scale_log2;
                     q[h][c * K::EPC + e + 1] = x.y * p.scale_log2;
@@ -403,7 +409,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         int b, kvh, s;
         decode_item(it, item, b, kvh, s);
         const int p0 = s * it.chunk[b];
-        const int p1 = min(item_len(p, b), p0 + it.chunk[b]); // p1 <= p0: an empty item
+        const int Lb = item_len(p, b);
+        const int p1 = min(Lb, p0 + it.chunk[b]); // p1 <= p0: an empty item
+        // token i of q_len sees positions below lim0 + i (causal among the new
+        // tokens); with one token lim0 = Lb and no tile reaches past it
+        const int lim0 = Lb - p.q_len + 1;
 
         float acc[G][K::EPL];
         float m[G];
@@ -453,11 +463,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                                 dv[r2 * G + h] = fmaf(q[h][c * K::EPC + e], kf[e], dv[r2 * G + h]);
                     }
                 tr_reduce<K::NVL, LPR / 2>(dv, lane);
+                const bool causal = t1 > lim0; // a tile that reaches the new tokens
 #pragma unroll
                 for (int r = 0; r < K::R; ++r) {
-                    const int idx = tbase + r;                       // (step, head) of this group
+                    const int idx = tbase + r;                       // (step, row) of this group
                     const int row = (idx / G) * K::RPW + half;
-                    const float sv = (row < valid) ? dv[r] : -INFINITY;
+                    bool live = row < valid;
+                    if (causal)
+                        live = live && t0 + warp * K::P + row < lim0 + (idx % G) / Gh;
+                    const float sv = live ? dv[r] : -INFINITY;
                     if (twriter) sc[row * G + idx % G] = sv;
                 }
                 __syncwarp();
@@ -640,7 +654,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         // warp 0 writes the partial: acc from its registers, (m, l) per head
         if (warp == 0) {
             const size_t slot_id = (size_t)it.split_base[b] + s;
-            const size_t row0 = slot_id * p.n_heads + (size_t)kvh * G;
+            const size_t row0 = slot_id * p.n_heads + (size_t)kvh * Gh;
             if (half == 0) {
                 float *dst = p.acc + row0 * D;
 #pragma unroll
@@ -649,11 +663,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                     for (int c = 0; c < K::NCH; ++c)
 #pragma unroll
                         for (int e = 0; e < K::EPC; e += 4)
-                            *reinterpret_cast<float4 *>(dst + h * D + (c * LPR + sub) * K::EPC + e) =
+                            *reinterpret_cast<float4 *>(dst + (size_t)row_off(h) * D +
+                                                        (c * LPR + sub) * K::EPC + e) =
                                 make_float4(acc[h][c * K::EPC + e], acc[h][c * K::EPC + e + 1],
                                             acc[h][c * K::EPC + e + 2], acc[h][c * K::EPC + e + 3]);
             }
-            if (lane < G) p.ml[row0 + lane] = make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
+            if (lane < G)
+                p.ml[row0 + row_off(lane)] = make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
         }
     }
     if (threadIdx.x == 0) griddep_launch_dependents();

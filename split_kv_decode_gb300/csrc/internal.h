@@ -45,11 +45,13 @@ struct ItemTable {
 };
 
 struct SplitParams {
-    const float *q;          // [B][Hq][Dk]
-    float2 *ml;              // workspace (m, l) per (slot, head)
-    float *acc;              // workspace acc per (slot, head, Dv)
+    const float *q;          // [B][q_len][hq][Dk]
+    float2 *ml;              // workspace (m, l) per (slot, row)
+    float *acc;              // workspace acc per (slot, row, Dv)
     int *status;             // workspace status word
-    int32_t n_heads;
+    int32_t n_heads;         // rows per sequence: q_len * hq (query token, head)
+    int32_t q_len;           // query tokens per sequence (causal among them)
+    int32_t hq;              // query heads per token
     float scale_log2;        // scale * log2(e)
     uint64_t timeout_ns;
     int32_t flags;

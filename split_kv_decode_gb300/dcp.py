@@ -91,6 +91,10 @@ class ContextParallelDecode:
                  seq_lens: Sequence[int], scale: float, *, rank: int = 0, world: int = 1,
                  group=None, v_dim: Optional[int] = None,
                  out_dtype: torch.dtype = torch.float32):
+        if q.dim() != 3:
+            # the new tokens' causal window would need the global position of each
+            # rank's slice; only the one-token decode is sharded over the context
+            raise ValueError("context-parallel decode takes one query token: q [B, Hq, Dk]")
         self.world, self.rank, self.group = world, rank, group
         self.args = A.make_args(q, k_local, v_local, scale, v_dim=v_dim, out_dtype=out_dtype,
                                 flags=N.DA_FLAG_NO_COMBINE)

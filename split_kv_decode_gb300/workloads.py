@@ -108,6 +108,15 @@ def make_case(name: str, *, batch: int, n_heads: int, n_kv_heads: int, head_dim:
                 out_dtype, sc, q, k, v, shared_kv)
 
 
+def multi_token_q(batch: int, q_len: int, n_heads: int, head_dim: int, seed: int = 4321,
+                  std: float = 1.0) -> torch.Tensor:
+    """Seeded f32 queries [B, q_len, Hq, Dk] for q_len new tokens per sequence
+    (their keys and values are the last q_len rows of each cache)."""
+    g = torch.Generator().manual_seed(int(seed))
+    q = torch.randn((batch, q_len, n_heads, head_dim), generator=g, dtype=torch.float32)
+    return q.mul_(std) if std != 1.0 else q
+
+
 GQA16X4_RUNGS = (4096, 20480, 61440, 151552, 262144)
 GQA24X4_LENS = (8192, 20480, 61440, 131072)
 

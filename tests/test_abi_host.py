@@ -432,3 +432,51 @@ def test_dev_call_needs_one_latent_pool_for_mla_and_an_extension(lib):
     rc = lib.decode_attn_splitk_dev(ctypes.byref(a), ctypes.byref(p), None, fake, fake, fake,
                                     fake, fake, p.workspace_bytes, None)
     assert rc == N.DA_EINVAL
+
+
+# ---------------------------------------------------------------------------
+# several query tokens per sequence (q_len > 1)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("hq,hkv,q_len", [(16, 4, 2), (8, 4, 4), (4, 4, 6), (4, 4, 8), (32, 8, 2)])
+def test_plan_multi_token_groups(lib, hq, hkv, q_len):
+    d = 128 if hq == 32 else 256
+    a = args(hq=hq, hkv=hkv, d=d, cap=8192)
+    rc, p1 = plan(lib, a, [8192])
+    assert rc == 0
+    a.q_len = q_len
+    rc, p = plan(lib, a, [8192])
+    assert rc == 0, lib.decode_attn_last_error().decode()
+    # the workspace holds q_len rows per head for every split
+    ml = p.total_splits * hq * q_len * 8
+    acc = p.total_splits * hq * q_len * a.v_dim * 4
+    assert p.workspace_bytes >= ml + acc
+    assert p.kernel == N.DA_KERNEL_GQA_TMA
+
+
+@pytest.mark.parametrize("hq,hkv,q_len", [(16, 4, 3), (8, 2, 4), (16, 1, 2)])
+def test_plan_multi_token_rejects_large_groups(lib, hq, hkv, q_len):
+    a = args(hq=hq, hkv=hkv, cap=8192)
+    a.q_len = q_len
+    rc, _ = plan(lib, a, [8192])
+    assert rc == N.DA_EUNSUPPORTED
+    assert "q_len" in lib.decode_attn_last_error().decode()
+
+
+def test_plan_multi_token_needs_q_len_positions(lib):
+    a = args(hq=8, hkv=4, cap=8192)
+    a.q_len = 4
+    assert plan(lib, a, [4, 100])[0] == 0
+    assert plan(lib, a, [3, 100])[0] == N.DA_EINVAL
+    assert "q_len" in lib.decode_attn_last_error().decode()
+    a.q_len = -1
+    assert plan(lib, a, [100])[0] == N.DA_EINVAL
+    a.q_len = 0                                # 0 reads as one token
+    assert plan(lib, a, [1])[0] == 0
+
+
+def test_mla_refuses_multi_token(lib):
+    a = mla_args(cap=4096)
+    a.q_len = 2
+    rc, _ = plan(lib, a, [4096])
+    assert rc == N.DA_EUNSUPPORTED
+    assert "one query token" in lib.decode_attn_last_error().decode()

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from split_kv_decode_gb300 import workloads as W
-from tests._naive import naive_attention, widen
+from tests._naive import naive_attention, naive_causal_attention, widen
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -291,3 +291,59 @@ def test_worked_example_with_a_neutral_third_partial():
         assert np.isfinite(got[0]) and abs(got[0] - ref[0]) <= 1e-15 * abs(ref[0])
     with pytest.raises(ValueError):
         oracle.merge([-1e30, -1e30], [0.0, 0.0], [[0.0], [0.0]])
+
+
+# ---------------------------------------------------------------------------
+# several new tokens per sequence, causal among themselves
+# ---------------------------------------------------------------------------
+def _multi(hq, hkv, d, lens, T, dtype="f32", seed=11, scale=0.6):
+    c = small(hq, hkv, d, lens, dtype=dtype, cap=max(lens) + 3, seed=seed, scale=scale)
+    return c, W.multi_token_q(len(lens), T, hq, d, seed=seed + 1)
+
+
+@pytest.mark.parametrize("hq,hkv,T", [(1, 1, 2), (4, 2, 3), (8, 2, 4), (6, 1, 2), (16, 4, 2)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_multi_token_brute_force_with_explicit_mask(hq, hkv, T, dtype):
+    c, q = _multi(hq, hkv, 16, [T, 7, 40], T, dtype=dtype, seed=hq + 3 * T)
+    ref = naive_causal_attention(q, c.k, c.v, c.seq_lens, c.scale)
+    got = oracle.attention_multi(q, c.k, c.v, c.seq_lens, c.scale)
+    assert got.shape == (3, T, hq, 16)
+    assert np.max(np.abs(got - ref)) <= 1e-13 * vmax(c)
+
+
+def test_multi_token_whole_sequence_first_token_sees_only_position_zero():
+    # q_len = L: the prefill of the whole sequence; token 0 attends to position 0
+    # alone, so its output is that value row exactly
+    c, q = _multi(4, 2, 8, [6], 6, seed=5)
+    got = oracle.attention_multi(q, c.k, c.v, c.seq_lens, c.scale)
+    for h in range(4):
+        assert np.array_equal(got[0, 0, h], widen(c.v[0, 0, h // 2]))
+    ref = naive_causal_attention(q, c.k, c.v, c.seq_lens, c.scale)
+    assert np.max(np.abs(got - ref)) <= 1e-13 * vmax(c)
+
+
+def test_multi_token_last_token_is_single_token_decode():
+    c, q = _multi(8, 2, 16, [9, 33], 3, seed=9)
+    got = oracle.attention_multi(q, c.k, c.v, c.seq_lens, c.scale)
+    one = oracle.attention(q[:, -1], c.k, c.v, c.seq_lens, c.scale)
+    assert np.array_equal(got[:, -1], one)
+    # and one token is the single-token call itself
+    got1 = oracle.attention_multi(q[:, :1], c.k, c.v, c.seq_lens, c.scale)
+    assert np.array_equal(got1[:, 0], oracle.attention(q[:, 0], c.k, c.v, c.seq_lens, c.scale))
+
+
+def test_multi_token_negative_control_off_by_one_mask_is_caught():
+    # a mask that lets token t see one position too many (or too few) differs
+    c, q = _multi(4, 1, 16, [12], 3, seed=13)
+    ref = naive_causal_attention(q, c.k, c.v, c.seq_lens, c.scale)
+    for shift in (1, -1):
+        bad = np.stack([oracle.attention(q[:, t], c.k, c.v,
+                                         np.array([12 - 3 + 1 + t + shift], dtype=np.int32),
+                                         c.scale) for t in range(2)], axis=1)
+        assert np.max(np.abs(bad - ref[:, :2])) > 1e-3
+
+
+def test_multi_token_rejects_short_sequences():
+    c, q = _multi(2, 1, 8, [2, 9], 3, seed=2)
+    with pytest.raises(ValueError):
+        oracle.attention_multi(q, c.k, c.v, c.seq_lens, c.scale)
