@@ -373,6 +373,9 @@ def main():
             line["graph"] = measure_graph(case, q, k, v, out_dt, dev, flush, args)
             line["paged"] = {f"block_{bs}": measure_paged(case, q, k, v, out_dt, dev, flush, args, bs)
                              for bs in (64, 256)}
+            ml = measure_multi_token(case, k, v, out_dt, dev, flush, args)
+            if ml:
+                line["multi_token"] = ml
         line["cpu_baseline"] = cpu_baseline(case)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -461,6 +464,34 @@ def measure_paged(case, q, k, v, out_dt, dev, flush, args, block_size):
     return {"value": round(us, 2), "unit": "us/layer-step", "steps": n, "block_size": block_size,
             "kv_gbs": round(gbs, 1),
             "what": "split + combine with the caches in a pool of blocks, random block order"}
+
+
+def measure_multi_token(case, k, v, out_dt, dev, flush, args):
+    """The same caches with the largest q_len (new tokens per sequence, causal
+    among themselves) whose query rows per KV head still fit one kernel group:
+    every K/V tile is read once for all of them."""
+    import torch
+    from split_kv_decode_gb300 import api as A
+    from split_kv_decode_gb300 import workloads as W
+    G = case.n_heads // case.n_kv_heads
+    q_len = max((t for t in (2, 4, 8) if G * t in (2, 4, 6, 8)), default=0)
+    if not q_len or int(case.seq_lens.min()) < q_len:
+        return None
+    q = W.multi_token_q(case.batch, q_len, case.n_heads, case.head_dim).to(dev)
+    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
+    p = A.decode_attn_plan(a, case.seq_lens.tolist())
+    ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    out = torch.empty(case.batch, q_len, case.n_heads, case.v_dim, dtype=out_dt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
+    n = max(20, min(args.steps, 200))
+    us = _timed_steps(lambda: A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream),
+                      flush, n, stream)
+    return {"value": round(us, 2), "unit": "us/layer-step", "steps": n, "q_len": q_len,
+            "kv_gbs": round(case.kv_bytes / (us * 1e-6) / 1e9, 1),
+            "what": f"split + combine for {q_len} new tokens per sequence, causal among "
+                    "themselves, sharing every K/V tile"}
 
 
 def measure_e2e(case, q_dev, out_dt, dev, stream, args):

@@ -94,9 +94,11 @@ typedef struct {
                             [head_dim] and out [batch][q_len][n_heads][v_dim];
                             token i sits at position L - q_len + i and attends
                             to positions 0 .. L - q_len + i (causal among the
-                            new tokens, whose K/V rows are in the cache).
-                            (n_heads / n_kv_heads) * q_len must be 1, 2, 4, 6
-                            or 8, and every seq_len >= q_len.                  */
+                            new tokens, whose K/V rows are in the cache: the
+                            causal query tile of "Decoder Block 6: Online
+                            Attention, the Capstone", Lesson). (n_heads /
+                            n_kv_heads) * q_len must be 1, 2, 4, 6 or 8, and
+                            every seq_len >= q_len; at most 64.                */
 } da_args_t;
 
 /* A host-side plan (plan/run separation): which kernel, how the context is
