@@ -376,6 +376,9 @@ def main():
             ml = measure_multi_token(case, k, v, out_dt, dev, flush, args)
             if ml:
                 line["multi_token"] = ml
+        if kernel == "mla_split_kernel":
+            line["wv_b"] = {name: measure_wv_b(case, q, k, v, out_dt, dev, flush, args, wdt)
+                            for name, wdt in (("f32", torch.float32), ("bf16", torch.bfloat16))}
         line["cpu_baseline"] = cpu_baseline(case)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -464,6 +467,31 @@ def measure_paged(case, q, k, v, out_dt, dev, flush, args, block_size):
     return {"value": round(us, 2), "unit": "us/layer-step", "steps": n, "block_size": block_size,
             "kv_gbs": round(gbs, 1),
             "what": "split + combine with the caches in a pool of blocks, random block order"}
+
+
+def measure_wv_b(case, q, k, v, out_dt, dev, flush, args, wdt):
+    """The step with the value up-projection wv_b fused into the combine: every
+    head's merged 512-wide latent times its [128 x 512] matrix (random weights
+    of that shape), split + combine_proj."""
+    import torch
+    from split_kv_decode_gb300 import api as A
+    g = torch.Generator().manual_seed(77)
+    w = (torch.randn((case.n_heads, 128, case.v_dim), generator=g) / 23.0).to(wdt).to(dev)
+    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
+    p = A.decode_attn_plan(a, case.seq_lens.tolist())
+    ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    out = torch.empty(case.batch, case.n_heads, 128, dtype=out_dt, device=dev)
+    pj = A.make_proj(w)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        A.decode_attn_splitk_proj(a, p, pj, q, k, v, out, ws, stream)
+    n = max(20, min(args.steps, 200))
+    us = _timed_steps(lambda: A.decode_attn_splitk_proj(a, p, pj, q, k, v, out, ws, stream),
+                      flush, n, stream)
+    return {"value": round(us, 2), "unit": "us/layer-step", "steps": n,
+            "w_bytes": w.numel() * w.element_size(),
+            "what": f"split + combine fused with wv_b ({case.n_heads} x 128 x {case.v_dim} "
+                    f"{str(wdt).split('.')[-1]} weights)"}
 
 
 def measure_multi_token(case, k, v, out_dt, dev, flush, args):

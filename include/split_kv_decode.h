@@ -191,6 +191,54 @@ int decode_attn_combine_ranks(const da_args_t *args, const da_plan_t *plan,
                               da_stream_t stream);
 
 /*
+ * da_proj_t -- a per-head output projection applied to the merged attention
+ * output: out[b][h][e] = sum_c W[h][e][c] * attn[b][h][c], e < out_dim,
+ * c < v_dim. For MLA this is the value up-projection wv_b, which maps a head's
+ * merged 512-wide latent to its value head; it is a function of the merged
+ * result, not of any one split, so it runs in the combine ("Attention at 128k"
+ * §2, the PR #49 decisions: the output projection moves into the combine).
+ * With q_len > 1 every token of a head uses that head's W. Caller-owned device
+ * memory, read only.
+ */
+typedef struct da_proj_t {
+    const void *w;        /* DEVICE: element (h, e, c) at h*head_stride + e*row_stride
+                             + c, 16-byte aligned                                   */
+    int32_t w_dtype;      /* DA_F32 or DA_BF16                                    */
+    int32_t out_dim;      /* projected width per head, 1 .. 256                    */
+    int64_t head_stride;  /* elements between heads' matrices; 0: out_dim*row_stride
+                             (byte size a multiple of 16)                          */
+    int64_t row_stride;   /* elements between rows of one head; 0: v_dim (>= v_dim,
+                             byte size a multiple of 16)                           */
+} da_proj_t;
+
+/*
+ * decode_attn_combine_proj -- decode_attn_combine_ranks followed, in the same
+ * kernel, by the projection `proj`: out is [batch][q_len][n_heads][out_dim]
+ * in args->out_dtype. The merge is the one of decode_attn_combine_ranks
+ * (n_ranks = 1: decode_attn_combine); v_dim must be a multiple of 8 and at
+ * most 1024. One launch of clusters of ceil(v_dim / 128) CTAs per (sequence,
+ * query head); the weights are fetched while the split kernel drains. A
+ * weight load that does not finish within args->timeout_us sets the status
+ * word of the first workspace (decode_attn_device_status: "combine
+ * (projection)") and leaves that part of out undefined. Errors as
+ * decode_attn_combine, plus DA_EUNSUPPORTED for a weight type, out_dim or
+ * v_dim outside the above and DA_EINVAL for misaligned weights.
+ */
+int decode_attn_combine_proj(const da_args_t *args, const da_plan_t *plan,
+                             const da_proj_t *proj, const void *workspaces, int n_ranks,
+                             void *out, da_stream_t stream);
+
+/*
+ * decode_attn_splitk_proj -- decode_attn_splitk_ex whose combine is
+ * decode_attn_combine_proj: the split kernel, then the merge with the
+ * projection, two launches on `stream`; out is [batch][q_len][n_heads]
+ * [out_dim]. DA_FLAG_NO_COMBINE is ignored.
+ */
+int decode_attn_splitk_proj(const da_args_t *args, const da_plan_t *plan, const da_proj_t *proj,
+                            const float *q, const void *k_cache, const void *v_cache, void *out,
+                            void *workspace, size_t workspace_bytes, da_stream_t stream);
+
+/*
  * decode_attn_splitk -- the short form: batch 1, f32 q/K/V/out,
  * v_dim = head_dim, caches laid out [seq_len][n_kv_heads][head_dim]
  * contiguous, scale given.

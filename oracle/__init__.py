@@ -211,6 +211,29 @@ def attention_multi(q, k, v, seq_lens, scale, *, v_dim=None, pairs=None, threads
     return np.stack(outs, axis=0 if pairs is not None else 1)
 
 
+def attention_proj(q, k, v, seq_lens, scale, w, *, v_dim=None, pairs=None, threads=1):
+    """Attention followed by a per-head output projection, in double:
+    out[b][h][e] = sum_c W[h][e][c] * attn[b][h][c] (the MLA value up-projection
+    wv_b applied to the merged latent, "Attention at 128k", §2: the output
+    projection is a function of the merged result). q is [B, Hq, Dk] or
+    [B, T, Hq, Dk] (attention_multi; every token of head h uses W[h]); w is
+    [Hq, out_dim, v_dim] (numpy or CPU torch, any float type, widened exactly).
+    With pairs (b, h) only those rows are formed: [n_pairs, out_dim] (or
+    [T, n_pairs, out_dim])."""
+    if hasattr(w, "detach"):                                # a CPU torch tensor (incl. bf16)
+        import torch
+        W = w.detach().cpu().to(torch.float64).numpy()
+    else:
+        W = np.asarray(w, dtype=np.float64)
+    multi = len(q.shape) == 4
+    att = (attention_multi if multi else attention)(q, k, v, seq_lens, scale, v_dim=v_dim,
+                                                    pairs=pairs, threads=threads)
+    if pairs is not None:
+        Wp = W[[h for _, h in pairs]]                       # [n_pairs, out_dim, v_dim]
+        return np.einsum("...pc,pec->...pe", att, Wp)
+    return np.einsum("...hc,hec->...he", att, W)
+
+
 def attention_split(q, k, v, seq_lens, scale, n_splits, *, block=64, form=MERGE_ML, flags=0,
                     v_dim=None, pairs=None, return_partials=False):
     """The split-KV method in double: n_splits contiguous segments per row, the

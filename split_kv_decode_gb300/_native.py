@@ -65,6 +65,13 @@ class DaDev(ctypes.Structure):
     ]
 
 
+class DaProj(ctypes.Structure):
+    _fields_ = [
+        ("w", ctypes.c_void_p), ("w_dtype", ctypes.c_int32), ("out_dim", ctypes.c_int32),
+        ("head_stride", ctypes.c_int64), ("row_stride", ctypes.c_int64),
+    ]
+
+
 SIGNATURES = {
     "decode_attn_plan": (ctypes.c_int, [ctypes.POINTER(DaArgs), _P, ctypes.c_int,
                                         ctypes.POINTER(DaPlan)]),
@@ -83,6 +90,12 @@ SIGNATURES = {
     "decode_attn_splitk_dev": (ctypes.c_int, [ctypes.POINTER(DaArgs), ctypes.POINTER(DaPlan),
                                               ctypes.POINTER(DaDev), _P, _P, _P, _P, _P,
                                               ctypes.c_size_t, _P]),
+    "decode_attn_combine_proj": (ctypes.c_int, [ctypes.POINTER(DaArgs), ctypes.POINTER(DaPlan),
+                                                ctypes.POINTER(DaProj), _P, ctypes.c_int, _P,
+                                                _P]),
+    "decode_attn_splitk_proj": (ctypes.c_int, [ctypes.POINTER(DaArgs), ctypes.POINTER(DaPlan),
+                                               ctypes.POINTER(DaProj), _P, _P, _P, _P, _P,
+                                               ctypes.c_size_t, _P]),
     "decode_attn_last_error": (ctypes.c_char_p, []),
     "decode_attn_release": (None, []),
     "decode_attn_version": (ctypes.c_char_p, []),

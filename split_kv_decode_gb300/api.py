@@ -245,3 +245,38 @@ class DecodeAttention:
         decode_attn_splitk_ex(self.args, self.plan, q, k_cache, v_cache, out, self.workspace,
                               stream)
         return out
+
+
+def make_proj(w: torch.Tensor) -> N.DaProj:
+    """da_proj_t for per-head projection weights w [n_heads, out_dim, v_dim]
+    (f32 or bf16, on the device, last dimension contiguous). The tensor must
+    outlive every launch that uses the descriptor."""
+    if w.dim() != 3 or w.stride(2) != 1:
+        raise ValueError("w must be [n_heads, out_dim, v_dim] with a contiguous last dimension")
+    p = N.DaProj()
+    p.w = w.data_ptr()
+    p.w_dtype = dtype_code(w.dtype)
+    p.out_dim = w.shape[1]
+    p.head_stride, p.row_stride = w.stride(0), w.stride(1)
+    return p
+
+
+def decode_attn_combine_proj(args: N.DaArgs, plan: N.DaPlan, proj: N.DaProj,
+                             workspaces: torch.Tensor, out: torch.Tensor, n_ranks: int = 1,
+                             stream=None) -> None:
+    """The merge of n_ranks workspaces (back to back) followed by the per-head
+    projection: out [B, (q_len,) Hq, out_dim]."""
+    _check(N.load().decode_attn_combine_proj(ctypes.byref(args), ctypes.byref(plan),
+                                             ctypes.byref(proj), _ptr(workspaces),
+                                             int(n_ranks), _ptr(out), _stream(stream)))
+
+
+def decode_attn_splitk_proj(args: N.DaArgs, plan: N.DaPlan, proj: N.DaProj, q: torch.Tensor,
+                            k_cache: torch.Tensor, v_cache: torch.Tensor, out: torch.Tensor,
+                            workspace: torch.Tensor, stream=None) -> None:
+    """Split kernel, then the combine fused with the per-head projection."""
+    _check(N.load().decode_attn_splitk_proj(ctypes.byref(args), ctypes.byref(plan),
+                                            ctypes.byref(proj), _ptr(q), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(out), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream(stream)))

@@ -375,8 +375,33 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     return DA_OK;
 }
 
+// the projection's weights: element type, width, strides and alignment
+int check_proj(const da_args_t *a, const da_proj_t *pj, da_proj_t *norm)
+{
+    if (!pj || !pj->w) return fail(DA_EINVAL, "args", "proj or proj->w is NULL");
+    if (pj->w_dtype != DA_F32 && pj->w_dtype != DA_BF16)
+        return fail(DA_EUNSUPPORTED, "args", "projection weights must be f32 or bf16");
+    if (pj->out_dim < 1 || pj->out_dim > kProjMaxOut)
+        return fail(DA_EUNSUPPORTED, "args", "projection out_dim %d outside [1, %d]", pj->out_dim,
+                    kProjMaxOut);
+    if (a->v_dim % 8 || a->v_dim > kProjMaxVdim)
+        return fail(DA_EUNSUPPORTED, "args",
+                    "a projected v_dim must be a multiple of 8 and at most %d", kProjMaxVdim);
+    *norm = *pj;
+    if (!norm->row_stride) norm->row_stride = a->v_dim;
+    if (!norm->head_stride) norm->head_stride = (int64_t)pj->out_dim * norm->row_stride;
+    const int es = dtype_size(pj->w_dtype);
+    if (!aligned(pj->w, 16) || (norm->row_stride * es) % 16 || (norm->head_stride * es) % 16)
+        return fail(DA_EINVAL, "args",
+                    "projection weights and their strides must be 16-byte aligned");
+    if (norm->row_stride < a->v_dim || norm->head_stride < 0)
+        return fail(DA_EINVAL, "args", "projection row_stride %lld < v_dim %d",
+                    (long long)norm->row_stride, a->v_dim);
+    return DA_OK;
+}
+
 int launch_combine_phase(const da_args_t *a, const da_plan_t *pl, const void *ws, void *out,
-                         cudaStream_t st, int n_ranks = 1)
+                         cudaStream_t st, int n_ranks = 1, const da_proj_t *proj = nullptr)
 {
     CombineParams c;
     std::memset(&c, 0, sizeof c);
@@ -394,7 +419,20 @@ int launch_combine_phase(const da_args_t *a, const da_plan_t *pl, const void *ws
         c.n_splits[b] = pl->n_splits[b];
         c.split_base[b] = pl->split_base[b];
     }
-    cudaError_t e = launch_combine(a->out_dtype, a->v_dim, c, rows_of(a), a->batch, st, true);
+    cudaError_t e;
+    if (proj) {
+        c.w = proj->w;
+        c.w_head_stride = proj->head_stride;
+        c.w_row_stride = proj->row_stride;
+        c.out_dim = proj->out_dim;
+        c.w_heads = a->n_heads;
+        c.status = reinterpret_cast<int *>(const_cast<uint8_t *>(w));
+        c.timeout_ns = (uint64_t)(a->timeout_us > 0 ? a->timeout_us : 2000000) * 1000ull;
+        c.flags = a->flags;
+        e = launch_combine_proj(a->out_dtype, proj->w_dtype, c, rows_of(a), a->batch, st, true);
+    } else {
+        e = launch_combine(a->out_dtype, a->v_dim, c, rows_of(a), a->batch, st, true);
+    }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(DA_ELAUNCH, "combine", "%s", cudaGetErrorString(e));
     return DA_OK;
@@ -585,6 +623,57 @@ int decode_attn_combine_ranks(const da_args_t *a, const da_plan_t *plan, const v
                                 n_ranks);
 }
 
+int decode_attn_combine_proj(const da_args_t *a, const da_plan_t *plan, const da_proj_t *proj,
+                             const void *ws, int n_ranks, void *out, da_stream_t stream)
+{
+    int rc = check_args(a);
+    if (rc) return rc;
+    KernelChoice kc;
+    rc = check_plan(a, plan, &kc);
+    if (rc) return rc;
+    da_proj_t pj;
+    rc = check_proj(a, proj, &pj);
+    if (rc) return rc;
+    if (n_ranks < 1 || n_ranks > 4096)
+        return fail(DA_EINVAL, "args", "n_ranks %d outside [1, 4096]", n_ranks);
+    if (!ws || !aligned(ws, 256)) return fail(DA_EINVAL, "args", "workspaces misaligned or NULL");
+    if (!out || !aligned(out, 16)) return fail(DA_EINVAL, "args", "out misaligned or NULL");
+    cudaError_t pre = cudaGetLastError();
+    if (pre != cudaSuccess)
+        return fail(DA_ECUDA, "before combine", "pending CUDA error: %s",
+                    cudaGetErrorString(pre));
+    return launch_combine_phase(a, plan, ws, out, reinterpret_cast<cudaStream_t>(stream),
+                                n_ranks, &pj);
+}
+
+int decode_attn_splitk_proj(const da_args_t *a, const da_plan_t *plan, const da_proj_t *proj,
+                            const float *q, const void *k, const void *v, void *out, void *ws,
+                            size_t ws_bytes, da_stream_t stream)
+{
+    int rc = check_args(a);
+    if (rc) return rc;
+    KernelChoice kc;
+    rc = check_plan(a, plan, &kc);
+    if (rc) return rc;
+    da_proj_t pj;
+    rc = check_proj(a, proj, &pj);
+    if (rc) return rc;
+    rc = check_buffers(kc.kernel, q, k, v, out);
+    if (rc) return rc;
+    if (!ws || !aligned(ws, 256))
+        return fail(DA_EINVAL, "args", "workspace must be non-NULL and 256-byte aligned");
+    if ((int64_t)ws_bytes < plan->workspace_bytes)
+        return fail(DA_ENOSPACE, "args", "workspace %zu bytes < %lld needed", ws_bytes,
+                    (long long)plan->workspace_bytes);
+    cudaError_t pre = cudaGetLastError();
+    if (pre != cudaSuccess)
+        return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    rc = launch_split(a, plan, q, k, v, ws, st, nullptr);
+    if (rc) return rc;
+    return launch_combine_phase(a, plan, ws, out, st, 1, &pj);
+}
+
 int decode_attn_combine(const da_args_t *a, const da_plan_t *plan, const void *ws, void *out,
                         da_stream_t stream)
 {
@@ -665,7 +754,10 @@ int decode_attn_device_status(void *ws, da_stream_t stream)
     cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice);
     const int code = v & 0xff, kernel = (v >> 8) & 0xff;
     if (code == DA_ETIMEOUT)
-        return fail(DA_ETIMEOUT, kernel == DA_KERNEL_MLA_TC ? "split (mla)" : "split (gqa)",
+        return fail(DA_ETIMEOUT,
+                    kernel == DA_KERNEL_MLA_TC ? "split (mla)"
+                    : kernel == (kStatusTimeoutProj >> 8) ? "combine (projection)"
+                                                          : "split (gqa)",
                     "a bounded in-kernel wait ran out");
     return fail(DA_ECUDA, "status", "unexpected status word 0x%x", v);
 }

@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -49,6 +51,17 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 
     *reinterpret_cast<uint2 *>(p) = u;
 }
 
+template <typename OT> __device__ __forceinline__ void store1(OT *p, float v);
+template <> __device__ __forceinline__ void store1<float>(float *p, float v) { *p = v; }
+template <> __device__ __forceinline__ void store1<__half>(__half *p, float v)
+{
+    *p = __float2half_rn(v);
+}
+template <> __device__ __forceinline__ void store1<__nv_bfloat16>(__nv_bfloat16 *p, float v)
+{
+    *p = __float2bfloat16_rn(v);
+}
+
 __device__ __forceinline__ void fma4(float4 &a, float w, const float4 &v)
 {
     a.x = fmaf(w, v.x, a.x);
@@ -57,20 +70,18 @@ __device__ __forceinline__ void fma4(float4 &a, float w, const float4 &v)
     a.w = fmaf(w, v.w, a.w);
 }
 
-template <typename OT>
-__global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(const __grid_constant__ CombineParams p)
+// Merge the partials of row h of sequence b over the 128 value columns of
+// block z. Every warp takes part; warp 0 returns the normalised result of its
+// lane's four columns (the other warps' return values are not used). Ends with
+// the block barrier that makes part[] reusable.
+__device__ __forceinline__ float4 merge_columns(const CombineParams &p, int h, int b, int z,
+                                                float4 (*part)[32])
 {
-    __shared__ __align__(16) float4 part[kCombineWarps][32];
-
-    griddep_wait();
-
-    const int h = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.n_splits[b];
     const int SR = S * p.n_ranks;                            // (rank, split) pairs
     const size_t slot0 = (size_t)p.split_base[b];
-    const int col = blockIdx.z * kCombineCols + lane * 4;
+    const int col = z * kCombineCols + lane * 4;
     const bool live = col < p.v_dim;
     // pair i = r * S + s: rank r's split s
     auto ml_of = [&](int i) {
@@ -118,8 +129,9 @@ __global__ void __launch_bounds__(kCombineThreads)
     }
     part[warp][lane] = a;
     __syncthreads();
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == 0 && live) {
-        float4 t = part[0][lane];
+        t = part[0][lane];
 #pragma unroll
         for (int w = 1; w < kCombineWarps; ++w) {
             const float4 u = part[w][lane];
@@ -127,8 +139,147 @@ __global__ void __launch_bounds__(kCombineThreads)
         }
         const float inv = 1.f / L;
         t.x *= inv; t.y *= inv; t.z *= inv; t.w *= inv;
+    }
+    return t;
+}
+
+template <typename OT>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const __grid_constant__ CombineParams p)
+{
+    __shared__ __align__(16) float4 part[kCombineWarps][32];
+
+    griddep_wait();
+
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const float4 t = merge_columns(p, h, b, blockIdx.z, part);
+    const int col = blockIdx.z * kCombineCols + lane * 4;
+    if (threadIdx.x < 32 && col < p.v_dim) {
         OT *out = reinterpret_cast<OT *>(p.out) + ((size_t)b * p.n_heads + h) * p.v_dim + col;
         store4<OT>(out, t);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Combine fused with the per-head output projection (the MLA value
+// up-projection wv_b): out[b][h][e] = sum_c W[h][e][c] merged[b][h][c]. The
+// projection is a function of the merged result, not of any one partial, so it
+// runs after the merge and never per split ("The Kernel Level" / PR #49
+// write-up: the output projection moves into the combine).
+//
+// A cluster of Z = ceil(v_dim / 128) CTAs serves one (row, sequence); CTA z
+// merges the columns [128 z, 128 z + 128) as the plain combine does, projects
+// them with its slice W[h][:][128 z ...] (held in shared memory) into out_dim
+// partial sums, and the cluster adds the Z partial vectors through distributed
+// shared memory in a fixed order (bit-reproducible). The weight slice is
+// fetched with bulk copies before griddepcontrol.wait, so its load overlaps the
+// tail of the split kernel.
+template <typename WT> struct WLoad;
+template <> struct WLoad<float> {
+    static __device__ __forceinline__ float4 get(const unsigned char *row, int c)
+    {
+        return *reinterpret_cast<const float4 *>(row + c * 4);
+    }
+};
+template <> struct WLoad<__nv_bfloat16> {
+    static __device__ __forceinline__ float4 get(const unsigned char *row, int c)
+    {
+        const uint2 u = *reinterpret_cast<const uint2 *>(row + c * 2);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+};
+
+int combine_proj_smem_bytes(int w_dtype, int out_dim)
+{
+    const int es = w_dtype == DA_BF16 ? 2 : 4;
+    // W slice [out_dim][128] | partial outputs [out_dim] | mbarrier
+    return out_dim * kCombineCols * es + ((out_dim * 4 + 15) / 16) * 16 + 16;
+}
+
+template <typename OT, typename WT>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_proj_kernel(const __grid_constant__ CombineParams p)
+{
+    __shared__ __align__(16) float4 part[kCombineWarps][32];
+    __shared__ __align__(16) float merged[kCombineCols];
+    extern __shared__ __align__(128) unsigned char dsm[];
+    constexpr int ES = sizeof(WT);
+    unsigned char *wsl = dsm;                                           // [out_dim][128] WT
+    float *po = reinterpret_cast<float *>(dsm + p.out_dim * kCombineCols * ES);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(
+        dsm + p.out_dim * kCombineCols * ES + ((p.out_dim * 4 + 15) / 16) * 16);
+
+    const int h = blockIdx.x, b = blockIdx.y, z = blockIdx.z, Z = gridDim.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = z * kCombineCols;
+    const int ncols = min(kCombineCols, p.v_dim - c0);
+    const uint32_t row_bytes = (uint32_t)(ncols * ES);
+
+    // the weight slice of this CTA: out_dim rows of ncols elements
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool load_w = !(p.flags & DA_FLAG_TEST_NO_TMA);
+    if (threadIdx.x == 0 && load_w) mbar_arrive_expect_tx(bar, row_bytes * p.out_dim);
+    if (load_w) {
+        const unsigned char *w0 = static_cast<const unsigned char *>(p.w) +
+                                  ((size_t)(h % p.w_heads) * p.w_head_stride + c0) * ES;
+        for (int e = threadIdx.x; e < p.out_dim; e += kCombineThreads)
+            bulk_load_g2s(wsl + (size_t)e * kCombineCols * ES,
+                          w0 + (size_t)e * p.w_row_stride * ES, row_bytes, bar);
+    }
+
+    griddep_wait();
+
+    const float4 t = merge_columns(p, h, b, z, part);
+    if (warp == 0) reinterpret_cast<float4 *>(merged)[lane] = t; // zeros past v_dim
+    __syncthreads();
+
+    // every thread waits for the slice; a wait that runs out (or a slice never
+    // requested, the test hook) leaves this CTA's partial sums at zero and
+    // records the timeout, and the cluster still meets at both barriers
+    bool have_w = load_w;
+    if (have_w) {
+        volatile int never = 0;
+        have_w = mbar_wait_bounded(bar, 0, p.timeout_ns, &never);
+    }
+    if (!have_w && threadIdx.x == 0) atomicCAS(p.status, 0, kStatusTimeoutProj);
+
+    // partial projection: warp w takes rows w, w + 8, ...; lane l its 4 columns
+    const bool live = lane * 4 < ncols;
+    const float4 m4 = reinterpret_cast<const float4 *>(merged)[lane];
+    for (int e = warp; e < p.out_dim; e += kCombineWarps) {
+        float v = 0.f;
+        if (have_w && live) {
+            const float4 w4 = WLoad<WT>::get(wsl + (size_t)e * kCombineCols * ES, lane * 4);
+            v = fmaf(w4.x, m4.x, fmaf(w4.y, m4.y, fmaf(w4.z, m4.z, w4.w * m4.w)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) po[e] = v;
+    }
+    __syncthreads();
+    cluster_sync_all(); // every CTA's po is written and visible in the cluster
+
+    // CTA z adds the Z partial vectors for its share of the out_dim rows
+    const int per = (p.out_dim + Z - 1) / Z;
+    const int e = z * per + (int)threadIdx.x;
+    if ((int)threadIdx.x < per && e < p.out_dim) {
+        const uint32_t a = smem_u32(po + e);
+        float sum = 0.f;
+        for (int r = 0; r < Z; ++r) sum += ld_cluster_f32(map_to_rank(a, r));
+        OT *out = reinterpret_cast<OT *>(p.out) + ((size_t)b * p.n_heads + h) * p.out_dim + e;
+        store1<OT>(out, sum);
+    }
+    cluster_sync_all(); // the peers have read this CTA's po
+    if (!have_w && load_w) {
+        // copies still in flight must land before the CTA's memory is released
+        volatile int never = 0;
+        (void)mbar_wait_bounded(bar, 0, p.timeout_ns, &never);
     }
 }
 
@@ -150,6 +301,53 @@ cudaError_t launch_combine(int out_dtype, int v_dim, const CombineParams &p, int
     case DA_F32: return cudaLaunchKernelEx(&cfg, combine_kernel<float>, p);
     case DA_F16: return cudaLaunchKernelEx(&cfg, combine_kernel<__half>, p);
     case DA_BF16: return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename OT, typename WT>
+cudaError_t launch_proj_t(const CombineParams &p, int grid_x, int grid_y, cudaStream_t stream,
+                          bool pdl)
+{
+    const int smem = combine_proj_smem_bytes(std::is_same<WT, float>::value ? DA_F32 : DA_BF16,
+                                             p.out_dim);
+    cudaError_t e = cudaFuncSetAttribute(combine_proj_kernel<OT, WT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int Z = (p.v_dim + kCombineCols - 1) / kCombineCols;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_x, grid_y, Z);
+    cfg.blockDim = dim3(kCombineThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = Z;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, combine_proj_kernel<OT, WT>, p);
+}
+
+cudaError_t launch_combine_proj(int out_dtype, int w_dtype, const CombineParams &p, int grid_x,
+                                int grid_y, cudaStream_t stream, bool pdl)
+{
+    const int Z = (p.v_dim + kCombineCols - 1) / kCombineCols;
+    if (p.v_dim % 8 != 0 || Z > 8 || p.out_dim < 1 || p.out_dim > kProjMaxOut)
+        return cudaErrorInvalidValue;
+    const bool bf = w_dtype == DA_BF16;
+    if (!bf && w_dtype != DA_F32) return cudaErrorInvalidValue;
+    switch (out_dtype) {
+    case DA_F32: return bf ? launch_proj_t<float, __nv_bfloat16>(p, grid_x, grid_y, stream, pdl)
+                           : launch_proj_t<float, float>(p, grid_x, grid_y, stream, pdl);
+    case DA_F16: return bf ? launch_proj_t<__half, __nv_bfloat16>(p, grid_x, grid_y, stream, pdl)
+                           : launch_proj_t<__half, float>(p, grid_x, grid_y, stream, pdl);
+    case DA_BF16:
+        return bf ? launch_proj_t<__nv_bfloat16, __nv_bfloat16>(p, grid_x, grid_y, stream, pdl)
+                  : launch_proj_t<__nv_bfloat16, float>(p, grid_x, grid_y, stream, pdl);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -33,6 +33,7 @@ inline int64_t ws_total(int64_t total_splits, int n_heads, int v_dim)
 // Status word codes written by kernels (low byte = da_status_t, next byte = kernel).
 constexpr int kStatusTimeoutGqa = DA_ETIMEOUT | (DA_KERNEL_GQA_TMA << 8);
 constexpr int kStatusTimeoutMla = DA_ETIMEOUT | (DA_KERNEL_MLA_TC << 8);
+constexpr int kStatusTimeoutProj = DA_ETIMEOUT | (3 << 8); // combine with the projection
 
 // Per-launch description of the work items shared by the split kernels.
 struct ItemTable {
@@ -107,6 +108,16 @@ struct CombineParams {
     int32_t n_ranks;
     int64_t rank_ml;
     int64_t rank_acc;
+    // the per-head output projection of combine_proj_kernel: out row e of row h
+    // is sum_c w[(h % w_heads) * w_head_stride + e * w_row_stride + c] * merged[c]
+    const void *w;
+    int64_t w_head_stride;
+    int64_t w_row_stride;
+    int32_t out_dim;
+    int32_t w_heads;
+    int *status;             // workspace status word (a timed-out weight load)
+    uint64_t timeout_ns;
+    int32_t flags;
     int32_t n_splits[DA_MAX_BATCH];
     int32_t split_base[DA_MAX_BATCH];
 };
@@ -130,5 +141,12 @@ bool gqa_config(int kv_dtype, int head_dim, int group, GqaConfig *cfg);
 
 cudaError_t launch_combine(int out_dtype, int v_dim, const CombineParams &p, int grid_x,
                            int grid_y, cudaStream_t stream, bool pdl);
+// combine fused with the per-head output projection: clusters of ceil(v_dim /
+// 128) CTAs (at most 8), each merging 128 columns and projecting them
+constexpr int kProjMaxOut = 256;
+constexpr int kProjMaxVdim = 1024;
+int combine_proj_smem_bytes(int w_dtype, int out_dim);
+cudaError_t launch_combine_proj(int out_dtype, int w_dtype, const CombineParams &p, int grid_x,
+                                int grid_y, cudaStream_t stream, bool pdl);
 
 } // namespace skv

@@ -45,11 +45,14 @@ def test_struct_layout_matches_the_c_compiler():
 #include <stddef.h>
 #include "split_kv_decode.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(da_args_t), sizeof(da_plan_t),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n",
+         sizeof(da_args_t), sizeof(da_plan_t),
          offsetof(da_args_t, k_batch_stride), offsetof(da_args_t, scale),
          offsetof(da_plan_t, seq_lens), offsetof(da_plan_t, workspace_bytes),
          offsetof(da_plan_t, est_cost), sizeof(da_dev_t), offsetof(da_dev_t, max_blocks_per_seq),
-         offsetof(da_dev_t, num_blocks), offsetof(da_dev_t, v_block_stride));
+         offsetof(da_dev_t, num_blocks), offsetof(da_dev_t, v_block_stride),
+         offsetof(da_args_t, q_len), sizeof(da_proj_t), offsetof(da_proj_t, out_dim),
+         offsetof(da_proj_t, head_stride), offsetof(da_proj_t, row_stride));
   return 0;
 }
 """
@@ -63,7 +66,9 @@ int main(void) {
     want = [ctypes.sizeof(N.DaArgs), ctypes.sizeof(N.DaPlan), N.DaArgs.k_batch_stride.offset,
             N.DaArgs.scale.offset, N.DaPlan.seq_lens.offset, N.DaPlan.workspace_bytes.offset,
             N.DaPlan.est_cost.offset, ctypes.sizeof(N.DaDev), N.DaDev.max_blocks_per_seq.offset,
-            N.DaDev.num_blocks.offset, N.DaDev.v_block_stride.offset]
+            N.DaDev.num_blocks.offset, N.DaDev.v_block_stride.offset, N.DaArgs.q_len.offset,
+            ctypes.sizeof(N.DaProj), N.DaProj.out_dim.offset, N.DaProj.head_stride.offset,
+            N.DaProj.row_stride.offset]
     assert got == want
 
 
@@ -480,3 +485,38 @@ def test_mla_refuses_multi_token(lib):
     rc, _ = plan(lib, a, [4096])
     assert rc == N.DA_EUNSUPPORTED
     assert "one query token" in lib.decode_attn_last_error().decode()
+
+
+# ---------------------------------------------------------------------------
+# the combine fused with a per-head projection: validation before any launch
+# ---------------------------------------------------------------------------
+def _proj(w=1 << 20, dt=N.DA_F32, out_dim=128, hs=0, rs=0):
+    p = N.DaProj()
+    p.w, p.w_dtype, p.out_dim, p.head_stride, p.row_stride = w, dt, out_dim, hs, rs
+    return p
+
+
+@pytest.mark.parametrize("proj,status,msg", [
+    (_proj(w=0), N.DA_EINVAL, "NULL"),
+    (_proj(dt=N.DA_F16), N.DA_EUNSUPPORTED, "f32 or bf16"),
+    (_proj(out_dim=0), N.DA_EUNSUPPORTED, "out_dim"),
+    (_proj(out_dim=257), N.DA_EUNSUPPORTED, "out_dim"),
+    (_proj(w=(1 << 20) | 8), N.DA_EINVAL, "aligned"),
+    (_proj(rs=258), N.DA_EINVAL, "aligned"),            # 1032 B rows: not a 16-byte multiple
+    (_proj(rs=128), N.DA_EINVAL, "row_stride"),
+    (_proj(dt=N.DA_BF16, hs=4), N.DA_EINVAL, "aligned"),
+])
+def test_combine_proj_validates_weights(lib, proj, status, msg):
+    a = args(cap=4096)
+    rc, p = plan(lib, a, [4096])
+    assert rc == 0
+    P = ctypes.c_void_p
+    fake = P(1 << 21)                        # never dereferenced: validation fails first
+    rc = lib.decode_attn_combine_proj(ctypes.byref(a), ctypes.byref(p), ctypes.byref(proj),
+                                      fake, 1, fake, None)
+    assert rc == status
+    assert msg in lib.decode_attn_last_error().decode()
+    rc = lib.decode_attn_splitk_proj(ctypes.byref(a), ctypes.byref(p), ctypes.byref(proj), fake,
+                                     fake, fake, fake, fake, p.workspace_bytes, None)
+    assert rc == status
+

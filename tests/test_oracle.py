@@ -347,3 +347,69 @@ def test_multi_token_rejects_short_sequences():
     c, q = _multi(2, 1, 8, [2, 9], 3, seed=2)
     with pytest.raises(ValueError):
         oracle.attention_multi(q, c.k, c.v, c.seq_lens, c.scale)
+
+
+# ---------------------------------------------------------------------------
+# attention followed by a per-head projection (wv_b)
+# ---------------------------------------------------------------------------
+def _proj_weights(h, e, c, seed, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn((h, e, c), generator=g) / math.sqrt(c)).to(dtype)
+
+
+def test_projection_equals_attention_over_projected_values():
+    # (P V) W^T = P (V W^T): project every value row with head h's matrix first,
+    # then run materialised attention for that head alone
+    c = small(6, 1, 24, [1, 9, 40], dv=16, cap=41, seed=21, shared=True)
+    W_ = _proj_weights(6, 8, 16, 22)
+    got = oracle.attention_proj(c.q, c.k, c.v, c.seq_lens, c.scale, W_, v_dim=16)
+    Wn = widen(W_)
+    V = widen(c.v)[..., :16]
+    for h in range(6):
+        Vh = np.einsum("bpkc,ec->bpke", V, Wn[h])            # [B, cap, 1, out]
+        ref = naive_attention(widen(c.q)[:, h:h + 1], widen(c.k), Vh, c.seq_lens, c.scale)
+        assert np.max(np.abs(got[:, h] - ref[:, 0])) <= 1e-13 * np.max(np.abs(ref))
+
+
+def test_projection_identity_and_selectors_are_exact():
+    c = small(4, 2, 16, [5, 33], seed=23)
+    att = run_oracle(c)
+    eye = torch.eye(16).expand(4, 16, 16).contiguous()
+    assert np.array_equal(oracle.attention_proj(c.q, c.k, c.v, c.seq_lens, c.scale, eye), att)
+    sel = torch.zeros(4, 3, 16)
+    for h in range(4):
+        for e, col in enumerate((h, 15 - h, 7)):
+            sel[h, e, col] = 1.0
+    got = oracle.attention_proj(c.q, c.k, c.v, c.seq_lens, c.scale, sel)
+    for h in range(4):
+        assert np.array_equal(got[:, h], att[:, h][:, [h, 15 - h, 7]])
+
+
+def test_projection_bf16_weights_widen_exactly_and_pairs_match():
+    c = small(4, 1, 16, [12, 30], seed=25)
+    Wb = _proj_weights(4, 8, 16, 26, torch.bfloat16)
+    full = oracle.attention_proj(c.q, c.k, c.v, c.seq_lens, c.scale, Wb)
+    ref = np.einsum("bhc,hec->bhe", run_oracle(c), Wb.to(torch.float64).numpy())
+    assert np.array_equal(full, ref)
+    pairs = [(1, 3), (0, 0), (1, 1)]
+    got = oracle.attention_proj(c.q, c.k, c.v, c.seq_lens, c.scale, Wb, pairs=pairs)
+    for i, (b, h) in enumerate(pairs):
+        assert np.array_equal(got[i], full[b, h])
+
+
+def test_projection_multi_token_uses_each_heads_matrix():
+    c, q = _multi(4, 2, 16, [6, 20], 2, seed=27)
+    W_ = _proj_weights(4, 5, 16, 28)
+    got = oracle.attention_proj(q, c.k, c.v, c.seq_lens, c.scale, W_)
+    ref = np.einsum("bthc,hec->bthe", naive_causal_attention(q, c.k, c.v, c.seq_lens, c.scale),
+                    widen(W_))
+    assert got.shape == (2, 2, 4, 5)
+    assert np.max(np.abs(got - ref)) <= 1e-13 * np.max(np.abs(ref))
+
+
+def test_projection_negative_control_transposed_weights_are_caught():
+    c = small(2, 1, 16, [25], seed=29)
+    W_ = _proj_weights(2, 16, 16, 30)
+    good = oracle.attention_proj(c.q, c.k, c.v, c.seq_lens, c.scale, W_)
+    bad = oracle.attention_proj(c.q, c.k, c.v, c.seq_lens, c.scale, W_.transpose(1, 2))
+    assert np.max(np.abs(good - bad)) > 1e-2
