@@ -316,7 +316,9 @@ def main():
         for _ in range(20):
             combine(step())
         torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # the timed steps: events only around the whole step, so the combine's
+    # programmatic launch overlaps the split kernel's tail as it does in use
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -324,20 +326,28 @@ def main():
     for i in range(args.steps):
         flush.fill_(float(i))
         ev[i][0].record(stream)
-        p = step()
+        combine(step())
         ev[i][1].record(stream)
-        combine(p)
-        ev[i][2].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
+    # the split kernel alone (for its roofline): the same launches, events
+    # around the split launch only, L2 flushed before each
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        evs[i][0].record(stream)
+        p = step()
+        evs[i][1].record(stream)
+        combine(p)
+    torch.cuda.synchronize()
     clocks = sampler.stop()
-    clocks["window"] = "untimed soak (0.6 s) + timed steps"
+    clocks["window"] = "untimed soak (0.6 s) + timed steps + split-only steps"
     if world > 1:
         dist.barrier()
     A.decode_attn_device_status(ws, stream)
 
-    step_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(args.steps)]
-    split_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(args.steps)]
+    step_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(args.steps)]
+    split_us = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in range(args.steps)]
     total_us = max_over_ranks(sum(step_us), dev)
     value = total_us / (args.steps * world)                # µs per layer-step, whole job
     split_mean = statistics.mean(split_us)
@@ -495,31 +505,42 @@ def measure_wv_b(case, q, k, v, out_dt, dev, flush, args, wdt):
 
 
 def measure_multi_token(case, k, v, out_dt, dev, flush, args):
-    """The same caches with the largest q_len (new tokens per sequence, causal
-    among themselves) whose query rows per KV head still fit one kernel group:
-    every K/V tile is read once for all of them."""
+    """The same caches with q_len = 2, 4, 8 new tokens per sequence (causal among
+    themselves): every K/V tile is read once for all of them. Query rows per KV
+    head (heads per KV head x q_len) of 8 to 128 run on the tensor-core kernel
+    (16-bit caches); the SIMT kernel takes up to 8 rows."""
     import torch
     from split_kv_decode_gb300 import api as A
+    from split_kv_decode_gb300 import _native as N
     from split_kv_decode_gb300 import workloads as W
     G = case.n_heads // case.n_kv_heads
-    q_len = max((t for t in (2, 4, 8) if G * t in (2, 4, 6, 8)), default=0)
-    if not q_len or int(case.seq_lens.min()) < q_len:
+    res = {}
+    for q_len in (2, 4, 8):
+        rows = G * q_len
+        if int(case.seq_lens.min()) < q_len:
+            continue
+        if not (rows in (2, 4, 6, 8) or (case.kv_dtype in ("f16", "bf16") and 8 <= rows <= 128)):
+            continue
+        q = W.multi_token_q(case.batch, q_len, case.n_heads, case.head_dim).to(dev)
+        a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
+        p = A.decode_attn_plan(a, case.seq_lens.tolist())
+        ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
+        out = torch.empty(case.batch, q_len, case.n_heads, case.v_dim, dtype=out_dt, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        for _ in range(3):
+            A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
+        n = max(20, min(args.steps, 200))
+        us = _timed_steps(lambda: A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream),
+                          flush, n, stream)
+        res[f"q_len_{q_len}"] = {
+            "value": round(us, 2), "unit": "us/layer-step", "steps": n, "rows_per_item": rows,
+            "kernel": "gqa_tc_kernel" if p.kernel == N.DA_KERNEL_GQA_TC else "gqa_split_kernel",
+            "kv_gbs": round(case.kv_bytes / (us * 1e-6) / 1e9, 1)}
+    if not res:
         return None
-    q = W.multi_token_q(case.batch, q_len, case.n_heads, case.head_dim).to(dev)
-    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
-    p = A.decode_attn_plan(a, case.seq_lens.tolist())
-    ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
-    out = torch.empty(case.batch, q_len, case.n_heads, case.v_dim, dtype=out_dt, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    for _ in range(3):
-        A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
-    n = max(20, min(args.steps, 200))
-    us = _timed_steps(lambda: A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream),
-                      flush, n, stream)
-    return {"value": round(us, 2), "unit": "us/layer-step", "steps": n, "q_len": q_len,
-            "kv_gbs": round(case.kv_bytes / (us * 1e-6) / 1e9, 1),
-            "what": f"split + combine for {q_len} new tokens per sequence, causal among "
-                    "themselves, sharing every K/V tile"}
+    res["what"] = ("split + combine for q_len new tokens per sequence, causal among "
+                   "themselves, sharing every K/V tile")
+    return res
 
 
 def measure_e2e(case, q_dev, out_dt, dev, stream, args):

@@ -65,6 +65,8 @@ typedef enum {
 
 /* da_args_t.flags */
 #define DA_FLAG_NO_COMBINE 0x1   /* decode_attn_splitk_ex runs the split kernel only */
+#define DA_FLAG_GQA_SIMT 0x2     /* for 16-bit caches with 8 rows per work item (see
+                                    DA_KERNEL_GQA_TC), use the SIMT kernel instead  */
 #define DA_FLAG_TEST_NO_TMA 0x100 /* test hook: the producer issues no copy, so every
                                      consumer wait runs out after timeout_us and the
                                      kernel reports DA_ETIMEOUT through device_status */
@@ -72,6 +74,10 @@ typedef enum {
 /* Kernels the planner can choose (da_plan_t.kernel). */
 #define DA_KERNEL_GQA_TMA 1 /* SIMT split kernel, TMA-staged K/V tiles (GQA, MQA) */
 #define DA_KERNEL_MLA_TC 2  /* tcgen05/TMEM split kernel for MLA (576/512 latent)  */
+#define DA_KERNEL_GQA_TC 3  /* tcgen05/TMEM split kernel for GQA/MQA work items of
+                               8 to 128 query rows ((n_heads / n_kv_heads) * q_len),
+                               f16 or bf16 caches, head_dim 128 or 256; q and the
+                               probabilities are rounded to the cache type         */
 
 typedef struct {
     int32_t batch;       /* 1 .. DA_MAX_BATCH                                  */

@@ -145,12 +145,6 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
     if (a->head_dim != a->v_dim)
         return fail(DA_EUNSUPPORTED, "plan", "GQA kernel needs v_dim == head_dim (got %d, %d)",
                     a->head_dim, a->v_dim);
-    GqaConfig cfg;
-    if (!gqa_config_any(a->kv_dtype, a->head_dim, G, &cfg))
-        return fail(DA_EUNSUPPORTED, "plan",
-                    "no GQA kernel for head_dim %d, group %d (heads per KV head x q_len), "
-                    "%s KV (head_dim 128 or 256; group 1, 2, 4, 6 or 8)",
-                    a->head_dim, G, dtype_name(a->kv_dtype));
     const int64_t st[6] = {a->k_pos_stride, a->k_head_stride, a->v_pos_stride,
                            a->v_head_stride, a->batch > 1 ? a->k_batch_stride : 0,
                            a->batch > 1 ? a->v_batch_stride : 0};
@@ -158,6 +152,23 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
         if ((st[i] * es) % 16)
             return fail(DA_EUNSUPPORTED, "plan",
                         "cache strides must be multiples of 16 bytes for TMA tiles");
+    // many rows per item on a 16-bit cache: the tensor-core kernel
+    const bool tc_shape = es == 2 && (a->head_dim == 128 || a->head_dim == 256) && G >= 8 &&
+                          G <= 128;
+    if (tc_shape && !(G == 8 && (a->flags & DA_FLAG_GQA_SIMT))) {
+        kc->kernel = DA_KERNEL_GQA_TC;
+        kc->tile = kTcT;
+        kc->ctas_per_sm = 1;
+        kc->cluster = 1;
+        return DA_OK;
+    }
+    GqaConfig cfg;
+    if (!gqa_config_any(a->kv_dtype, a->head_dim, G, &cfg))
+        return fail(DA_EUNSUPPORTED, "plan",
+                    "no GQA kernel for head_dim %d, group %d (heads per KV head x q_len), "
+                    "%s KV (head_dim 128 or 256; group 1, 2, 4, 6 or 8, or 8 to 128 for a "
+                    "16-bit cache)",
+                    a->head_dim, G, dtype_name(a->kv_dtype));
     kc->kernel = DA_KERNEL_GQA_TMA;
     kc->tile = cfg.tile;
     kc->ctas_per_sm = cfg.ctas_per_sm;
@@ -195,9 +206,12 @@ CUtensorMapDataType tma_dtype(int dt)
     }
 }
 
-// 4-D map over (d, kv head, position, batch) with box (D, 1, rows, 1).
+// 4-D map over (d, kv head, position, batch) with box (box_d, 1, rows, 1):
+// box_d = D unswizzled (SIMT kernel), or 64 columns landing 128-byte-swizzled
+// (tensor-core kernel, sw128 = true).
 int encode_cache_map(CUtensorMap *map, const void *base, int dt, int D, int hkv, int cap,
-                     int batch, int64_t head_st, int64_t pos_st, int64_t batch_st, int rows)
+                     int batch, int64_t head_st, int64_t pos_st, int64_t batch_st, int rows,
+                     bool sw128 = false)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(DA_ECUDA, "tma", "cuTensorMapEncodeTiled is unavailable");
@@ -206,10 +220,11 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dt, int D, int hkv,
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)cap, (cuuint64_t)batch};
     cuuint64_t strides[3] = {(cuuint64_t)(head_st * es), (cuuint64_t)(pos_st * es),
                              (cuuint64_t)(batch_st * es)};
-    cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)rows, 1};
+    cuuint32_t box[4] = {(cuuint32_t)(sw128 ? 64 : D), 1, (cuuint32_t)rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, tma_dtype(dt), 4, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(DA_EUNSUPPORTED, "tma", "cuTensorMapEncodeTiled rejected the cache layout (%d)",
@@ -220,7 +235,8 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dt, int D, int hkv,
 // 4-D map over a paged pool (d, kv head, slot in block, block) with box
 // (D, 1, rows, 1); slots past block_size and blocks past num_blocks read zeros.
 int encode_pool_map(CUtensorMap *map, const void *base, int dt, int D, int hkv, int block_size,
-                    int num_blocks, int64_t head_st, int64_t pos_st, int64_t block_st, int rows)
+                    int num_blocks, int64_t head_st, int64_t pos_st, int64_t block_st, int rows,
+                    bool sw128 = false)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(DA_ECUDA, "tma", "cuTensorMapEncodeTiled is unavailable");
@@ -229,10 +245,11 @@ int encode_pool_map(CUtensorMap *map, const void *base, int dt, int D, int hkv, 
                           (cuuint64_t)num_blocks};
     cuuint64_t strides[3] = {(cuuint64_t)(head_st * es), (cuuint64_t)(pos_st * es),
                              (cuuint64_t)(block_st * es)};
-    cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)rows, 1};
+    cuuint32_t box[4] = {(cuuint32_t)(sw128 ? 64 : D), 1, (cuuint32_t)rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, tma_dtype(dt), 4, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(DA_EUNSUPPORTED, "tma", "cuTensorMapEncodeTiled rejected the paged pool (%d)",
@@ -339,6 +356,7 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
 
     CUtensorMap km, vm;
     int rc;
+    const bool tc = pl->kernel == DA_KERNEL_GQA_TC;
     if (dev && dev->block_table) {
         p.block_table = dev->block_table;
         p.max_blocks = dev->max_blocks_per_seq;
@@ -346,23 +364,28 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
         p.oob_block = dev->num_blocks;
         rc = encode_pool_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, dev->block_size,
                              dev->num_blocks, a->k_head_stride, a->k_pos_stride,
-                             dev->k_block_stride, pl->tile);
+                             dev->k_block_stride, pl->tile, tc);
         if (rc) return rc;
         rc = encode_pool_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, dev->block_size,
                              dev->num_blocks, a->v_head_stride, a->v_pos_stride,
-                             dev->v_block_stride, pl->tile);
+                             dev->v_block_stride, pl->tile, tc);
         if (rc) return rc;
     } else {
         rc = encode_cache_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, a->capacity,
                               a->batch, a->k_head_stride, a->k_pos_stride, a->k_batch_stride,
-                              pl->tile);
+                              pl->tile, tc);
         if (rc) return rc;
         rc = encode_cache_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, a->capacity,
                               a->batch, a->v_head_stride, a->v_pos_stride, a->v_batch_stride,
-                              pl->tile);
+                              pl->tile, tc);
         if (rc) return rc;
     }
     if (dev) p.dev_lens = dev->seq_lens;
+    if (tc) {
+        const cudaError_t e = launch_gqa_tc(a->kv_dtype, a->head_dim, pl->grid, st, km, vm, p);
+        if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
+        return DA_OK;
+    }
 
     const int G = a->n_heads / a->n_kv_heads * q_len_of(a);
     cudaError_t e;
@@ -755,7 +778,8 @@ int decode_attn_device_status(void *ws, da_stream_t stream)
     const int code = v & 0xff, kernel = (v >> 8) & 0xff;
     if (code == DA_ETIMEOUT)
         return fail(DA_ETIMEOUT,
-                    kernel == DA_KERNEL_MLA_TC ? "split (mla)"
+                    kernel == DA_KERNEL_MLA_TC   ? "split (mla)"
+                    : kernel == DA_KERNEL_GQA_TC ? "split (gqa, tensor cores)"
                     : kernel == (kStatusTimeoutProj >> 8) ? "combine (projection)"
                                                           : "split (gqa)",
                     "a bounded in-kernel wait ran out");

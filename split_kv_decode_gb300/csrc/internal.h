@@ -33,7 +33,8 @@ inline int64_t ws_total(int64_t total_splits, int n_heads, int v_dim)
 // Status word codes written by kernels (low byte = da_status_t, next byte = kernel).
 constexpr int kStatusTimeoutGqa = DA_ETIMEOUT | (DA_KERNEL_GQA_TMA << 8);
 constexpr int kStatusTimeoutMla = DA_ETIMEOUT | (DA_KERNEL_MLA_TC << 8);
-constexpr int kStatusTimeoutProj = DA_ETIMEOUT | (3 << 8); // combine with the projection
+constexpr int kStatusTimeoutTc = DA_ETIMEOUT | (DA_KERNEL_GQA_TC << 8);
+constexpr int kStatusTimeoutProj = DA_ETIMEOUT | (15 << 8); // combine with the projection
 
 // Per-launch description of the work items shared by the split kernels.
 struct ItemTable {
@@ -121,6 +122,50 @@ struct CombineParams {
     int32_t n_splits[DA_MAX_BATCH];
     int32_t split_base[DA_MAX_BATCH];
 };
+
+// Tensor-core GQA kernel (gqa_tc.cu): tiles of kTcT positions; shared-memory
+// layout for head_dim D and R rows per item (the same on host and device).
+constexpr int kTcT = 64;
+constexpr int kTcMaxStages = 6;
+constexpr int kTcBarriers = 32;
+constexpr int kTcSmemMax = 232448;
+struct TcLayout {
+    int chunk_bytes;  // one 64-column chunk of a tile: kTcT rows of 128 B
+    int tile_bytes;   // K (or V) tile: D / 64 chunks
+    int stage_bytes;  // K + V
+    int rpad, npv;    // rows rounded up to 8 (Q rows written), to 16 (PV N)
+    int qch;          // one 64-column chunk of Q: rpad rows of 128 B
+    int pslot;        // one P buffer: npv rows of 128 B
+    int nst;          // stages
+    int q_off, p_off, bar_off, misc_off, alpha_off, used;
+};
+__host__ __device__ inline TcLayout tc_layout(int D, int R)
+{
+    TcLayout L;
+    L.chunk_bytes = kTcT * 128;
+    L.tile_bytes = (D / 64) * L.chunk_bytes;
+    L.stage_bytes = 2 * L.tile_bytes;
+    L.rpad = (R + 7) / 8 * 8;
+    L.npv = (R + 15) / 16 * 16;
+    L.qch = L.rpad * 128;
+    L.pslot = L.npv * 128;
+    // the 128-row MMA reads 128 rows from the start of every Q chunk: past the
+    // last one it reads (128 - rpad) rows more
+    const int qbytes = (D / 64) * L.qch + (128 - L.rpad) * 128;
+    const int rest = (qbytes + 1023) / 1024 * 1024 + 2 * L.pslot + kTcBarriers * 8 + 16 +
+                     128 * 4 + 1024;
+    int nst = (kTcSmemMax - rest) / L.stage_bytes;
+    L.nst = nst > kTcMaxStages ? kTcMaxStages : nst;
+    L.q_off = L.nst * L.stage_bytes;
+    L.p_off = (L.q_off + qbytes + 1023) / 1024 * 1024;
+    L.bar_off = L.p_off + 2 * L.pslot;
+    L.misc_off = L.bar_off + kTcBarriers * 8;
+    L.alpha_off = L.misc_off + 16;
+    L.used = L.alpha_off + 128 * 4;
+    return L;
+}
+cudaError_t launch_gqa_tc(int kv_dtype, int head_dim, int grid, cudaStream_t st,
+                          const CUtensorMap &km, const CUtensorMap &vm, const SplitParams &p);
 
 // Launchers (return cudaError_t of the launch).
 struct GqaLaunch {

@@ -455,16 +455,48 @@ def test_plan_multi_token_groups(lib, hq, hkv, q_len):
     ml = p.total_splits * hq * q_len * 8
     acc = p.total_splits * hq * q_len * a.v_dim * 4
     assert p.workspace_bytes >= ml + acc
-    assert p.kernel == N.DA_KERNEL_GQA_TMA
+    # 8 or more rows per item on a 16-bit cache go to the tensor-core kernel
+    rows = hq // hkv * q_len
+    assert p.kernel == (N.DA_KERNEL_GQA_TC if rows >= 8 else N.DA_KERNEL_GQA_TMA)
 
 
-@pytest.mark.parametrize("hq,hkv,q_len", [(16, 4, 3), (8, 2, 4), (16, 1, 2)])
-def test_plan_multi_token_rejects_large_groups(lib, hq, hkv, q_len):
-    a = args(hq=hq, hkv=hkv, cap=8192)
+@pytest.mark.parametrize("hq,hkv,q_len,dt", [(16, 4, 3, N.DA_F32), (8, 2, 4, N.DA_F32),
+                                             (16, 1, 2, N.DA_F32), (64, 1, 4, N.DA_F16),
+                                             (128, 1, 2, N.DA_BF16)])
+def test_plan_multi_token_rejects_large_groups(lib, hq, hkv, q_len, dt):
+    a = args(hq=hq, hkv=hkv, cap=8192, dt=dt)
     a.q_len = q_len
     rc, _ = plan(lib, a, [8192])
     assert rc == N.DA_EUNSUPPORTED
     assert "q_len" in lib.decode_attn_last_error().decode()
+
+
+@pytest.mark.parametrize("hq,hkv,q_len,d,dt", [(32, 1, 1, 128, N.DA_F16), (16, 4, 4, 256, N.DA_BF16),
+                                               (64, 1, 2, 256, N.DA_F16), (8, 1, 1, 256, N.DA_BF16),
+                                               (16, 2, 8, 128, N.DA_F16)])
+def test_plan_tensor_core_gqa(lib, hq, hkv, q_len, d, dt):
+    a = args(batch=3, hq=hq, hkv=hkv, d=d, cap=20000, dt=dt)
+    a.q_len = q_len
+    lens = [q_len, 777, 20000]
+    rc, p = plan(lib, a, lens)
+    assert rc == 0, lib.decode_attn_last_error().decode()
+    assert p.kernel == N.DA_KERNEL_GQA_TC and p.tile == 64 and p.ctas_per_sm == 1
+    base = 0
+    for b, L in enumerate(lens):
+        assert p.chunk[b] % 64 == 0 and p.n_splits[b] == -(-L // p.chunk[b])
+        assert p.split_base[b] == base
+        base += p.n_splits[b]
+    assert p.n_items == base * hkv and 1 <= p.grid <= min(152, p.n_items)
+
+
+def test_plan_simt_flag_keeps_eight_row_groups_on_the_simt_kernel(lib):
+    a = args(hq=8, hkv=1, d=256, cap=4096, dt=N.DA_F16)
+    assert plan(lib, a, [4096])[1].kernel == N.DA_KERNEL_GQA_TC
+    a.flags = N.DA_FLAG_GQA_SIMT
+    assert plan(lib, a, [4096])[1].kernel == N.DA_KERNEL_GQA_TMA
+    a = args(hq=16, hkv=1, d=256, cap=4096, dt=N.DA_F16)  # 16 rows: tensor cores only
+    a.flags = N.DA_FLAG_GQA_SIMT
+    assert plan(lib, a, [4096])[1].kernel == N.DA_KERNEL_GQA_TC
 
 
 def test_plan_multi_token_needs_q_len_positions(lib):
