@@ -157,7 +157,7 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
                           G <= 128;
     if (tc_shape && !(G == 8 && (a->flags & DA_FLAG_GQA_SIMT))) {
         kc->kernel = DA_KERNEL_GQA_TC;
-        kc->tile = kTcT;
+        kc->tile = tc_tile(a->head_dim);
         kc->ctas_per_sm = 1;
         kc->cluster = 1;
         return DA_OK;

@@ -17,9 +17,9 @@
 // TMA in 64-column boxes that land 128-byte-swizzled (the layout the MMA
 // reads), into a ring of stages; there is no conversion and no register
 // staging. Q (scale * log2 e folded in, rounded to the cache type) is written
-// once per item into the same swizzled K-major layout; rows R.. of the
-// 128-row MMA read past a Q chunk into the next one and give S rows that no
-// thread reads.
+// once per item into the same swizzled K-major layout at the start of shared
+// memory; rows R.. of the 128-row MMA read past a Q chunk into the next one
+// (past the last, into the first stage) and give S rows that no thread reads.
 //
 // Roles (6 warps, one CTA per SM):
 //   warps 0-3  softmax and epilogue: thread r owns row r (TMEM lane r of S):
@@ -51,7 +51,7 @@ constexpr int kTcThreads = 192;
 constexpr int kTcProd = 4;  // producer warp
 constexpr int kTcMma = 5;   // MMA warp
 constexpr float kTcTau = 8.f;
-constexpr int kTcOCol = 2 * kTcT; // O^T block j at kTcOCol + j * npv (after two S slots)
+constexpr int kTcOCol = 128; // O^T block j at kTcOCol + j * npv (after two S slots of T <= 64)
 
 // barrier indices
 constexpr int TB_FULL = 0, TB_EMPTY = kTcMaxStages, TB_SFULL = 2 * kTcMaxStages,
@@ -94,10 +94,10 @@ __device__ __forceinline__ bool tc_bar_or(bool pred)
 }
 
 // The (item, tile) sequence of a CTA, the same for every role: items
-// blockIdx.x, blockIdx.x + gridDim.x, ...; an item's tiles are kTcT positions,
+// blockIdx.x, blockIdx.x + gridDim.x, ...; an item's tiles are T positions,
 // cut at its end and (paged caches) at block ends; items without positions
 // (device lengths shorter than the plan's) have no tiles and are skipped.
-struct Walk {
+template <int T> struct Walk {
     int item, b, kvh, s, p0, p1, t0, t1, bend, gt;
     bool done, first;
     __device__ __forceinline__ void load_item(const SplitParams &p)
@@ -113,7 +113,7 @@ struct Walk {
         }
         t0 = p0;
         bend = first_block_end(p, p0);
-        t1 = tile_end<kTcT>(t0, p1, bend, p.block_size);
+        t1 = tile_end<T>(t0, p1, bend, p.block_size);
         first = true;
     }
     __device__ __forceinline__ void start(const SplitParams &p)
@@ -131,7 +131,7 @@ struct Walk {
             load_item(p);
         } else {
             t0 = t1;
-            t1 = tile_end<kTcT>(t0, p1, bend, p.block_size);
+            t1 = tile_end<T>(t0, p1, bend, p.block_size);
             first = false;
         }
     }
@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     gqa_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const __grid_constant__ SplitParams p)
 {
+    constexpr int T = tc_tile(D); // positions per tile: QK N, PV K
     constexpr int NCH = D / 64;   // 64-column chunks of a row
     constexpr int NBLK = D / 128; // 128-column blocks of O^T
     const int R = p.n_heads / p.items.n_kv_heads; // rows of an item
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int win_b = -1, win_lo = 0;
             int32_t win_entry = 0;
             bool ok = true;
-            Walk w;
+            Walk<T> w;
             for (w.start(p); !w.done; w.next(p)) {
                 const int st = w.gt % NST;
                 // a stage's first use finds its barrier's previous phase complete
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (lane == 0 && !(p.flags & DA_FLAG_TEST_NO_TMA)) {
                     // rows of a box past the block (or the pool, or the cache) read as zeros
-                    uint8_t *dst = sm + st * L.stage_bytes;
+                    uint8_t *dst = sm + L.stage_off + st * L.stage_bytes;
                     mbar_arrive_expect_tx(bar + TB_FULL + st, L.stage_bytes);
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
@@ -249,12 +250,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ============================ MMA issue (1 thread) ============================
         if (lane == 0) {
             constexpr bool BF = sizeof(DT) == 2 && !std::is_same<DT, __half>::value;
-            const uint32_t idesc_qk = idesc_f16kind(128, kTcT, 0, 0, BF);
+            const uint32_t idesc_qk = idesc_f16kind(128, T, 0, 0, BF);
             const uint32_t idesc_pv = idesc_f16kind(128, L.npv, 1, 0, BF);
             uint32_t fph = 0, sph = 0, pph = 0, qph = 0, oph = 0;
             bool ok = true, q_ready = false;
             int items_pv = 0;
-            Walk qk, pv;
+            Walk<T> qk, pv;
             qk.start(p);
             pv.start(p);
             uint64_t last = global_ns();
@@ -270,13 +271,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (pv.first && items_pv > 0) oph ^= 1u;
                         if (pv.first) ++items_pv;
                         tc_fence_after();
-                        const uint32_t vt = sb + st * L.stage_bytes + L.tile_bytes;
+                        const uint32_t vt = sb + L.stage_off + st * L.stage_bytes + L.tile_bytes;
                         const uint64_t vd = smem_desc_sw128(vt, L.chunk_bytes, 1024);
                         const uint64_t pd = smem_desc_sw128(sb + L.p_off + ps * L.pslot, 16, 1024);
 #pragma unroll
                         for (int j = 0; j < NBLK; ++j)
 #pragma unroll
-                            for (int k = 0; k < kTcT / 16; ++k)
+                            for (int k = 0; k < T / 16; ++k)
                                 tc_mma_bf16(tmem + kTcOCol + j * L.npv,
                                             vd + (uint64_t)((2 * j * L.chunk_bytes + k * 2048) >> 4),
                                             pd + (uint64_t)((k * 32) >> 4), idesc_pv,
@@ -303,12 +304,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         sph ^= 1u << ss;
                         tc_fence_after();
                         const uint64_t qd = smem_desc_sw128(sb + L.q_off, 16, 1024);
-                        const uint64_t kd = smem_desc_sw128(sb + st * L.stage_bytes, 16, 1024);
+                        const uint64_t kd = smem_desc_sw128(sb + L.stage_off + st * L.stage_bytes, 16, 1024);
 #pragma unroll
                         for (int c = 0; c < NCH; ++c)
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                tc_mma_bf16(tmem + ss * kTcT,
+                                tc_mma_bf16(tmem + ss * T,
                                             qd + (uint64_t)((c * L.qch + k * 32) >> 4),
                                             kd + (uint64_t)((c * L.chunk_bytes + k * 32) >> 4),
                                             idesc_qk, (c | k) != 0 ? 1u : 0u);
@@ -403,39 +404,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int bend = first_block_end(p, p0);
             bool firsttile = true;
             for (int t0 = p0, t1; t0 < p1; t0 = t1, ++gt, firsttile = false) {
-                t1 = tile_end<kTcT>(t0, p1, bend, p.block_size);
+                t1 = tile_end<T>(t0, p1, bend, p.block_size);
                 const int ss = gt & 1;
+                // S(t) is in, and PV(t-2) is done with this P slot; the outcome of
+                // both waits joins the rescale vote below (one block-wide vote per
+                // tile in the common case)
                 bool okw = mbar_wait_bounded(bar + TB_SFULL + ss, (sph >> ss) & 1u, p.timeout_ns,
                                              abort_flag);
-                if (tc_bar_or(!okw)) {
-                    ab = true;
-                    break;
-                }
+                okw = okw && mbar_wait_bounded(bar + TB_PFREE + ss, ((pfp >> ss) & 1u) ^ 1u,
+                                               p.timeout_ns, abort_flag);
                 sph ^= 1u << ss;
+                pfp ^= 1u << ss;
                 tc_fence_after();
-                if (t1 - t0 < kTcT) {
+                if (t1 - t0 < T) {
                     // a short tile: the V rows past it hold whatever the cache (or
                     // the pool) has there; zero them, as 0 * NaN would reach O^T.
                     // (The K rows past it only give scores that are masked.)
                     const int tv = t1 - t0;
-                    const uint32_t vt = sb + (gt % NST) * L.stage_bytes + L.tile_bytes;
-                    for (int i = r; i < (kTcT - tv) * NCH * 8; i += 128) {
+                    const uint32_t vt = sb + L.stage_off + (gt % NST) * L.stage_bytes + L.tile_bytes;
+                    for (int i = r; i < (T - tv) * NCH * 8; i += 128) {
                         const int row = tv + i / (NCH * 8), rem = i % (NCH * 8);
                         sts_v4(vt + (rem >> 3) * L.chunk_bytes + tsw(row, (rem & 7) * 16), 0u, 0u,
                                0u, 0u);
                     }
                 }
                 const int nv = max(0, min(t1, lim) - t0); // visible positions of this row
-                float sc[kTcT];
+                float sc[T];
 #pragma unroll
-                for (int q4 = 0; q4 < kTcT / 16; ++q4) tmem_ld16(tl + ss * kTcT + 16 * q4, sc + 16 * q4);
+                for (int q4 = 0; q4 < T / 16; ++q4) tmem_ld16(tl + ss * T + 16 * q4, sc + 16 * q4);
                 tmem_wait_ld();
                 float tm = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < kTcT; ++i)
+                for (int i = 0; i < T; ++i)
                     if (i < nv) tm = fmaxf(tm, sc[i]);
                 const bool ex = owner && tm > m + kTcTau;
-                if (tc_bar_or(ex)) {
+                if (tc_bar_or(ex || !okw)) {
+                    if (tc_bar_or(!okw)) { // a wait ran out somewhere: leave together
+                        ab = true;
+                        break;
+                    }
                     // move the reference of the rows that outgrew it; rescale l and O^T
                     const float mn = ex ? tm : m;
                     const float alpha = (mn == m) ? 1.f : (m == -INFINITY ? 0.f : ex2(m - mn));
@@ -465,22 +472,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     named_bar_sync(1, 128); // alpha_sm is read before it is rewritten
 #pragma unroll
-                    for (int q4 = 0; q4 < kTcT / 16; ++q4)
-                        tmem_ld16(tl + ss * kTcT + 16 * q4, sc + 16 * q4);
+                    for (int q4 = 0; q4 < T / 16; ++q4)
+                        tmem_ld16(tl + ss * T + 16 * q4, sc + 16 * q4);
                     tmem_wait_ld();
                 }
-                // P row: 2^(s - m) in the cache type, once PV(t-2) is done with the slot
-                okw = mbar_wait_bounded(bar + TB_PFREE + ss, ((pfp >> ss) & 1u) ^ 1u, p.timeout_ns,
-                                        abort_flag);
-                if (tc_bar_or(!okw)) {
-                    ab = true;
-                    break;
-                }
-                pfp ^= 1u << ss;
+                // P row: 2^(s - m) in the cache type
                 if (r < L.npv) {
                     const uint32_t prow = sb + L.p_off + ss * L.pslot;
 #pragma unroll
-                    for (int q4 = 0; q4 < kTcT / 16; ++q4) {
+                    for (int q4 = 0; q4 < T / 16; ++q4) {
                         uint32_t w8[8];
 #pragma unroll
                         for (int i = 0; i < 16; i += 2) {

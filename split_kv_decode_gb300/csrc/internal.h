@@ -123,41 +123,46 @@ struct CombineParams {
     int32_t split_base[DA_MAX_BATCH];
 };
 
-// Tensor-core GQA kernel (gqa_tc.cu): tiles of kTcT positions; shared-memory
-// layout for head_dim D and R rows per item (the same on host and device).
-constexpr int kTcT = 64;
+// Tensor-core GQA kernel (gqa_tc.cu): tiles of tc_tile(D) positions;
+// shared-memory layout for head_dim D and R rows per item (the same on host
+// and device). 64-position tiles beat 32-position ones with twice the stages
+// (117 against 179 us for 8 rows at D = 256): the per-tile hand-offs, not the
+// ring depth, set the pace.
+__host__ __device__ constexpr int tc_tile(int) { return 64; }
 constexpr int kTcMaxStages = 6;
 constexpr int kTcBarriers = 32;
 constexpr int kTcSmemMax = 232448;
 struct TcLayout {
-    int chunk_bytes;  // one 64-column chunk of a tile: kTcT rows of 128 B
+    int chunk_bytes;  // one 64-column chunk of a tile: tc_tile(D) rows of 128 B
     int tile_bytes;   // K (or V) tile: D / 64 chunks
     int stage_bytes;  // K + V
     int rpad, npv;    // rows rounded up to 8 (Q rows written), to 16 (PV N)
     int qch;          // one 64-column chunk of Q: rpad rows of 128 B
     int pslot;        // one P buffer: npv rows of 128 B
     int nst;          // stages
-    int q_off, p_off, bar_off, misc_off, alpha_off, used;
+    int q_off, stage_off, p_off, bar_off, misc_off, alpha_off, used;
 };
 __host__ __device__ inline TcLayout tc_layout(int D, int R)
 {
     TcLayout L;
-    L.chunk_bytes = kTcT * 128;
+    L.chunk_bytes = tc_tile(D) * 128;
     L.tile_bytes = (D / 64) * L.chunk_bytes;
     L.stage_bytes = 2 * L.tile_bytes;
     L.rpad = (R + 7) / 8 * 8;
     L.npv = (R + 15) / 16 * 16;
     L.qch = L.rpad * 128;
     L.pslot = L.npv * 128;
-    // the 128-row MMA reads 128 rows from the start of every Q chunk: past the
-    // last one it reads (128 - rpad) rows more
-    const int qbytes = (D / 64) * L.qch + (128 - L.rpad) * 128;
-    const int rest = (qbytes + 1023) / 1024 * 1024 + 2 * L.pslot + kTcBarriers * 8 + 16 +
-                     128 * 4 + 1024;
-    int nst = (kTcSmemMax - rest) / L.stage_bytes;
+    // Q comes first: the 128-row MMA reads 128 rows from the start of every Q
+    // chunk, so past the last one it reads into the first stage (rows whose
+    // scores nobody reads)
+    L.q_off = 0;
+    const int qbytes = (D / 64) * L.qch;
+    const int stages_off = (qbytes + 1023) / 1024 * 1024;
+    const int rest = 2 * L.pslot + kTcBarriers * 8 + 16 + 128 * 4 + 1024;
+    int nst = (kTcSmemMax - stages_off - rest) / L.stage_bytes;
     L.nst = nst > kTcMaxStages ? kTcMaxStages : nst;
-    L.q_off = L.nst * L.stage_bytes;
-    L.p_off = (L.q_off + qbytes + 1023) / 1024 * 1024;
+    L.stage_off = stages_off;
+    L.p_off = stages_off + L.nst * L.stage_bytes;
     L.bar_off = L.p_off + 2 * L.pslot;
     L.misc_off = L.bar_off + kTcBarriers * 8;
     L.alpha_off = L.misc_off + 16;

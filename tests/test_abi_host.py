@@ -480,10 +480,11 @@ def test_plan_tensor_core_gqa(lib, hq, hkv, q_len, d, dt):
     lens = [q_len, 777, 20000]
     rc, p = plan(lib, a, lens)
     assert rc == 0, lib.decode_attn_last_error().decode()
-    assert p.kernel == N.DA_KERNEL_GQA_TC and p.tile == 64 and p.ctas_per_sm == 1
+    tile = 64                               # positions per tile
+    assert p.kernel == N.DA_KERNEL_GQA_TC and p.tile == tile and p.ctas_per_sm == 1
     base = 0
     for b, L in enumerate(lens):
-        assert p.chunk[b] % 64 == 0 and p.n_splits[b] == -(-L // p.chunk[b])
+        assert p.chunk[b] % tile == 0 and p.n_splits[b] == -(-L // p.chunk[b])
         assert p.split_base[b] == base
         base += p.n_splits[b]
     assert p.n_items == base * hkv and 1 <= p.grid <= min(152, p.n_items)
