@@ -31,7 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = {
-    # name: (named case, seq_len override)
+    # name: (named case, seq_len override[, new tokens per sequence])
     "gqa16x4_f16_L151552": ("gqa_16x4", 151552),
     "gqa16x4_f16_L262144": ("gqa_16x4", 262144),
     "gqa16x4_f16_L61440": ("gqa_16x4", 61440),
@@ -41,10 +41,13 @@ WORKLOADS = {
     "gqa24x4_f32_b4": ("gqa_24x4", None),
     "ragged32_bf16": ("ragged_32", None),
     "mla96_f32_L131072": ("mla_96", None),
+    # four new tokens per sequence on the default cache: 16 query rows per KV head
+    "gqa16x4_f16_L151552_q4": ("gqa_16x4", 151552, 4),
 }
 DEFAULT = "gqa16x4_f16_L151552"
 # the split kernel each workload runs, and the arithmetic type it computes in
-KERNEL = {"mla96_f32_L131072": ("mla_split_kernel", "bf16")}
+KERNEL = {"mla96_f32_L131072": ("mla_split_kernel", "bf16"),
+          "gqa16x4_f16_L151552_q4": ("gqa_tc_kernel", "f16")}
 DEFAULT_KERNEL = ("gqa_split_kernel", "f32")
 
 
@@ -75,16 +78,21 @@ def load_peaks():
         return 6800.0, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
 
 
+KERNEL_SOURCES = {
+    "gqa_split_kernel": ("gqa_split.cuh", "gqa_inst.cuh", "gqa_f32.cu", "gqa_f16.cu", "gqa_bf16.cu"),
+    "gqa_tc_kernel": ("gqa_tc.cu", "gqa_split.cuh"),
+    "mla_split_kernel": ("mla_split.cu",),
+}
+
+
 def kernel_source_hash(kernel):
     """Hash of the sources a split kernel is compiled from (its own files plus
     the shared PTX helpers and internal header)."""
     import hashlib
     h = hashlib.sha256()
     src = os.path.join(ROOT, "split_kv_decode_gb300", "csrc")
-    own = "gqa" if kernel.startswith("gqa") else "mla"
-    for f in sorted(os.listdir(src)):
-        if f.startswith(own) or f in ("ptx.cuh", "internal.h"):
-            h.update(open(os.path.join(src, f), "rb").read())
+    for f in KERNEL_SOURCES[kernel] + ("ptx.cuh", "internal.h"):
+        h.update(open(os.path.join(src, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -160,13 +168,32 @@ class ClockSampler:
 
 
 def make_inputs(workload, device):
+    """The workload's seeded case on `device`. With several new tokens per
+    sequence, case.q is [B, q_len, Hq, Dk]."""
+    import dataclasses
     from split_kv_decode_gb300 import workloads as W
-    name, L = WORKLOADS[workload]
+    name, L = WORKLOADS[workload][:2]
+    q_len = WORKLOADS[workload][2] if len(WORKLOADS[workload]) > 2 else 1
     case = W.named(name, seq_len=L) if L else W.named(name)
+    if q_len > 1:
+        case = dataclasses.replace(case, q=W.multi_token_q(case.batch, q_len, case.n_heads,
+                                                           case.head_dim))
     q = case.q.to(device)
     k = case.k.to(device)
     v = k if case.shared_kv else case.v.to(device)
     return case, q, k, v
+
+
+def out_shape(case):
+    return tuple(case.q.shape[:-1]) + (case.v_dim,)
+
+
+def oracle_rows(case, pairs, threads):
+    """The oracle on the (b, h) rows `pairs` (every new token of them)."""
+    import oracle
+    fn = oracle.attention_multi if case.q.dim() == 4 else oracle.attention
+    return fn(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim, pairs=pairs,
+              threads=threads)
 
 
 def cpu_baseline(case, budget_s=12.0):
@@ -177,8 +204,7 @@ def cpu_baseline(case, budget_s=12.0):
     threads = oracle.max_threads()
     pairs_all = [(b, h) for b in range(case.batch) for h in range(case.n_heads)]
     t0 = time.perf_counter()
-    oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
-                     pairs=[pairs_all[0]], threads=1)
+    oracle_rows(case, [pairs_all[0]], 1)
     t_row = time.perf_counter() - t0
     # rows per repetition: all of them, or as many as fit in a third of the budget
     n = max(1, min(len(pairs_all), int(budget_s / 3 / max(t_row, 1e-6) * threads)))
@@ -189,8 +215,7 @@ def cpu_baseline(case, budget_s=12.0):
     times, t_start = [], time.perf_counter()
     while not times or (time.perf_counter() - t_start < budget_s and len(times) < 50):
         t0 = time.perf_counter()
-        oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
-                         pairs=pairs, threads=threads)
+        oracle_rows(case, pairs, threads)
         times.append(time.perf_counter() - t0)
     us = statistics.median(times) * 1e6 * pos_all / pos_sample
     return {"value": round(us, 1), "unit": "us/layer-step", "cores": threads, "kind": "oracle",
@@ -211,8 +236,7 @@ def run_reference(args):
     pairs_all = [(b, h) for b in range(case.batch) for h in range(case.n_heads)]
     # each step: a bounded sample of rows (about 2 s of host work), scaled to a full step
     t0 = time.perf_counter()
-    oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
-                     pairs=[pairs_all[0]], threads=1)
+    oracle_rows(case, [pairs_all[0]], 1)
     t_row = time.perf_counter() - t0
     n = max(1, min(len(pairs_all), int(2.0 / max(t_row, 1e-6) * threads)))
     stride = max(1, len(pairs_all) // n)
@@ -220,13 +244,11 @@ def run_reference(args):
     pos_sample = sum(int(case.seq_lens[b]) for b, _ in pairs)
     pos_all = sum(int(case.seq_lens[b]) for b, _ in pairs_all)
     for _ in range(args.warmup):
-        oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
-                         pairs=pairs[:1], threads=threads)
+        oracle_rows(case, pairs[:1], threads)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.attention(case.q, case.k, case.v, case.seq_lens, case.scale, v_dim=case.v_dim,
-                         pairs=pairs, threads=threads)
+        oracle_rows(case, pairs, threads)
         times.append((time.perf_counter() - t0) * pos_all / pos_sample)
     us = statistics.mean(times) * 1e6
     line = {
@@ -251,6 +273,7 @@ def workload_config(workload, case):
             "n_kv_heads": case.n_kv_heads, "head_dim": case.head_dim, "v_dim": case.v_dim,
             "seq_lens": (case.seq_lens.tolist() if case.batch <= 8 else
                          f"{case.batch} lengths, sum {int(case.seq_lens.sum())}"),
+            "q_len": int(case.q.shape[1]) if case.q.dim() == 4 else 1,
             "kv_dtype": case.kv_dtype, "q_dtype": "f32", "out_dtype": case.out_dtype,
             "kv_bytes_per_step": case.kv_bytes, "parallelism": "replicas",
             "l2": "flushed between steps (2 x L2 write, outside the events)"}
@@ -291,7 +314,7 @@ def main():
                           flags=N.DA_FLAG_NO_COMBINE)
     plan = A.decode_attn_plan(a_split, case.seq_lens.tolist())
     ws = torch.empty(A.decode_attn_workspace_bytes(plan), dtype=torch.uint8, device=dev)
-    out = torch.empty(case.batch, case.n_heads, case.v_dim, dtype=out_dt, device=dev)
+    out = torch.empty(out_shape(case), dtype=out_dt, device=dev)
     lens = case.seq_lens.tolist()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
@@ -379,7 +402,7 @@ def main():
     }
     if rank == 0 and not args.no_extra:
         line["e2e"] = measure_e2e(case, q, out_dt, dev, stream, args)
-        if kernel == "gqa_split_kernel":
+        if kernel == "gqa_split_kernel" and case.q.dim() == 3:
             line["graph"] = measure_graph(case, q, k, v, out_dt, dev, flush, args)
             line["paged"] = {f"block_{bs}": measure_paged(case, q, k, v, out_dt, dev, flush, args, bs)
                              for bs in (64, 256)}
@@ -552,7 +575,7 @@ def measure_e2e(case, q_dev, out_dt, dev, stream, args):
     hq = case.q.pin_memory()
     hk = case.k.pin_memory()
     hv = hk if case.shared_kv else case.v.pin_memory()
-    hout = torch.empty(case.batch, case.n_heads, case.v_dim, dtype=out_dt).pin_memory()
+    hout = torch.empty(out_shape(case), dtype=out_dt).pin_memory()
     dq = torch.empty_like(hq, device=dev)
     dk = torch.empty_like(hk, device=dev)
     dv = dk if case.shared_kv else torch.empty_like(hv, device=dev)
