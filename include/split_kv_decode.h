@@ -96,15 +96,17 @@ typedef struct {
     int32_t flags;       /* DA_FLAG_*                                          */
     int32_t timeout_us;  /* bound on every in-kernel wait; 0 = 2 000 000 us    */
     int32_t q_len;       /* query tokens per sequence; 0 or 1: one. With q_len
-                            > 1 (GQA/MQA only), q is [batch][q_len][n_heads]
-                            [head_dim] and out [batch][q_len][n_heads][v_dim];
-                            token i sits at position L - q_len + i and attends
-                            to positions 0 .. L - q_len + i (causal among the
-                            new tokens, whose K/V rows are in the cache: the
-                            causal query tile of "Decoder Block 6: Online
-                            Attention, the Capstone", Lesson). (n_heads /
-                            n_kv_heads) * q_len must be 1, 2, 4, 6 or 8, and
-                            every seq_len >= q_len; at most 64.                */
+                            > 1, q is [batch][q_len][n_heads][head_dim] and out
+                            [batch][q_len][n_heads][v_dim]; token i sits at
+                            position L - q_len + i and attends to positions
+                            0 .. L - q_len + i (causal among the new tokens,
+                            whose K/V rows are in the cache: the causal query
+                            tile of "Decoder Block 6: Online Attention, the
+                            Capstone", Lesson). The rows of a work item are
+                            (n_heads / n_kv_heads) * q_len (token, head)
+                            pairs: 1, 2, 4, 6 or 8 (SIMT GQA kernel), 8 to 128
+                            (tensor-core GQA kernel, 16-bit caches), or 32, 64
+                            or 96 (MLA). Every seq_len >= q_len; at most 64.  */
 } da_args_t;
 
 /* A host-side plan (plan/run separation): which kernel, how the context is

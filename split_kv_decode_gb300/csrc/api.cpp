@@ -123,12 +123,13 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
     const int G = a->n_heads / a->n_kv_heads * q_len_of(a);
     const int es = dtype_size(a->kv_dtype);
     if (a->head_dim == 576 && a->v_dim == 512 && a->n_kv_heads == 1) {
-        if (q_len_of(a) > 1)
-            return fail(DA_EUNSUPPORTED, "plan", "the MLA kernel serves one query token");
         if (a->kv_dtype != DA_F32)
             return fail(DA_EUNSUPPORTED, "plan", "the MLA kernel reads an f32 latent cache");
-        if (!mla_supported_heads(a->n_heads))
-            return fail(DA_EUNSUPPORTED, "plan", "the MLA kernel serves 32, 64 or 96 query heads");
+        // the rows of an item are (query token, head) pairs, like heads of MQA
+        if (!mla_supported_heads(rows_of(a)))
+            return fail(DA_EUNSUPPORTED, "plan",
+                        "the MLA kernel serves 32, 64 or 96 query rows (heads x q_len; got %d)",
+                        rows_of(a));
         if (a->k_pos_stride < 576 || (a->k_pos_stride * 4) % 16 ||
             (a->batch > 1 && (a->k_batch_stride * 4) % 16))
             return fail(DA_EUNSUPPORTED, "plan",
@@ -300,7 +301,9 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
     p.ml = reinterpret_cast<float2 *>(w + ws_ml_offset());
     p.acc = reinterpret_cast<float *>(w + ws_acc_offset(pl->total_splits, rows_of(a)));
     p.status = reinterpret_cast<int *>(w);
-    p.n_heads = a->n_heads;
+    p.n_heads = rows_of(a);
+    p.q_len = q_len_of(a);
+    p.hq = a->n_heads;
     p.scale_log2 = a->scale * 1.4426950408889634f;
     p.timeout_ns = (uint64_t)(a->timeout_us > 0 ? a->timeout_us : 2000000) * 1000ull;
     p.flags = a->flags;

@@ -76,7 +76,9 @@ struct MlaParams {
     float2 *ml;              // workspace (m, l) per (slot, head)
     float *acc;              // workspace acc per (slot, head, 512)
     int *status;             // workspace status word
-    int32_t n_heads;
+    int32_t n_heads;         // rows per sequence: q_len * hq (query token, head), token-major
+    int32_t q_len;           // query tokens per sequence (causal among them)
+    int32_t hq;              // query heads per token
     float scale_log2;        // scale * log2(e)
     uint64_t timeout_ns;
     int32_t flags;
@@ -91,8 +93,8 @@ struct MlaParams {
     ItemTable items;         // n_kv_heads = 1
 };
 
-// MLA tensor-core split kernel: heads per CTA = n_heads / 2 (a 2-CTA cluster
-// shares every tile); supported n_heads: 32, 64, 96.
+// MLA tensor-core split kernel: rows per CTA = rows / 2 (a 2-CTA cluster
+// shares every tile); supported rows (heads x q_len): 32, 64, 96.
 bool mla_supported_heads(int n_heads);
 int mla_smem_bytes(int n_heads);
 cudaError_t launch_mla_split(int grid, cudaStream_t stream, const MlaParams &p);

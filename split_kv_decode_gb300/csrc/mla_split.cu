@@ -16,7 +16,9 @@
 //   * converts rows [32r, 32r + 32) of every tile from f32 to bf16 into its own
 //     shared memory and ships them to the peer CTA with bulk shared-memory
 //     copies, so every row is read from HBM once and converted once;
-//   * owns query heads [r*N, r*N + N), N = n_heads / 2: their bf16 Q (scale and
+//   * owns query rows [r*N, r*N + N), N = rows / 2 (a row is a query head, or
+//     with several new tokens per sequence a (token, head) pair, token-major,
+//     whose token sees the positions up to its own): their bf16 Q (scale and
 //     log2 e folded in), S and O^T in its TMEM, and their partials.
 // The tile buffer is double-buffered (two slots of nine 64-column chunks,
 // 128-byte-swizzled, K-major), so the converters fill tile t+1 while the
@@ -127,7 +129,7 @@ __device__ __forceinline__ bool bar_or(int id, int threads, bool pred)
 }
 
 struct Item {
-    int b, s, p0, p1, ntiles;
+    int b, s, p0, p1, ntiles, L; // L: the length the item's sequence attends over
 };
 
 // item -> (sequence, split, positions [p0, p1), tiles). With lengths read on
@@ -146,7 +148,8 @@ __device__ __forceinline__ Item get_item(const MlaParams &p, int item)
     x.s = item - it.split_base[lo];
     x.p0 = x.s * it.chunk[lo];
     int L = it.seq_lens[lo];
-    if (p.dev_lens) L = max(1, min(__ldg(p.dev_lens + lo), L));
+    if (p.dev_lens) L = max(p.q_len, min(__ldg(p.dev_lens + lo), L));
+    x.L = L;
     x.p1 = min(L, x.p0 + it.chunk[lo]);
     x.ntiles = x.p1 > x.p0 ? (x.p1 - x.p0 + kTile - 1) / kTile : 0;
     return x;
@@ -515,6 +518,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 continue;
             }
             float m = -INFINITY, l = 0.f;
+            // this row's token sees positions below lim (causal among the new
+            // tokens; with one token, every position of the item)
+            const int lim = x.L - p.q_len + 1 + (hbase + h) / p.hq;
             for (int t = 0; t < x.ntiles; ++t, ++gt) {
                 const int slot = gt & 1;
                 bool okw = mbar_wait_bounded(bar + B_SFULL + slot, (sph >> slot) & 1u,
@@ -525,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 sph ^= 1u << slot;
                 tc_fence_after();
-                const int nvalid = min(kTile, x.p1 - (x.p0 + t * kTile));
+                const int nvalid = max(0, min(kTile, min(x.p1, lim) - (x.p0 + t * kTile)));
                 const uint32_t scol = tl + slot * kTile;
                 // this thread's head: its 64 scores (one TMEM round trip) and
                 // their max over the valid positions

@@ -512,12 +512,19 @@ def test_plan_multi_token_needs_q_len_positions(lib):
     assert plan(lib, a, [1])[0] == 0
 
 
-def test_mla_refuses_multi_token(lib):
-    a = mla_args(cap=4096)
-    a.q_len = 2
-    rc, _ = plan(lib, a, [4096])
-    assert rc == N.DA_EUNSUPPORTED
-    assert "one query token" in lib.decode_attn_last_error().decode()
+@pytest.mark.parametrize("hq,q_len,ok", [(48, 2, True), (16, 4, True), (32, 3, True),
+                                         (16, 6, True), (96, 2, False), (24, 2, False)])
+def test_mla_multi_token_rows(lib, hq, q_len, ok):
+    # the rows of an MLA item are (token, head) pairs: 32, 64 or 96 of them
+    a = mla_args(hq=hq, cap=4096)
+    a.q_len = q_len
+    rc, p = plan(lib, a, [4096])
+    if ok:
+        assert rc == 0 and p.kernel == N.DA_KERNEL_MLA_TC
+        assert p.workspace_bytes >= p.total_splits * hq * q_len * (512 * 4 + 8)
+    else:
+        assert rc == N.DA_EUNSUPPORTED
+        assert "rows" in lib.decode_attn_last_error().decode()
 
 
 # ---------------------------------------------------------------------------

@@ -103,3 +103,76 @@ def test_mla_timed_out_wait_is_reported_and_the_context_survives():
         A.decode_attn_device_status(da.workspace)
     assert e.value.status == N.DA_ETIMEOUT and "mla" in e.value.message
     check(case, BF16_BAR)
+
+
+# ---------------------------------------------------------------------------
+# several new tokens per sequence: the rows of an item are (token, head) pairs
+# ---------------------------------------------------------------------------
+def _multi_errors(case, q4, got, lens=None, pairs=None):
+    import oracle
+    lens = case.seq_lens if lens is None else torch.tensor(lens, dtype=torch.int32)
+    T = q4.shape[1]
+    ref = oracle.attention_multi(q4, case.k, case.v, lens, case.scale, v_dim=512, pairs=pairs,
+                                 threads=0)
+    worst = 0.0
+    for b in range(case.batch):
+        L = int(lens[b])
+        for t in range(T):
+            vm = float(case.k[b, :L - T + 1 + t, 0, :512].abs().max())
+            if pairs is None:
+                worst = max(worst, float(np.max(np.abs(got[b, t] - ref[b, t]))) / vm)
+            else:
+                for i, (bb, h) in enumerate(pairs):
+                    if bb == b:
+                        worst = max(worst, float(np.max(np.abs(got[b, t, h] - ref[t, i]))) / vm)
+    return worst
+
+
+def _run_multi(case, q4, force_splits=0, dev_lens=None):
+    q = q4.cuda()
+    k = case.k.cuda()
+    a = A.make_args(q, k, k, case.scale, v_dim=512, force_splits=force_splits)
+    p = A.decode_attn_plan(a, case.seq_lens.tolist())
+    assert p.kernel == N.DA_KERNEL_MLA_TC
+    ws = A.new_workspace(p)
+    ws.fill_(0xFF)
+    out = torch.empty(case.batch, q4.shape[1], q4.shape[2], 512, device="cuda")
+    if dev_lens is None:
+        A.decode_attn_splitk_ex(a, p, q, k, k, out, ws)
+    else:
+        d = A.make_dev(seq_lens=torch.tensor(dev_lens, dtype=torch.int32, device="cuda"))
+        A.decode_attn_splitk_dev(a, p, d, q, k, k, out, ws)
+    torch.cuda.synchronize()
+    A.decode_attn_device_status(ws)
+    got = out.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    return got
+
+
+@pytest.mark.parametrize("heads,q_len,lens,force", [
+    (48, 2, [2, 129, 5000], 0),     # 96 rows
+    (16, 4, [4, 3000], 0),          # 64 rows
+    (32, 3, [3, 900, 2500], 9),     # 96 rows; short splits inside the causal tail
+    (16, 2, [2, 64, 65], 0),        # 32 rows
+])
+def test_mla_several_new_tokens(heads, q_len, lens, force):
+    case = mla_case(lens, heads=heads, seed=3100 + heads + q_len)
+    q4 = W.multi_token_q(len(lens), q_len, heads, 576, seed=3101 + q_len)
+    got = _run_multi(case, q4, force_splits=force)
+    assert _multi_errors(case, q4, got) <= BF16_BAR
+
+
+def test_mla_several_new_tokens_full_context_sampled():
+    # the 131072-position latent cache, 48 heads x 2 new tokens (96 rows)
+    case = W.named("mla_96")
+    q4 = W.multi_token_q(1, 2, 48, 576, seed=3120)
+    got = _run_multi(case, q4)
+    pairs = [(0, 0), (0, 23), (0, 47)]
+    assert _multi_errors(case, q4, got, pairs=pairs) <= F32_BAR
+
+
+def test_mla_several_new_tokens_device_lengths():
+    case = mla_case([3000, 800], heads=32, seed=3130)
+    q4 = W.multi_token_q(2, 2, 32, 576, seed=3131)
+    got = _run_multi(case, q4, dev_lens=[2000, 1])        # 1 is kept at q_len
+    assert _multi_errors(case, q4, got, lens=[2000, 2]) <= BF16_BAR
