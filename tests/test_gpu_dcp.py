@@ -90,3 +90,13 @@ def test_single_rank_object_matches_the_plain_call():
     short = dataclasses.replace(short, seq_lens=torch.tensor([1500, 1200], dtype=torch.int32))
     worst, rel = errors(short, out.double().cpu().numpy(), oracle_rows(short))
     assert worst <= TOL["f32"], (worst, rel)
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_tensor_core_gqa_context_parallel(world):
+    # 32 query heads over one KV head, f16: the tensor-core kernel on every rank
+    case = W.make_case("t", batch=2, n_heads=32, n_kv_heads=1, head_dim=128,
+                       seq_lens=[9001, 1234], kv_dtype="f16", seed=740 + world)
+    got = dcp_emulated(case, world)
+    worst, rel = errors(case, got, oracle_rows(case))
+    assert np.all(np.isfinite(got)) and worst <= TOL["f16"], (worst, rel)

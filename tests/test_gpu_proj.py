@@ -204,3 +204,39 @@ def test_projection_over_two_context_ranks():
     got = out.double().cpu().numpy()
     ref = oracle.attention_proj(case.q, case.k, case.v, case.seq_lens, case.scale, w, threads=0)
     assert worst_err(got, ref) <= bar(case, w, TOL["f16"])
+
+
+def test_projection_in_a_captured_graph():
+    # split (lengths on the device) + combine with the projection, captured once
+    # and replayed over growing contexts
+    case = W.make_case("t", batch=2, n_heads=16, n_kv_heads=4, head_dim=256,
+                       seq_lens=[5000, 3000], kv_dtype="bf16", scale=1 / 16, seed=2170)
+    w = proj_weights(16, 64, 256, 2171)
+    q, k, v = to_device(case)
+    wd = w.cuda()
+    a = A.make_args(q, k, v, case.scale, flags=N.DA_FLAG_NO_COMBINE)
+    p = A.decode_attn_plan(a, case.seq_lens.tolist())
+    ws = A.new_workspace(p)
+    dev_lens = torch.tensor([10, 10], dtype=torch.int32, device="cuda")
+    d = A.make_dev(seq_lens=dev_lens)
+    pj = A.make_proj(wd)
+    out = torch.empty(2, 16, 64, device="cuda")
+    scratch = torch.empty(2, 16, 256, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        A.decode_attn_splitk_dev(a, p, d, q, k, v, scratch, ws, s)
+        A.decode_attn_combine_proj(a, p, pj, ws, out, stream=s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            A.decode_attn_splitk_dev(a, p, d, q, k, v, scratch, ws, s)
+            A.decode_attn_combine_proj(a, p, pj, ws, out, stream=s)
+    import dataclasses
+    for lens in ([10, 10], [4000, 2999], [5000, 3000]):
+        dev_lens.copy_(torch.tensor(lens, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        c2 = dataclasses.replace(case, seq_lens=torch.tensor(lens, dtype=torch.int32))
+        ref = oracle.attention_proj(c2.q, c2.k, c2.v, c2.seq_lens, c2.scale, w, threads=0)
+        assert worst_err(out.double().cpu().numpy(), ref) <= bar(c2, w, TOL["bf16"]), lens
