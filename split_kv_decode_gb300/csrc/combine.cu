@@ -27,7 +27,8 @@ namespace skv {
 constexpr int kCombineThreads = 256;
 constexpr int kCombineWarps = kCombineThreads / 32;
 constexpr int kCombineCols = 128;   // value columns per CTA (one float4 per lane)
-constexpr int kCombinePrefetch = 8; // acc vectors per lane loaded before the weights
+constexpr int kCombinePrefetch = 10; // acc vectors per lane loaded before the weights
+                                     // (all of them for up to 80 splits)
 
 template <typename OT> __device__ __forceinline__ void store4(OT *p, float4 v);
 template <> __device__ __forceinline__ void store4<float>(float *p, float4 v)
@@ -101,18 +102,27 @@ __device__ __forceinline__ float4 merge_columns(const CombineParams &p, int h, i
         const int sp = warp + kCombineWarps * i;
         pv[i] = (live && sp < SR) ? acc_of(sp) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // m = max_i m_i and l = sum_i e^{m_i - m} l_i, by every warp for itself
-    float M = kNeutralM;
-    for (int sp = lane; sp < SR; sp += 32) M = fmaxf(M, ml_of(sp).x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
+    // m = max_i m_i and l = sum_i e^{m_i - m} l_i, by every warp for itself, in
+    // one pass: each lane merges its pairs online, then the lanes merge theirs
+    // pairwise with the same rescaling (every lane ends with the same M and L)
+    float M = kNeutralM, L = 0.f;
     for (int sp = lane; sp < SR; sp += 32) {
         const float2 x = ml_of(sp);
-        L = fmaf(x.y, ex2((x.x - M) * kLog2e), L);
+        if (x.x > M) {
+            L = fmaf(L, ex2((M - x.x) * kLog2e), x.y);
+            M = x.x;
+        } else {
+            L = fmaf(x.y, ex2((x.x - M) * kLog2e), L);
+        }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    for (int o = 16; o > 0; o >>= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+        const float Lo = __shfl_xor_sync(0xffffffffu, L, o);
+        const float Mn = fmaxf(M, Mo);
+        L = L * ex2((M - Mn) * kLog2e) + Lo * ex2((Mo - Mn) * kLog2e);
+        M = Mn;
+    }
 
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll

@@ -378,6 +378,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     // Offsets of row j from the (sequence, group) base, in q and workspace rows:
     const int Gh = G / p.q_len;
     auto row_off = [&](int j) { return p.q_len == 1 ? j : (j / Gh) * p.hq + j % Gh; };
+    // the token of each (step, row) value this lane writes after the reduce;
+    // constant over the tiles, so the causal test in the tile loop is an add
+    int tok_r[K::R];
+#pragma unroll
+    for (int r = 0; r < K::R; ++r) tok_r[r] = ((tbase + r) % G) / Gh;
 
     // q for the G rows of an item's group, pre-scaled into log2 units. The
     // next item's q is loaded right after the last tile of the current one,
@@ -463,16 +468,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                                 dv[r2 * G + h] = fmaf(q[h][c * K::EPC + e], kf[e], dv[r2 * G + h]);
                     }
                 tr_reduce<K::NVL, LPR / 2>(dv, lane);
-                const bool causal = t1 > lim0; // a tile that reaches the new tokens
+                if (t1 <= lim0) {
 #pragma unroll
-                for (int r = 0; r < K::R; ++r) {
-                    const int idx = tbase + r;                       // (step, row) of this group
-                    const int row = (idx / G) * K::RPW + half;
-                    bool live = row < valid;
-                    if (causal)
-                        live = live && t0 + warp * K::P + row < lim0 + (idx % G) / Gh;
-                    const float sv = live ? dv[r] : -INFINITY;
-                    if (twriter) sc[row * G + idx % G] = sv;
+                    for (int r = 0; r < K::R; ++r) {
+                        const int idx = tbase + r;                   // (step, row) of this group
+                        const int row = (idx / G) * K::RPW + half;
+                        const float sv = (row < valid) ? dv[r] : -INFINITY;
+                        if (twriter) sc[row * G + idx % G] = sv;
+                    }
+                } else { // a tile that reaches the new tokens (rare): the causal limit too
+#pragma unroll
+                    for (int r = 0; r < K::R; ++r) {
+                        const int idx = tbase + r;
+                        const int row = (idx / G) * K::RPW + half;
+                        const bool live =
+                            row < valid && t0 + warp * K::P + row < lim0 + tok_r[r];
+                        const float sv = live ? dv[r] : -INFINITY;
+                        if (twriter) sc[row * G + idx % G] = sv;
+                    }
                 }
                 __syncwarp();
                 // ---- running max per head (every lane computes it redundantly)
