@@ -218,7 +218,10 @@ def cpu_baseline(case, budget_s=12.0):
         oracle_rows(case, pairs, threads)
         times.append(time.perf_counter() - t0)
     us = statistics.median(times) * 1e6 * pos_all / pos_sample
+    pos_row = int(case.seq_lens[pairs_all[0][0]])
     return {"value": round(us, 1), "unit": "us/layer-step", "cores": threads, "kind": "oracle",
+            "single_thread": {"value": round(t_row * 1e6 * pos_all / pos_row, 1),
+                              "sample": "one (b,h) row at full context on one thread, scaled"},
             "sample": f"{len(pairs)} of {len(pairs_all)} (b,h) rows at full context, median of "
                       f"{len(times)} repetitions ({time.perf_counter() - t_start:.1f} s), "
                       "scaled by attended positions"}
@@ -402,6 +405,8 @@ def main():
     }
     if rank == 0 and not args.no_extra:
         line["e2e"] = measure_e2e(case, q, out_dt, dev, stream, args)
+        line["hot_l2"] = measure_hot(case, q, k, v, out_dt, dev, args)
+        line["copy_probe"] = read_probe(dev, stream, max(case.kv_bytes, 512 << 20))
         if kernel == "gqa_split_kernel" and case.q.dim() == 3:
             line["graph"] = measure_graph(case, q, k, v, out_dt, dev, flush, args)
             line["paged"] = {f"block_{bs}": measure_paged(case, q, k, v, out_dt, dev, flush, args, bs)
@@ -564,6 +569,77 @@ def measure_multi_token(case, k, v, out_dt, dev, flush, args):
     res["what"] = ("split + combine for q_len new tokens per sequence, causal among "
                    "themselves, sharing every K/V tile")
     return res
+
+
+def measure_hot(case, q, k, v, out_dt, dev, args, reps=10):
+    """The step with no L2 flush between steps (labelled: inputs that fit the
+    129 MB L2 are then served from it). The device time alone: `reps`
+    consecutive steps (split with the lengths read on the device, then the
+    combine) are captured in one CUDA graph and replayed, so host work does not
+    show."""
+    import torch
+    from split_kv_decode_gb300 import _native as N
+    from split_kv_decode_gb300 import api as A
+    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
+                    flags=N.DA_FLAG_NO_COMBINE)
+    p = A.decode_attn_plan(a, case.seq_lens.tolist())
+    ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    out = torch.empty(out_shape(case), dtype=out_dt, device=dev)
+    d = A.make_dev(seq_lens=case.seq_lens.to(device=dev, dtype=torch.int32))
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+
+    def one():
+        A.decode_attn_splitk_dev(a, p, d, q, k, v, out, ws, s)
+        A.decode_attn_combine(a, p, ws, out, s)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(reps):
+                one()
+    torch.cuda.synchronize()
+    ts = []
+    with torch.cuda.stream(s):                    # replay() launches on the current stream
+        g.replay()
+        for _ in range(max(5, min(args.steps, 50))):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median(x.elapsed_time(y) * 1e3 for x, y in ts) / reps
+    return {"value": round(us, 2), "unit": "us/layer-step", "steps": len(ts) * reps,
+            "what": f"split + combine, {reps} steps per CUDA graph replay, no L2 flush",
+            "fits_l2": case.kv_bytes < 120 * (1 << 20)}
+
+
+def read_probe(dev, stream, nbytes):
+    """An in-run bandwidth probe beside the measured copy peak: torch's copy of a
+    buffer of at least the workload's K/V bytes (read + write bytes / time; L2
+    flushed before each copy), to show the state of this box during the run."""
+    import torch
+    x = torch.ones(nbytes // 2, dtype=torch.float16, device=dev)
+    y = torch.empty_like(x)
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4, device=dev)
+    ts = []
+    for i in range(13):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        y.copy_(x)
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in ts[3:])
+    del x, y, flush
+    torch.cuda.empty_cache()
+    return {"gbs": round(2 * nbytes / (us * 1e-6) / 1e9, 1), "bytes_copied": nbytes,
+            "what": "torch copy_ of an f16 buffer (read + write bytes), L2 flushed before each"}
 
 
 def measure_e2e(case, q_dev, out_dt, dev, stream, args):
