@@ -24,7 +24,8 @@
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers of the current CUDA device,
  *     owned by the caller; the library never frees them.
- *   - q is float32 [batch][n_heads][head_dim], contiguous.
+ *   - q is float32 [batch][n_heads][head_dim] (with q_len > 1:
+ *     [batch][q_len][n_heads][head_dim]), contiguous.
  *   - K/V element (b, pos, kv, d) lives at base + b*batch_stride +
  *     pos*pos_stride + kv*head_stride + d (strides in ELEMENTS). For MLA pass
  *     the same buffer as k_cache and v_cache with v_dim < head_dim: the
@@ -153,17 +154,21 @@ int64_t decode_attn_workspace_bytes(const da_plan_t *plan);
 /*
  * decode_attn_splitk_ex -- run the split kernel and (unless
  * DA_FLAG_NO_COMBINE) the combine kernel on `stream`.
- * Split kernel: Kernel A of aprender issue 3725 §2 re-designed for sm_103a,
- * or for MLA the heads-batched kernel of "Attention at 128k" §4 on tensor
- * cores; partials (m, l, acc) are written per (query head, split), acc left
- * un-normalised; empty slices are neutral (l = 0, m = -1e30).
+ * Split kernel (the plan's choice, da_plan_t.kernel): Kernel A of aprender
+ * issue 3725 §2 re-designed for sm_103a (DA_KERNEL_GQA_TMA); for work items
+ * of 8 to 128 query rows on a 16-bit cache the same item on tensor cores
+ * (DA_KERNEL_GQA_TC); for MLA the heads-batched kernel of "Attention at 128k"
+ * §4 on tensor cores (DA_KERNEL_MLA_TC). Partials (m, l, acc) are written per
+ * (query row, split), acc left un-normalised; empty slices are neutral
+ * (l = 0, m = -1e30).
  *   workspace   DEVICE memory, >= plan->workspace_bytes, 256-byte aligned,
  *               caller-owned (per device; "Attention at 128k" §2 explains why
  *               one pointer must never serve two devices). Contents need no
  *               initialisation.
  * Validation before any launch: DA_EINVAL / DA_EUNSUPPORTED / DA_ENOSPACE.
  * The MLA kernel (head_dim 576, v_dim 512, one KV head) needs an f32 cache,
- * 32, 64 or 96 heads, and k_cache == v_cache; otherwise DA_EUNSUPPORTED.
+ * 32, 64 or 96 query rows (heads x q_len), and k_cache == v_cache; otherwise
+ * DA_EUNSUPPORTED.
  * A failed launch: DA_ELAUNCH, message names the phase ("split"/"combine").
  * Asynchronous: a timed-out wait inside the kernel is reported later by
  * decode_attn_device_status().
