@@ -71,6 +71,11 @@ typedef enum {
 #define DA_FLAG_TEST_NO_TMA 0x100 /* test hook: the producer issues no copy, so every
                                      consumer wait runs out after timeout_us and the
                                      kernel reports DA_ETIMEOUT through device_status */
+#define DA_FLAG_TEST_BAD_LAUNCH 0x200 /* test hook: the split kernel is launched with an
+                                     empty grid, which the runtime refuses before
+                                     anything runs (a launch error that does not stick
+                                     to the context): the call returns DA_ELAUNCH and
+                                     the message names the "split" phase             */
 
 /* Kernels the planner can choose (da_plan_t.kernel). */
 #define DA_KERNEL_GQA_TMA 1 /* SIMT split kernel, TMA-staged K/V tiles (GQA, MQA) */

@@ -287,6 +287,13 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// the split kernel's grid; the test hook DA_FLAG_TEST_BAD_LAUNCH asks for an
+// empty one, which the runtime refuses before anything runs
+int split_grid(const da_args_t *a, const da_plan_t *pl)
+{
+    return (a->flags & DA_FLAG_TEST_BAD_LAUNCH) ? 0 : pl->grid;
+}
+
 int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
                const void *v, void *ws, cudaStream_t st, const da_dev_t *dev)
 {
@@ -325,7 +332,7 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
             p.block_stride = dev->k_block_stride;
         }
     }
-    cudaError_t e = launch_mla_split(pl->grid, st, p);
+    cudaError_t e = launch_mla_split(split_grid(a, pl), st, p);
     if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
     return DA_OK;
 }
@@ -385,7 +392,8 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     }
     if (dev) p.dev_lens = dev->seq_lens;
     if (tc) {
-        const cudaError_t e = launch_gqa_tc(a->kv_dtype, a->head_dim, pl->grid, st, km, vm, p);
+        const cudaError_t e =
+            launch_gqa_tc(a->kv_dtype, a->head_dim, split_grid(a, pl), st, km, vm, p);
         if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
         return DA_OK;
     }
@@ -393,9 +401,9 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     const int G = a->n_heads / a->n_kv_heads * q_len_of(a);
     cudaError_t e;
     switch (a->kv_dtype) {
-    case DA_F32: e = gqa_launch_f32(a->head_dim, G, pl->grid, st, km, vm, p); break;
-    case DA_F16: e = gqa_launch_f16(a->head_dim, G, pl->grid, st, km, vm, p); break;
-    default: e = gqa_launch_bf16(a->head_dim, G, pl->grid, st, km, vm, p); break;
+    case DA_F32: e = gqa_launch_f32(a->head_dim, G, split_grid(a, pl), st, km, vm, p); break;
+    case DA_F16: e = gqa_launch_f16(a->head_dim, G, split_grid(a, pl), st, km, vm, p); break;
+    default: e = gqa_launch_bf16(a->head_dim, G, split_grid(a, pl), st, km, vm, p); break;
     }
     if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
     return DA_OK;

@@ -245,3 +245,30 @@ def test_timed_out_wait_is_reported_and_the_context_survives():
     assert e.value.status == N.DA_ETIMEOUT
     assert "split" in e.value.message
     check(case)                              # the context is still usable
+
+
+@pytest.mark.parametrize("shape", ["simt", "tc", "mla"])
+def test_refused_launch_is_reported_and_the_context_survives(shape):
+    # the test hook launches the split kernel with an empty grid: the runtime
+    # refuses it before anything runs, the call returns DA_ELAUNCH naming the
+    # split phase, and the next call on the same context is correct
+    if shape == "mla":
+        case = W.make_case("t", batch=1, n_heads=32, n_kv_heads=1, head_dim=576, v_dim=512,
+                           seq_lens=[2000], kv_dtype="f32", scale=1 / math.sqrt(576.0), seed=61,
+                           std=0.5, shared_kv=True)
+    elif shape == "tc":
+        case = W.make_case("t", batch=1, n_heads=16, n_kv_heads=1, head_dim=128,
+                           seq_lens=[2000], kv_dtype="f16", seed=62)
+    else:
+        case = W.make_case("t", batch=1, n_heads=8, n_kv_heads=2, head_dim=256,
+                           seq_lens=[2000], kv_dtype="f32", scale=1 / 16, seed=63)
+    q, k, v = to_device(case)
+    da = A.DecodeAttention(q, k, v, [2000], case.scale, v_dim=case.v_dim,
+                           flags=N.DA_FLAG_TEST_BAD_LAUNCH)
+    with pytest.raises(A.DecodeAttnError) as e:
+        da(q, k, v)
+    assert e.value.status == N.DA_ELAUNCH
+    assert "split" in e.value.message
+    got, _ = run(case)
+    worst, rel = errors(case, got, oracle_rows(case))
+    assert worst <= (5e-3 if shape == "mla" else TOL[case.kv_dtype]), (worst, rel)
