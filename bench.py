@@ -547,7 +547,7 @@ def measure_multi_token(case, k, v, out_dt, dev, flush, args):
         rows = G * q_len
         if int(case.seq_lens.min()) < q_len:
             continue
-        if not (rows in (2, 4, 6, 8) or (case.kv_dtype in ("f16", "bf16") and 8 <= rows <= 128)):
+        if not (rows <= 8 or (case.kv_dtype in ("f16", "bf16") and rows <= 128)):
             continue
         q = W.multi_token_q(case.batch, q_len, case.n_heads, case.head_dim).to(dev)
         a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)

@@ -110,7 +110,7 @@ typedef struct {
                             tile of "Decoder Block 6: Online Attention, the
                             Capstone", Lesson). The rows of a work item are
                             (n_heads / n_kv_heads) * q_len (token, head)
-                            pairs: 1, 2, 4, 6 or 8 (SIMT GQA kernel), 8 to 128
+                            pairs: 1 to 8 (SIMT GQA kernel), 8 to 128
                             (tensor-core GQA kernel, 16-bit caches), or 32, 64
                             or 96 (MLA). Every seq_len >= q_len; at most 64.  */
 } da_args_t;

@@ -167,8 +167,8 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
     if (!gqa_config_any(a->kv_dtype, a->head_dim, G, &cfg))
         return fail(DA_EUNSUPPORTED, "plan",
                     "no GQA kernel for head_dim %d, group %d (heads per KV head x q_len), "
-                    "%s KV (head_dim 128 or 256; group 1, 2, 4, 6 or 8, or 8 to 128 for a "
-                    "16-bit cache)",
+                    "%s KV (head_dim 128 or 256; group 1 to 8, or 8 to 128 for a 16-bit "
+                    "cache)",
                     a->head_dim, G, dtype_name(a->kv_dtype));
     kc->kernel = DA_KERNEL_GQA_TMA;
     kc->tile = cfg.tile;

@@ -76,8 +76,10 @@ template <typename DT, typename F> bool gqa_visit(int D, int G, F &&f)
         f(GqaInst<DT, d, g>{});                                                                  \
         return true;                                                                             \
     }
-    SKV_CASE(256, 1) SKV_CASE(256, 2) SKV_CASE(256, 4) SKV_CASE(256, 6) SKV_CASE(256, 8)
-    SKV_CASE(128, 1) SKV_CASE(128, 2) SKV_CASE(128, 4) SKV_CASE(128, 6) SKV_CASE(128, 8)
+    SKV_CASE(256, 1) SKV_CASE(256, 2) SKV_CASE(256, 3) SKV_CASE(256, 4) SKV_CASE(256, 5)
+    SKV_CASE(256, 6) SKV_CASE(256, 7) SKV_CASE(256, 8)
+    SKV_CASE(128, 1) SKV_CASE(128, 2) SKV_CASE(128, 3) SKV_CASE(128, 4) SKV_CASE(128, 5)
+    SKV_CASE(128, 6) SKV_CASE(128, 7) SKV_CASE(128, 8)
 #undef SKV_CASE
     return false;
 }

@@ -560,3 +560,14 @@ def test_combine_proj_validates_weights(lib, proj, status, msg):
                                      fake, fake, fake, fake, p.workspace_bytes, None)
     assert rc == status
 
+
+
+@pytest.mark.parametrize("hq,hkv,d,dt", [(12, 4, 256, N.DA_F32), (40, 8, 128, N.DA_BF16),
+                                         (14, 2, 256, N.DA_F16), (15, 5, 128, N.DA_F16)])
+def test_plan_odd_groups_on_the_simt_kernel(lib, hq, hkv, d, dt):
+    # groups of 3, 5 and 7 heads per KV head (e.g. 40 query / 8 KV heads)
+    a = args(hq=hq, hkv=hkv, d=d, cap=8192, dt=dt)
+    rc, p = plan(lib, a, [8192])
+    assert rc == 0, lib.decode_attn_last_error().decode()
+    assert p.kernel == N.DA_KERNEL_GQA_TMA
+    check_invariants(a, p, [8192], 152)

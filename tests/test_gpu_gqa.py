@@ -272,3 +272,15 @@ def test_refused_launch_is_reported_and_the_context_survives(shape):
     got, _ = run(case)
     worst, rel = errors(case, got, oracle_rows(case))
     assert worst <= (5e-3 if shape == "mla" else TOL[case.kv_dtype]), (worst, rel)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(12, 4, 256), (40, 8, 128), (14, 2, 256), (15, 5, 128)])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_odd_groups(hq, hkv, d, dtype):
+    # 3, 5 and 7 query heads per KV head, ragged lengths around tile boundaries
+    case = W.make_case("t", batch=3, n_heads=hq, n_kv_heads=hkv, head_dim=d,
+                       seq_lens=[1, 333, 5001], kv_dtype=dtype, seed=80 + hq + d)
+    got, da = run(case, poison_ws=True)
+    assert da.plan.kernel == N.DA_KERNEL_GQA_TMA
+    worst, rel = errors(case, got, oracle_rows(case))
+    assert np.all(np.isfinite(got)) and worst <= TOL[dtype], (worst, rel)

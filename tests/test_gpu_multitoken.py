@@ -165,3 +165,14 @@ def test_single_token_in_four_dims_matches_the_three_dim_call_bit_for_bit():
     ref = da(q, k, v)
     torch.cuda.synchronize()
     assert np.array_equal(got3[:, 0], ref.double().cpu().numpy())
+
+
+@pytest.mark.parametrize("hq,hkv,q_len,dtype", [(1, 1, 3, "f32"), (5, 5, 1, "bf16"),
+                                                (1, 1, 5, "f16"), (1, 1, 7, "f32")])
+def test_multi_token_odd_rows_on_the_simt_kernel(hq, hkv, q_len, dtype):
+    lens = [q_len, 100, 2000]
+    case = W.make_case("t", batch=3, n_heads=hq, n_kv_heads=hkv, head_dim=128, seq_lens=lens,
+                       kv_dtype=dtype, seed=760 + q_len)
+    q4 = W.multi_token_q(3, q_len, hq, 128, seed=761 + q_len)
+    got, _ = run_multi(case, q4)
+    assert compare(case, q4, got) <= TOL[dtype]

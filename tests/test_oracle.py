@@ -40,7 +40,8 @@ def run_oracle(c, **kw):
 # ---------------------------------------------------------------------------
 # brute force on tiny inputs, every geometry and storage type
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("hq,hkv", [(1, 1), (2, 1), (4, 2), (8, 2), (6, 1), (12, 2), (16, 4)])
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (2, 1), (4, 2), (8, 2), (6, 1), (12, 2), (16, 4),
+                                    (9, 3), (15, 3), (14, 2)])
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 def test_brute_force_agreement(hq, hkv, dtype):
     c = small(hq, hkv, 16, [1, 5, 33, 64], dtype=dtype, cap=70, scale=0.7, seed=hq * 31 + hkv)
