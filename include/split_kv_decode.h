@@ -68,6 +68,11 @@ typedef enum {
 #define DA_FLAG_NO_COMBINE 0x1   /* decode_attn_splitk_ex runs the split kernel only */
 #define DA_FLAG_GQA_SIMT 0x2     /* for 16-bit caches with 8 rows per work item (see
                                     DA_KERNEL_GQA_TC), use the SIMT kernel instead  */
+#define DA_FLAG_NO_CAUSAL 0x4    /* with q_len > 1: every new token sees every
+                                    position of the (slice of the) cache, for a
+                                    slice that lies wholly before the new tokens,
+                                    e.g. every rank but the last of a
+                                    context-parallel step                          */
 #define DA_FLAG_TEST_NO_TMA 0x100 /* test hook: the producer issues no copy, so every
                                      consumer wait runs out after timeout_us and the
                                      kernel reports DA_ETIMEOUT through device_status */

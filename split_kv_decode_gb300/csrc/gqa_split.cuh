@@ -417,8 +417,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         const int Lb = item_len(p, b);
         const int p1 = min(Lb, p0 + it.chunk[b]); // p1 <= p0: an empty item
         // token i of q_len sees positions below lim0 + i (causal among the new
-        // tokens); with one token lim0 = Lb and no tile reaches past it
-        const int lim0 = Lb - p.q_len + 1;
+        // tokens); with one token lim0 = Lb and no tile reaches past it, and a
+        // slice before the new tokens (DA_FLAG_NO_CAUSAL) has no limit
+        const int lim0 = (p.flags & DA_FLAG_NO_CAUSAL) ? (INT_MAX >> 1) : Lb - p.q_len + 1;
 
         float acc[G][K::EPL];
         float m[G];

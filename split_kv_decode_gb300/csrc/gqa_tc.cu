@@ -399,7 +399,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // ---- tiles
             // token i of q_len sees positions below lim0 + i (causal among the new
             // tokens); with one token every position of the item is visible
-            const int lim = Lb - p.q_len + 1 + token;
+            const int lim =
+                (p.flags & DA_FLAG_NO_CAUSAL) ? (INT_MAX >> 1) : Lb - p.q_len + 1 + token;
             float m = -INFINITY, l = 0.f;
             int bend = first_block_end(p, p0);
             bool firsttile = true;

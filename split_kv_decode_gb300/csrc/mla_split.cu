@@ -52,6 +52,7 @@
 // tile holds a score above m + 8 (log2 units), so P <= 2^8 and l, O^T cannot
 // overflow, and O^T (whose column h spans all lanes) is rescaled only then.
 // Any reference gives the same partial after normalisation.
+#include <climits>
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -520,7 +521,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float m = -INFINITY, l = 0.f;
             // this row's token sees positions below lim (causal among the new
             // tokens; with one token, every position of the item)
-            const int lim = x.L - p.q_len + 1 + (hbase + h) / p.hq;
+            const int lim = (p.flags & DA_FLAG_NO_CAUSAL) ? (INT_MAX >> 1)
+                                                          : x.L - p.q_len + 1 + (hbase + h) / p.hq;
             for (int t = 0; t < x.ntiles; ++t, ++gt) {
                 const int slot = gt & 1;
                 bool okw = mbar_wait_bounded(bar + B_SFULL + slot, (sph >> slot) & 1u,

@@ -15,6 +15,12 @@ rank and the gathered buffer is the input of decode_attn_combine_ranks.
 Slicing: rank r of R holds positions [r * L // R, (r + 1) * L // R) of a
 sequence of length L; slices differ in length by at most one and are non-empty
 when L >= R (required).
+
+Several new tokens per sequence (q [B, q_len, Hq, Dk]): the new tokens are the
+last q_len positions, so they fall in the last rank's slice (every slice must
+hold at least q_len positions); that rank applies the causal limit among them
+and every other rank, whose slice lies wholly before them, runs with
+DA_FLAG_NO_CAUSAL.
 """
 from __future__ import annotations
 
@@ -26,8 +32,10 @@ from . import _native as N
 from . import api as A
 
 
-def context_slices(seq_lens: Sequence[int], world: int) -> List[Tuple[List[int], List[int]]]:
-    """For every rank, (starts, lengths) of its slice of each sequence."""
+def context_slices(seq_lens: Sequence[int], world: int,
+                   min_len: int = 1) -> List[Tuple[List[int], List[int]]]:
+    """For every rank, (starts, lengths) of its slice of each sequence; every
+    slice holds at least min_len positions."""
     if world < 1:
         raise ValueError("world must be >= 1")
     out = []
@@ -35,8 +43,9 @@ def context_slices(seq_lens: Sequence[int], world: int) -> List[Tuple[List[int],
         starts, lens = [], []
         for L in seq_lens:
             L = int(L)
-            if L < world:
-                raise ValueError(f"a sequence of length {L} cannot be split over {world} ranks")
+            if L // world < min_len:
+                raise ValueError(f"a sequence of length {L} cannot be split over {world} ranks "
+                                 f"into slices of at least {min_len} positions")
             s, e = r * L // world, (r + 1) * L // world
             starts.append(s)
             lens.append(e - s)
@@ -81,33 +90,34 @@ def gather(local: torch.Tensor, group=None) -> torch.Tensor:
 class ContextParallelDecode:
     """One rank of a context-parallel decode step.
 
-    q is the full query [B, Hq, Dk] (every rank has it); k_local / v_local are
-    this rank's slices [B, max_slice, Hkv, D] (shard_cache). Calling the object
-    runs the split kernel on the slice, gathers every rank's workspace and
-    merges them into out [B, Hq, Dv] on every rank.
+    q is the full query [B, Hq, Dk], or [B, q_len, Hq, Dk] for several new
+    tokens (every rank has it); k_local / v_local are this rank's slices
+    [B, max_slice, Hkv, D] (shard_cache). Calling the object runs the split
+    kernel on the slice, gathers every rank's workspace and merges them into
+    out (q's shape with Dv last) on every rank.
     """
 
     def __init__(self, q: torch.Tensor, k_local: torch.Tensor, v_local: torch.Tensor,
                  seq_lens: Sequence[int], scale: float, *, rank: int = 0, world: int = 1,
                  group=None, v_dim: Optional[int] = None,
                  out_dtype: torch.dtype = torch.float32):
-        if q.dim() != 3:
-            # the new tokens' causal window would need the global position of each
-            # rank's slice; only the one-token decode is sharded over the context
-            raise ValueError("context-parallel decode takes one query token: q [B, Hq, Dk]")
         self.world, self.rank, self.group = world, rank, group
+        self.q_len = q.shape[1] if q.dim() == 4 else 1
+        flags = N.DA_FLAG_NO_COMBINE
+        if self.q_len > 1 and rank < world - 1:
+            flags |= N.DA_FLAG_NO_CAUSAL        # this slice lies before the new tokens
         self.args = A.make_args(q, k_local, v_local, scale, v_dim=v_dim, out_dtype=out_dtype,
-                                flags=N.DA_FLAG_NO_COMBINE)
+                                flags=flags)
         self.plan = A.decode_attn_plan(self.args, max_slice_lengths(seq_lens, world))
         self.workspace = A.new_workspace(self.plan, device=q.device)
-        _, lens = context_slices(seq_lens, world)[rank]
+        _, lens = context_slices(seq_lens, world, self.q_len)[rank]
         self.local_lens = torch.tensor(lens, dtype=torch.int32, device=q.device)
         self.dev = A.make_dev(seq_lens=self.local_lens)
 
     def set_lengths(self, seq_lens: Sequence[int]) -> None:
         """New lengths (at most those of the plan's): only device memory changes,
         so a captured launch stays valid."""
-        _, lens = context_slices(seq_lens, self.world)[self.rank]
+        _, lens = context_slices(seq_lens, self.world, self.q_len)[self.rank]
         self.local_lens.copy_(torch.tensor(lens, dtype=torch.int32))
 
     def __call__(self, q: torch.Tensor, k_local: torch.Tensor, v_local: torch.Tensor,

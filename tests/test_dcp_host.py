@@ -118,3 +118,11 @@ def test_bench_time_is_the_slowest_ranks_on_gloo():
         mp.spawn(_max_rank, args=(2, _free_port(), d), nprocs=2, join=True)
         got = [float(open(os.path.join(d, f"rank{r}.txt")).read()) for r in range(2)]
     assert got == [15.0, 15.0]
+
+
+def test_context_slices_hold_the_new_tokens():
+    # with q_len new tokens every slice must hold at least q_len positions
+    sl = dcp.context_slices([100, 12], 3, min_len=4)
+    assert all(n >= 4 for _, lens in sl for n in lens)
+    with pytest.raises(ValueError):
+        dcp.context_slices([100, 11], 3, min_len=4)

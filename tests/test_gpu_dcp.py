@@ -100,3 +100,49 @@ def test_tensor_core_gqa_context_parallel(world):
     got = dcp_emulated(case, world)
     worst, rel = errors(case, got, oracle_rows(case))
     assert np.all(np.isfinite(got)) and worst <= TOL["f16"], (worst, rel)
+
+
+@pytest.mark.parametrize("shape,world", [("simt", 2), ("tc", 3), ("mla", 2)])
+def test_context_parallel_several_new_tokens(shape, world):
+    # the new tokens fall in the last rank's slice; the other ranks' slices lie
+    # before them and run without the causal limit (DA_FLAG_NO_CAUSAL)
+    import oracle
+    if shape == "mla":
+        case = W.make_case("mla", batch=1, n_heads=48, n_kv_heads=1, head_dim=576, v_dim=512,
+                           seq_lens=[6000], kv_dtype="f32", scale=1 / math.sqrt(576.0),
+                           seed=750, std=0.5, shared_kv=True)
+        q_len, v_dim, bar = 2, 512, 5e-3
+    elif shape == "tc":
+        case = W.make_case("t", batch=2, n_heads=16, n_kv_heads=4, head_dim=256,
+                           seq_lens=[7001, 2999], kv_dtype="f16", scale=1 / 16, seed=751)
+        q_len, v_dim, bar = 4, None, TOL["f16"]
+    else:
+        case = W.make_case("t", batch=2, n_heads=8, n_kv_heads=4, head_dim=256,
+                           seq_lens=[7001, 2999], kv_dtype="f32", scale=1 / 16, seed=752)
+        q_len, v_dim, bar = 2, None, TOL["f32"]
+    lens = case.seq_lens.tolist()
+    q4 = W.multi_token_q(case.batch, q_len, case.n_heads, case.head_dim, seed=753)
+    q = q4.cuda()
+    dv = case.v_dim
+    wss, step = [], None
+    for r in range(world):
+        kl = dcp.shard_cache(case.k, lens, r, world).cuda()
+        vl = kl if case.shared_kv else dcp.shard_cache(case.v, lens, r, world).cuda()
+        step = dcp.ContextParallelDecode(q, kl, vl, lens, case.scale, rank=r, world=world,
+                                         v_dim=v_dim)
+        scratch = torch.empty(case.batch, q_len, case.n_heads, dv, device="cuda")
+        A.decode_attn_splitk_dev(step.args, step.plan, step.dev, q, kl, vl, scratch,
+                                 step.workspace)
+        wss.append(step.workspace)
+    out = torch.empty(case.batch, q_len, case.n_heads, dv, device="cuda")
+    A.decode_attn_combine_ranks(step.args, step.plan, torch.stack(wss), world, out)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    ref = oracle.attention_multi(q4, case.k, case.v, case.seq_lens, case.scale, v_dim=dv,
+                                 threads=0)
+    worst = 0.0
+    for b, L in enumerate(lens):
+        for t in range(q_len):
+            vm = float(case.v[b, :L - q_len + 1 + t, :, :dv].float().abs().max())
+            worst = max(worst, float(np.max(np.abs(got[b, t] - ref[b, t]))) / vm)
+    assert np.all(np.isfinite(got)) and worst <= bar, worst
