@@ -32,7 +32,7 @@
  *     LSE-weight form e^{LSE_s - LSE*} (The Kernel Level, same section).
  *   - empty segments are neutral: l = 0, m = -1e30 (Attention at 128k §2).
  * It exists so the tests can pin the split identity; it is not the reference
- * the GPU output is judged against (orc_attention is).
+ * the GPU output is compared with (orc_attention is).
  *
  * Storage: K/V elements are read as stored (f32, f16, bf16 or f64) and
  * widened exactly to double, so storage rounding is not part of any
