@@ -1,0 +1,70 @@
+"""Seeded random shapes against the oracle: for each seed a random geometry
+(heads per KV head, head_dim, storage type, batch, lengths from 1 to a few
+thousand, new tokens per sequence, output type, forced split count) runs through
+whichever kernel the plan picks, and every row is compared with the oracle."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from split_kv_decode_gb300 import _native as N
+from split_kv_decode_gb300 import api as A
+from split_kv_decode_gb300 import workloads as W
+from tests.gpu_util import TOL
+
+pytestmark = pytest.mark.gpu
+
+_TDT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+_ROUND = {"f32": 0.0, "f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+def draw(seed):
+    g = np.random.default_rng(seed)
+    dtype = ["f32", "f16", "bf16"][g.integers(3)]
+    d = [128, 256][g.integers(2)]
+    hkv = int(g.integers(1, 5))
+    gh = int(g.integers(1, 9))
+    q_len = int(g.choice([1, 1, 1, 2, 3, 4]))
+    if dtype == "f32":                       # the SIMT kernel: at most 8 rows per item
+        while gh * q_len > 8:
+            q_len -= 1
+            if q_len == 0:
+                q_len, gh = 1, 8
+    batch = int(g.integers(1, 7))
+    lens = [int(x) for x in g.integers(q_len, 6000, size=batch)]
+    if g.random() < 0.3:
+        lens[0] = q_len                      # a sequence no longer than its new tokens
+    out_dtype = ["f32", "f16", "bf16"][g.integers(3)]
+    force = int(g.choice([0, 0, 0, 1, 3, 17]))
+    return dtype, d, hkv, gh, q_len, batch, lens, out_dtype, force
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_shape(seed):
+    dtype, d, hkv, gh, q_len, batch, lens, out_dtype, force = draw(1000 + seed)
+    hq = hkv * gh
+    case = W.make_case("r", batch=batch, n_heads=hq, n_kv_heads=hkv, head_dim=d, seq_lens=lens,
+                       kv_dtype=dtype, seed=2000 + seed)
+    q4 = W.multi_token_q(batch, q_len, hq, d, seed=3000 + seed)
+    q = q4.cuda() if q_len > 1 else q4[:, 0].contiguous().cuda()
+    k, v = case.k.cuda(), case.v.cuda()
+    da = A.DecodeAttention(q, k, v, lens, case.scale, out_dtype=_TDT[out_dtype],
+                           force_splits=force)
+    da.workspace.fill_(0xFF)
+    out = da(q, k, v)
+    torch.cuda.synchronize()
+    A.decode_attn_device_status(da.workspace)
+    got = out.double().cpu().numpy().reshape(batch, q_len, hq, d)
+    assert np.all(np.isfinite(got))
+    ref = oracle.attention_multi(q4, case.k, case.v, case.seq_lens, case.scale, threads=0)
+    worst = 0.0
+    for b, L in enumerate(lens):
+        for t in range(q_len):
+            vm = float(case.v[b, :L - q_len + 1 + t].float().abs().max())
+            err = float(np.max(np.abs(got[b, t] - ref[b, t])))
+            bound = TOL[dtype] * vm + _ROUND[out_dtype] * float(np.max(np.abs(ref[b, t])))
+            worst = max(worst, err / bound)
+    kernel = {N.DA_KERNEL_GQA_TMA: "simt", N.DA_KERNEL_GQA_TC: "tc"}[da.plan.kernel]
+    assert worst <= 1.0, (dtype, d, hkv, gh, q_len, lens, out_dtype, force, kernel, worst)
