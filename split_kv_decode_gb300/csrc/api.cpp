@@ -813,6 +813,9 @@ void decode_attn_release(void)
     cudaSetDevice(cur);
 }
 
-const char *decode_attn_version(void) { return "split_kv_decode_gb300 0.1 (sm_103a)"; }
+const char *decode_attn_version(void)
+{
+    return "split_kv_decode_gb300 0.2 (sm_103a: SIMT and tcgen05 GQA, tcgen05 MLA, combine with projection)";
+}
 
 } // extern "C"
