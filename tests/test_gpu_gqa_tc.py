@@ -199,3 +199,22 @@ def test_tensor_core_timed_out_wait_is_reported_and_the_context_survives():
     assert e.value.status == N.DA_ETIMEOUT
     assert "tensor cores" in e.value.message
     check_single(case)
+
+
+def test_tensor_core_head_major_and_padded_caches():
+    # the same values in a head-major cache, and in a position-major cache whose
+    # rows are padded (strides are free as long as they are 16-byte multiples)
+    case = case_of(32, 2, 128, "bf16", lens=[1000, 3001], seed=996)
+    q, k, v = to_device(case)
+    kh = k.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    vh = v.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    got, da = run(case, dev=(q, kh, vh))
+    assert da.plan.kernel == N.DA_KERNEL_GQA_TC
+    worst, _ = errors(case, got, oracle_rows(case))
+    assert worst <= TOL["bf16"]
+    kp = torch.zeros(k.shape[0], k.shape[1], k.shape[2], 136, dtype=k.dtype, device="cuda")
+    vp = torch.zeros_like(kp)
+    kp[..., :128] = k
+    vp[..., :128] = v
+    got2, _ = run(case, dev=(q, kp[..., :128], vp[..., :128]))
+    assert np.array_equal(got, got2)

@@ -176,3 +176,19 @@ def test_mla_several_new_tokens_device_lengths():
     q4 = W.multi_token_q(2, 2, 32, 576, seed=3131)
     got = _run_multi(case, q4, dev_lens=[2000, 1])        # 1 is kept at q_len
     assert _multi_errors(case, q4, got, lens=[2000, 2]) <= BF16_BAR
+
+
+def test_mla_padded_latent_rows():
+    # latent rows padded to 640 elements: the kernel follows the row stride
+    case = mla_case([5000], heads=64, seed=3200)
+    kp = torch.zeros(1, 5000, 1, 640)
+    kp[..., :576] = case.k
+    k = kp.cuda()[..., :576]
+    q = case.q.cuda()
+    da = A.DecodeAttention(q, k, k, [5000], case.scale, v_dim=512)
+    assert da.plan.kernel == N.DA_KERNEL_MLA_TC
+    out = da(q, k, k)
+    torch.cuda.synchronize()
+    A.decode_attn_device_status(da.workspace)
+    worst, rel = errors(case, out.double().cpu().numpy(), oracle_rows(case))
+    assert worst <= F32_BAR, (worst, rel)
