@@ -410,7 +410,7 @@ def main():
         if kernel == "gqa_split_kernel" and case.q.dim() == 3:
             line["graph"] = measure_graph(case, q, k, v, out_dt, dev, flush, args)
             line["paged"] = {f"block_{bs}": measure_paged(case, q, k, v, out_dt, dev, flush, args, bs)
-                             for bs in (64, 256)}
+                             for bs in (16, 64, 256)}
             ml = measure_multi_token(case, k, v, out_dt, dev, flush, args)
             if ml:
                 line["multi_token"] = ml
@@ -471,8 +471,8 @@ def measure_graph(case, q, k, v, out_dt, dev, flush, args):
 def measure_paged(case, q, k, v, out_dt, dev, flush, args, block_size):
     """The same step with the caches scattered into pools of `block_size`-position
     blocks in a random order, read through a block table (decode_attn_splitk_dev).
-    A tile never spans two blocks, so blocks that the tile does not divide cost
-    partial tiles."""
+    A tile is copied as boxes of gcd(tile, block_size) rows, each inside one
+    block, so tiles stay whole at any block size."""
     import torch
     from split_kv_decode_gb300 import api as A
     B, cap, hkv, dk = k.shape

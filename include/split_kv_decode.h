@@ -328,16 +328,24 @@ int decode_attn_splitk_noalloc(const da_args_t *args, const da_plan_t *plan, con
  *   block_table   DEVICE int32[batch * max_blocks_per_seq], or NULL for the
  *                 contiguous caches of da_args_t. Entry [b][i] is the pool block
  *                 that holds positions [i * block_size, (i + 1) * block_size)
- *                 of sequence b; entries past a sequence's length are not read.
+ *                 of sequence b. Entries past a sequence's length may be loaded,
+ *                 and the GQA kernels may copy rows of the blocks they name by TMA
+ *                 for positions they then mask (any value is safe there: TMA reads
+ *                 zeros outside the pool); no result depends on them.
  *                 With a table, k_cache / v_cache point at pools whose element
  *                 (block, slot, kv, d) is at base + block * *_block_stride +
  *                 slot * *_pos_stride + kv * *_head_stride + d (elements);
  *                 capacity and the batch strides of da_args_t are not used for
  *                 addressing (capacity must still cover every length).
- *   block_size    positions per block: a positive multiple of 16. A tile of the
- *                 split kernel never spans two blocks, so blocks of 128 or more
- *                 positions stream at nearly the contiguous rate; smaller
- *                 blocks cost partial tiles.
+ *   block_size    positions per block: a positive multiple of 16. Tiles run
+ *                 across block ends, so every block size streams whole tiles:
+ *                 the SIMT GQA kernel copies a tile that lies in one block as one
+ *                 TMA box and one that spans a block end as a few boxes per
+ *                 block, the tensor-core GQA kernel every tile as boxes of
+ *                 gcd(64, block_size) rows; box heights are multiples of
+ *                 gcd(tile, block_size), so the plan's chunks must be too (the
+ *                 planner's are multiples of the tile; DA_EINVAL otherwise). The
+ *                 MLA kernel looks up every row.
  *   num_blocks    blocks in each pool; table entries must be < num_blocks.
  *   k_block_stride, v_block_stride  elements between blocks (16-byte multiples,
  *                 at least block_size * pos_stride).

@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <numeric>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -23,12 +24,12 @@ namespace skv {
 bool gqa_config_f32(int D, int G, GqaConfig *cfg);
 bool gqa_config_f16(int D, int G, GqaConfig *cfg);
 bool gqa_config_bf16(int D, int G, GqaConfig *cfg);
-cudaError_t gqa_launch_f32(int D, int G, int grid, cudaStream_t st, const CUtensorMap &km,
-                           const CUtensorMap &vm, const SplitParams &p);
-cudaError_t gqa_launch_f16(int D, int G, int grid, cudaStream_t st, const CUtensorMap &km,
-                           const CUtensorMap &vm, const SplitParams &p);
-cudaError_t gqa_launch_bf16(int D, int G, int grid, cudaStream_t st, const CUtensorMap &km,
-                            const CUtensorMap &vm, const SplitParams &p);
+cudaError_t gqa_launch_f32(int D, int G, int grid, cudaStream_t st,
+                           const GqaMaps &maps, const SplitParams &p);
+cudaError_t gqa_launch_f16(int D, int G, int grid, cudaStream_t st,
+                           const GqaMaps &maps, const SplitParams &p);
+cudaError_t gqa_launch_bf16(int D, int G, int grid, cudaStream_t st,
+                           const GqaMaps &maps, const SplitParams &p);
 
 namespace {
 
@@ -364,7 +365,8 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     }
     p.items.split_base[a->batch] = pl->total_splits;
 
-    CUtensorMap km, vm;
+    GqaMaps m;
+    std::memset(&m, 0, sizeof m);
     int rc;
     const bool tc = pl->kernel == DA_KERNEL_GQA_TC;
     if (dev && dev->block_table) {
@@ -372,20 +374,28 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
         p.max_blocks = dev->max_blocks_per_seq;
         p.block_size = dev->block_size;
         p.oob_block = dev->num_blocks;
-        rc = encode_pool_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, dev->block_size,
-                             dev->num_blocks, a->k_head_stride, a->k_pos_stride,
-                             dev->k_block_stride, pl->tile, tc);
-        if (rc) return rc;
-        rc = encode_pool_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, dev->block_size,
-                             dev->num_blocks, a->v_head_stride, a->v_pos_stride,
-                             dev->v_block_stride, pl->tile, tc);
-        if (rc) return rc;
+        // Tiles run across block ends. The tensor-core kernel copies every tile
+        // as boxes of box_rows rows, which never span a block. The SIMT kernel
+        // copies a tile that lies in one block as one box of T rows (maps k, v)
+        // and one that spans a block end as boxes of box_rows rows (maps kb, vb).
+        p.box_rows = std::gcd(pl->tile, dev->block_size);
+        auto pool = [&](CUtensorMap *km, CUtensorMap *vm, int rows) {
+            int r = encode_pool_map(km, k, a->kv_dtype, a->head_dim, a->n_kv_heads,
+                                    dev->block_size, dev->num_blocks, a->k_head_stride,
+                                    a->k_pos_stride, dev->k_block_stride, rows, tc);
+            if (r) return r;
+            return encode_pool_map(vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, dev->block_size,
+                                   dev->num_blocks, a->v_head_stride, a->v_pos_stride,
+                                   dev->v_block_stride, rows, tc);
+        };
+        if ((rc = pool(&m.k, &m.v, tc ? p.box_rows : pl->tile))) return rc;
+        if (!tc && (rc = pool(&m.kb, &m.vb, p.box_rows))) return rc;
     } else {
-        rc = encode_cache_map(&km, k, a->kv_dtype, a->head_dim, a->n_kv_heads, a->capacity,
+        rc = encode_cache_map(&m.k, k, a->kv_dtype, a->head_dim, a->n_kv_heads, a->capacity,
                               a->batch, a->k_head_stride, a->k_pos_stride, a->k_batch_stride,
                               pl->tile, tc);
         if (rc) return rc;
-        rc = encode_cache_map(&vm, v, a->kv_dtype, a->v_dim, a->n_kv_heads, a->capacity,
+        rc = encode_cache_map(&m.v, v, a->kv_dtype, a->v_dim, a->n_kv_heads, a->capacity,
                               a->batch, a->v_head_stride, a->v_pos_stride, a->v_batch_stride,
                               pl->tile, tc);
         if (rc) return rc;
@@ -393,7 +403,7 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     if (dev) p.dev_lens = dev->seq_lens;
     if (tc) {
         const cudaError_t e =
-            launch_gqa_tc(a->kv_dtype, a->head_dim, split_grid(a, pl), st, km, vm, p);
+            launch_gqa_tc(a->kv_dtype, a->head_dim, split_grid(a, pl), st, m.k, m.v, p);
         if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
         return DA_OK;
     }
@@ -401,9 +411,9 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     const int G = a->n_heads / a->n_kv_heads * q_len_of(a);
     cudaError_t e;
     switch (a->kv_dtype) {
-    case DA_F32: e = gqa_launch_f32(a->head_dim, G, split_grid(a, pl), st, km, vm, p); break;
-    case DA_F16: e = gqa_launch_f16(a->head_dim, G, split_grid(a, pl), st, km, vm, p); break;
-    default: e = gqa_launch_bf16(a->head_dim, G, split_grid(a, pl), st, km, vm, p); break;
+    case DA_F32: e = gqa_launch_f32(a->head_dim, G, split_grid(a, pl), st, m, p); break;
+    case DA_F16: e = gqa_launch_f16(a->head_dim, G, split_grid(a, pl), st, m, p); break;
+    default: e = gqa_launch_bf16(a->head_dim, G, split_grid(a, pl), st, m, p); break;
     }
     if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
     return DA_OK;
@@ -621,6 +631,18 @@ int decode_attn_splitk_dev(const da_args_t *a, const da_plan_t *plan, const da_d
                 return fail(DA_EINVAL, "args",
                             "seq_lens[%d] = %d exceeds max_blocks_per_seq x block_size", b,
                             plan->seq_lens[b]);
+        // the GQA kernels copy a paged tile in boxes of multiples of gcd(tile,
+        // block_size) rows that start at multiples of that height, so a split
+        // must start at one
+        if (kc.kernel != DA_KERNEL_MLA_TC) {
+            const int h = std::gcd(plan->tile, dev->block_size);
+            for (int b = 0; b < a->batch; ++b)
+                if (plan->chunk[b] % h)
+                    return fail(DA_EINVAL, "plan",
+                                "chunk[%d] = %d: paged caches need chunks that are multiples "
+                                "of %d",
+                                b, plan->chunk[b], h);
+        }
     }
     if (!ws || !aligned(ws, 256))
         return fail(DA_EINVAL, "args", "workspace must be non-NULL and 256-byte aligned");

@@ -5,10 +5,10 @@ namespace skv {
 
 bool gqa_config_f16(int D, int G, GqaConfig *cfg) { return gqa_config_dt<__half>(D, G, cfg); }
 
-cudaError_t gqa_launch_f16(int D, int G, int grid, cudaStream_t st, const CUtensorMap &km,
-                          const CUtensorMap &vm, const SplitParams &p)
+cudaError_t gqa_launch_f16(int D, int G, int grid, cudaStream_t st, const GqaMaps &maps,
+                        const SplitParams &p)
 {
-    return gqa_launch_dt<__half>(D, G, grid, st, km, vm, p);
+    return gqa_launch_dt<__half>(D, G, grid, st, maps, p);
 }
 
 } // namespace skv

@@ -43,6 +43,9 @@ template <int ES, int D, int G> struct GqaGeom {
     static constexpr int NST = cmin(6, 184320 / STAGE);
     static_assert(NST >= 2, "at least two stages");
     static_assert(P % RPW == 0, "whole row steps");
+    // a paged tile that spans a block end is T / gcd(T, block_size) boxes, at
+    // most T / gcd(T, 16) = NCW when P <= 16: one per lane of the producer warp
+    static_assert(P <= 16 && NCW <= 32, "paged boxes per tile");
     static_assert(!WIDE || gqa_reg_est(P / RPW, G, EPL) <= 168, "register estimate");
 };
 
@@ -56,14 +59,14 @@ template <typename DT, int D, int G> struct GqaInst {
         c->smem_bytes = Ker::SMEM_ALLOC;
         c->threads = Ker::THREADS;
     }
-    static cudaError_t launch(int grid, cudaStream_t st, const CUtensorMap &km,
-                              const CUtensorMap &vm, const SplitParams &p)
+    static cudaError_t launch(int grid, cudaStream_t st, const GqaMaps &maps,
+                              const SplitParams &p)
     {
         auto *fn = gqa_split_kernel<DT, D, G, Geo::T, Geo::NCW, Geo::NST, Geo::LPR>;
         cudaError_t e =
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Ker::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        fn<<<grid, Ker::THREADS, Ker::SMEM_ALLOC, st>>>(km, vm, p);
+        fn<<<grid, Ker::THREADS, Ker::SMEM_ALLOC, st>>>(maps, p);
         return cudaGetLastError();
     }
 };
@@ -90,11 +93,11 @@ template <typename DT> bool gqa_config_dt(int D, int G, GqaConfig *cfg)
 }
 
 template <typename DT>
-cudaError_t gqa_launch_dt(int D, int G, int grid, cudaStream_t st, const CUtensorMap &km,
-                          const CUtensorMap &vm, const SplitParams &p)
+cudaError_t gqa_launch_dt(int D, int G, int grid, cudaStream_t st, const GqaMaps &maps,
+                          const SplitParams &p)
 {
     cudaError_t err = cudaErrorInvalidValue;
-    gqa_visit<DT>(D, G, [&](auto inst) { err = decltype(inst)::launch(grid, st, km, vm, p); });
+    gqa_visit<DT>(D, G, [&](auto inst) { err = decltype(inst)::launch(grid, st, maps, p); });
     return err;
 }
 

@@ -181,22 +181,10 @@ __device__ __forceinline__ int item_len(const SplitParams &p, int b)
     return p.dev_lens ? max(p.q_len, min(__ldg(p.dev_lens + b), L)) : L;
 }
 
-// A tile is T rows, cut at the item's end and, for a paged cache, at the end
-// of its block (a tile never spans two blocks). The next block boundary is
-// tracked from the item's start, so a tile costs no division; contiguous caches
-// have no boundary.
-__device__ __forceinline__ int first_block_end(const SplitParams &p, int p0)
-{
-    return p.block_table ? (p0 / p.block_size + 1) * p.block_size : INT_MAX;
-}
-
-template <int T>
-__device__ __forceinline__ int tile_end(int t0, int p1, int &bend, int bs)
-{
-    const int e = min(min(t0 + T, p1), bend);
-    if (e == bend) bend += bs;
-    return e;
-}
+// A tile is T rows, cut only at the item's end: in a paged cache tiles run
+// across block ends like in a contiguous one (the producers copy such tiles
+// piecewise, each piece from its own block).
+template <int T> __device__ __forceinline__ int tile_end(int t0, int p1) { return min(t0 + T, p1); }
 
 template <int X> __host__ __device__ constexpr int align_up(int v) { return (v + X - 1) / X * X; }
 
@@ -246,9 +234,7 @@ template <typename DT, int D, int G, int T, int NCW, int NST, int LPR> struct Gq
 
 template <typename DT, int D, int G, int T, int NCW, int NST, int LPR>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1)
-    gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap,
-                     const __grid_constant__ SplitParams p)
+    gqa_split_kernel(const __grid_constant__ GqaMaps maps, const __grid_constant__ SplitParams p)
 {
     using K = GqaKernel<DT, D, G, T, NCW, NST, LPR>;
     extern __shared__ uint8_t smem_raw[];
@@ -280,15 +266,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         // Lane 0 waits on the stage barriers and issues the copies. For paged
         // caches the whole warp walks the items and tiles: the lanes hold a
         // window of 32 consecutive block-table entries of the current sequence
-        // (one coalesced load); a tile never spans two blocks (tile_end), so a
-        // tile is still one TMA box of T rows, whose rows past the block are
-        // read as zeros and masked. For contiguous caches lane 0 walks alone.
+        // (one coalesced load). A tile whose rows lie in one block is one TMA box
+        // of T rows; a tile that spans a block end is T / box_rows short boxes. So
+        // tiles run across blocks as in a contiguous cache and every stage
+        // carries a full tile. For contiguous caches lane 0 walks alone.
         const bool paged = p.block_table != nullptr;
         if (!paged && lane != 0) return;
         const unsigned mask = paged ? 0xffffffffu : 1u;
         if (lane == 0) {
-            tma_prefetch_map(&kmap);
-            tma_prefetch_map(&vmap);
+            tma_prefetch_map(&maps.k);
+            tma_prefetch_map(&maps.v);
+            if (paged) {
+                tma_prefetch_map(&maps.kb);
+                tma_prefetch_map(&maps.vb);
+            }
         }
         const uint64_t pol = l2_evict_first_policy();
         int last_parity[NST];
@@ -299,15 +290,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         bool ok = true;
         int win_b = -1, win_lo = 0;
         int32_t win_entry = 0;
+        // paged: tile and block lengths in units of the box height
+        const int hrows = paged ? p.box_rows : 1;
+        const int tile_u = T / hrows, block_u = paged ? p.block_size / hrows : 1;
         for (int item = blockIdx.x; ok && item < it.n_items; item += gridDim.x) {
             int b, kvh, s;
             decode_item(it, item, b, kvh, s);
             const int Lb = item_len(p, b);
             const int p0 = s * it.chunk[b];
             const int p1 = min(Lb, p0 + it.chunk[b]);
-            int bend = first_block_end(p, p0);
+            // paged: block index and slot of the tile start (slot in units of
+            // h = box_rows), advanced without divisions: the producer's time per
+            // tile is on the copy path
+            const int bs = p.block_size;
+            int bi = paged ? p0 / bs : 0, su = paged ? (p0 - bi * bs) / hrows : 0;
             for (int t0 = p0, t1; t0 < p1; t0 = t1) {
-                t1 = tile_end<T>(t0, p1, bend, p.block_size);
+                t1 = tile_end<T>(t0, p1);
                 bool got = true;
                 if (lane == 0)
                     got = mbar_wait_bounded(empty + stage, phase ^ 1u, p.timeout_ns, abort_flag);
@@ -317,24 +315,66 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                 }
                 if (!(p.flags & DA_FLAG_TEST_NO_TMA)) {
                     uint8_t *dst = smem + stage * K::STAGE_BYTES;
-                    int c2 = t0, c3 = b; // contiguous: (position, sequence)
-                    if (paged) {         // paged: (slot in block, block)
-                        const int idx = t0 / p.block_size;
-                        if (b != win_b || idx < win_lo || idx >= win_lo + 32) {
+                    if (paged) {
+                        // the window covers the kSpan blocks from bi, as many as a
+                        // tile can touch (blocks hold 16 or more positions)
+                        constexpr int kSpan = (T + 14) / 16 + 1;
+                        static_assert(kSpan <= 32, "window of 32 table entries");
+                        if (b != win_b || bi < win_lo || bi + kSpan > win_lo + 32) {
                             win_b = b;
-                            win_lo = idx;
-                            win_entry = (idx + lane < p.max_blocks)
-                                            ? p.block_table[(size_t)b * p.max_blocks + idx + lane]
+                            win_lo = bi;
+                            win_entry = (bi + lane < p.max_blocks)
+                                            ? p.block_table[(size_t)b * p.max_blocks + bi + lane]
                                             : p.oob_block;
                         }
-                        c3 = __shfl_sync(0xffffffffu, win_entry, idx - win_lo);
-                        c2 = t0 - idx * p.block_size;
-                    }
-                    // rows of the box past the block (or the pool) are read as zeros
-                    if (lane == 0) {
+                        const int so = su * hrows;
+                        if (so + (t1 - t0) <= bs) {
+                            // the tile's rows lie in one block: one box of T rows at
+                            // (slot in block, block); rows of the box past the block
+                            // lie past the item's end and read as zeros
+                            const int blk = __shfl_sync(0xffffffffu, win_entry, bi - win_lo);
+                            if (lane == 0) {
+                                mbar_arrive_expect_tx(full + stage, K::STAGE_BYTES);
+                                tma_load_4d(dst, &maps.k, full + stage, 0, kvh, so, blk, pol);
+                                tma_load_4d(dst + K::TILE_BYTES, &maps.v, full + stage, 0, kvh,
+                                            so, blk, pol);
+                            }
+                        } else {
+                            // the tile spans a block end: it is copied as T / h boxes
+                            // of h = box_rows rows (h divides T and block_size, so no
+                            // box spans a block), lane i copying box i from the block
+                            // that holds it; every lane walks the blocks' shares of the
+                            // tile (the block comes by shuffle), so the boxes go out
+                            // in one warp instruction
+                            int br = -1, bslot = 0, bblk = 0;
+                            for (int ru = 0, nb = 0, blki = bi, s0 = su; ru < tile_u;
+                                 ++blki, s0 = 0) {
+                                const int len = min(tile_u - ru, block_u - s0);
+                                const int blk = __shfl_sync(0xffffffffu, win_entry, blki - win_lo);
+                                const int i = lane - nb;
+                                if (i >= 0 && i < len) {
+                                    br = ru + i;
+                                    bslot = (s0 + i) * hrows;
+                                    bblk = blk;
+                                }
+                                nb += len;
+                                ru += len;
+                            }
+                            if (lane == 0) mbar_arrive_expect_tx(full + stage, K::STAGE_BYTES);
+                            __syncwarp();
+                            if (br >= 0) {
+                                const int off = br * hrows * D * K::ES;
+                                tma_load_4d(dst + off, &maps.kb, full + stage, 0, kvh, bslot, bblk,
+                                            pol);
+                                tma_load_4d(dst + K::TILE_BYTES + off, &maps.vb, full + stage, 0,
+                                            kvh, bslot, bblk, pol);
+                            }
+                        }
+                        for (su += tile_u; su >= block_u; su -= block_u) ++bi;
+                    } else if (lane == 0) { // contiguous: one box at (position, sequence)
                         mbar_arrive_expect_tx(full + stage, K::STAGE_BYTES);
-                        tma_load_4d(dst, &kmap, full + stage, 0, kvh, c2, c3, pol);
-                        tma_load_4d(dst + K::TILE_BYTES, &vmap, full + stage, 0, kvh, c2, c3, pol);
+                        tma_load_4d(dst, &maps.k, full + stage, 0, kvh, t0, b, pol);
+                        tma_load_4d(dst + K::TILE_BYTES, &maps.v, full + stage, 0, kvh, t0, b, pol);
                     }
 #pragma unroll
                     for (int x = 0; x < NST; ++x)
@@ -436,9 +476,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         __syncwarp();
 
         bool aborted = false;
-        int bend = first_block_end(p, p0);
         for (int t0 = p0, t1; t0 < p1; t0 = t1) {
-            t1 = tile_end<T>(t0, p1, bend, p.block_size);
+            t1 = tile_end<T>(t0, p1);
             if (!mbar_wait_bounded(full + stage, phase, p.timeout_ns, abort_flag)) {
                 aborted = true;
                 break;

@@ -29,7 +29,8 @@
 //              (reference max moved only by more than 8 in log2 units). In
 //              the epilogue thread e reads value column e of O^T.
 //   warp 4     TMA producer (one lane; the whole warp for paged caches, as in
-//              the SIMT kernel: tiles are cut at block ends).
+//              the SIMT kernel: a tile is copied as boxes that each lie in one
+//              block, so tiles span blocks).
 //   warp 5     TMEM owner and the one thread that issues the MMAs; it polls
 //              QK(t+1) (tile in, S slot free) and PV(t) (P written) and
 //              issues whichever is ready.
@@ -98,7 +99,7 @@ __device__ __forceinline__ bool tc_bar_or(bool pred)
 // cut at its end and (paged caches) at block ends; items without positions
 // (device lengths shorter than the plan's) have no tiles and are skipped.
 template <int T> struct Walk {
-    int item, b, kvh, s, p0, p1, t0, t1, bend, gt;
+    int item, b, kvh, s, p0, p1, t0, t1, gt;
     bool done, first;
     __device__ __forceinline__ void load_item(const SplitParams &p)
     {
@@ -112,8 +113,7 @@ template <int T> struct Walk {
             item += gridDim.x;
         }
         t0 = p0;
-        bend = first_block_end(p, p0);
-        t1 = tile_end<T>(t0, p1, bend, p.block_size);
+        t1 = tile_end<T>(t0, p1);
         first = true;
     }
     __device__ __forceinline__ void start(const SplitParams &p)
@@ -131,7 +131,7 @@ template <int T> struct Walk {
             load_item(p);
         } else {
             t0 = t1;
-            t1 = tile_end<T>(t0, p1, bend, p.block_size);
+            t1 = tile_end<T>(t0, p1);
             first = false;
         }
     }
@@ -215,29 +215,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-                int c2 = w.t0, c3 = w.b; // contiguous: (position, sequence)
-                if (paged) {             // paged: (slot in block, block)
-                    const int idx = w.t0 / p.block_size;
-                    if (w.b != win_b || idx < win_lo || idx >= win_lo + 32) {
+                if (p.flags & DA_FLAG_TEST_NO_TMA) continue;
+                uint8_t *dst = sm + L.stage_off + st * L.stage_bytes;
+                if (paged) {
+                    // box j holds rows [t0 + j*h, t0 + (j+1)*h) of every 64-column
+                    // chunk, h = box_rows (16, 32 or 64: a divisor of the tile and of
+                    // block_size), so no box spans two blocks and a tile spans blocks
+                    // freely; h * 128 bytes is a multiple of the 1024-byte swizzle
+                    // atom, so the boxes land in the layout one 64-row box would give
+                    const int bs = p.block_size, h = p.box_rows, nbox = T / h;
+                    const int lo = w.t0 / bs, hi = (w.t0 + T - 1) / bs;
+                    if (w.b != win_b || lo < win_lo || hi >= win_lo + 32) {
                         win_b = w.b;
-                        win_lo = idx;
-                        win_entry = (idx + lane < p.max_blocks)
-                                        ? p.block_table[(size_t)w.b * p.max_blocks + idx + lane]
+                        win_lo = lo;
+                        win_entry = (lo + lane < p.max_blocks)
+                                        ? p.block_table[(size_t)w.b * p.max_blocks + lo + lane]
                                         : p.oob_block;
                     }
-                    c3 = __shfl_sync(0xffffffffu, win_entry, idx - win_lo);
-                    c2 = w.t0 - idx * p.block_size;
-                }
-                if (lane == 0 && !(p.flags & DA_FLAG_TEST_NO_TMA)) {
-                    // rows of a box past the block (or the pool, or the cache) read as zeros
-                    uint8_t *dst = sm + L.stage_off + st * L.stage_bytes;
+                    const int pos = w.t0 + min(lane, nbox - 1) * h;
+                    const int idx = pos / bs;
+                    const int blk = __shfl_sync(0xffffffffu, win_entry, idx - win_lo);
+                    if (lane == 0) mbar_arrive_expect_tx(bar + TB_FULL + st, L.stage_bytes);
+                    __syncwarp();
+                    if (lane < nbox) {
+                        // rows of a box past the pool read as zeros
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            const int off = c * L.chunk_bytes + lane * h * 128;
+                            tma_load_4d(dst + off, &kmap, bar + TB_FULL + st, c * 64, w.kvh,
+                                        pos - idx * bs, blk, pol);
+                            tma_load_4d(dst + L.tile_bytes + off, &vmap, bar + TB_FULL + st,
+                                        c * 64, w.kvh, pos - idx * bs, blk, pol);
+                        }
+                    }
+                } else if (lane == 0) {
+                    // contiguous: one box per chunk at (position, sequence); rows past
+                    // the cache read as zeros
                     mbar_arrive_expect_tx(bar + TB_FULL + st, L.stage_bytes);
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
                         tma_load_4d(dst + c * L.chunk_bytes, &kmap, bar + TB_FULL + st, c * 64,
-                                    w.kvh, c2, c3, pol);
+                                    w.kvh, w.t0, w.b, pol);
                         tma_load_4d(dst + L.tile_bytes + c * L.chunk_bytes, &vmap,
-                                    bar + TB_FULL + st, c * 64, w.kvh, c2, c3, pol);
+                                    bar + TB_FULL + st, c * 64, w.kvh, w.t0, w.b, pol);
                     }
                 }
             }
@@ -402,10 +422,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int lim =
                 (p.flags & DA_FLAG_NO_CAUSAL) ? (INT_MAX >> 1) : Lb - p.q_len + 1 + token;
             float m = -INFINITY, l = 0.f;
-            int bend = first_block_end(p, p0);
             bool firsttile = true;
             for (int t0 = p0, t1; t0 < p1; t0 = t1, ++gt, firsttile = false) {
-                t1 = tile_end<T>(t0, p1, bend, p.block_size);
+                t1 = tile_end<T>(t0, p1);
                 const int ss = gt & 1;
                 // S(t) is in, and PV(t-2) is done with this P slot; the outcome of
                 // both waits joins the rescale vote below (one block-wide vote per

@@ -65,6 +65,8 @@ struct SplitParams {
     int32_t max_blocks;
     int32_t block_size;
     int32_t oob_block;       // a block coordinate past the pool: TMA fills zeros there
+    int32_t box_rows;        // paged: gcd(tile, block_size), so no box of box_rows rows
+                             // that starts at a multiple of box_rows spans two blocks
     ItemTable items;
 };
 
@@ -174,14 +176,12 @@ __host__ __device__ inline TcLayout tc_layout(int D, int R)
 cudaError_t launch_gqa_tc(int kv_dtype, int head_dim, int grid, cudaStream_t st,
                           const CUtensorMap &km, const CUtensorMap &vm, const SplitParams &p);
 
-// Launchers (return cudaError_t of the launch).
-struct GqaLaunch {
-    int kv_dtype, head_dim, group;      // selects the instantiation
-    int grid;
-    cudaStream_t stream;
+// TMA maps of the SIMT GQA kernel: k and v copy a whole tile of T rows; for a
+// paged pool kb and vb copy box_rows rows, the boxes of a tile that spans a
+// block end (contiguous caches: left zero, unused).
+struct GqaMaps {
+    CUtensorMap k, v, kb, vb;
 };
-cudaError_t launch_gqa_split(const GqaLaunch &L, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                             const SplitParams &p);
 // Static configuration of a GQA instantiation (tile rows, CTAs per SM, smem).
 struct GqaConfig {
     int tile;

@@ -417,6 +417,29 @@ def test_dev_call_validates_before_launch(lib, mutate, status, msg):
     assert msg in lib.decode_attn_last_error().decode()
 
 
+@pytest.mark.parametrize("hq,hkv,d,bs,kernel", [(32, 1, 128, 16, N.DA_KERNEL_GQA_TC),
+                                                (16, 4, 256, 64, N.DA_KERNEL_GQA_TMA)])
+def test_dev_call_paged_needs_chunks_on_the_box_grid(lib, hq, hkv, d, bs, kernel):
+    # the GQA kernels copy a paged tile as boxes whose heights are multiples of
+    # gcd(tile, block_size), starting at multiples of it, so a hand-made plan
+    # whose chunk is off that grid is refused before any launch (the planner's
+    # chunks are multiples of the tile)
+    a = paged_args(hq=hq, hkv=hkv, d=d, block_size=bs, max_blocks=640 // bs)
+    rc, p = plan(lib, a, [500, 300])
+    assert rc == 0 and p.kernel == kernel
+    h = math.gcd(p.tile, bs)
+    assert all(p.chunk[b] % p.tile == 0 for b in range(2)) and h < p.tile
+    L, n = 500, p.n_splits[0]
+    c = next(c for c in range(p.chunk[0], 0, -1) if c % h and -(-L // c) == n)
+    p.chunk[0] = c
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    d = dev_struct(block_size=bs, max_blocks=640 // bs, num_blocks=100, pos_stride=hkv * d)
+    rc = lib.decode_attn_splitk_dev(ctypes.byref(a), ctypes.byref(p), ctypes.byref(d), fake,
+                                    fake, fake, fake, fake, p.workspace_bytes, None)
+    assert rc == N.DA_EINVAL and "multiples of %d" % h in lib.decode_attn_last_error().decode()
+
+
 def test_dev_call_needs_one_latent_pool_for_mla_and_an_extension(lib):
     a = mla_args(cap=4096)
     rc, p = plan(lib, a, [4096])

@@ -68,3 +68,47 @@ def test_random_shape(seed):
             worst = max(worst, err / bound)
     kernel = {N.DA_KERNEL_GQA_TMA: "simt", N.DA_KERNEL_GQA_TC: "tc"}[da.plan.kernel]
     assert worst <= 1.0, (dtype, d, hkv, gh, q_len, lens, out_dtype, force, kernel, worst)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_paged_shape(seed):
+    # the same random geometries over a paged pool (random block size and block
+    # order, NaN in every unused block), attending over device lengths up to the
+    # plan's: tiles run across block ends whatever the block size
+    from tests.test_gpu_paged import paged
+    dtype, d, hkv, gh, q_len, batch, lens, out_dtype, force = draw(5000 + seed)
+    g = np.random.default_rng(6000 + seed)
+    block_size = int(g.choice([16, 32, 48, 64, 80, 128, 256]))
+    now = [int(g.integers(q_len, L + 1)) for L in lens]
+    hq = hkv * gh
+    case = W.make_case("p", batch=batch, n_heads=hq, n_kv_heads=hkv, head_dim=d, seq_lens=lens,
+                       kv_dtype=dtype, seed=7000 + seed)
+    q4 = W.multi_token_q(batch, q_len, hq, d, seed=8000 + seed)
+    q = q4.cuda() if q_len > 1 else q4[:, 0].contiguous().cuda()
+    kp, vp, table = paged(case, block_size, seed=seed)
+    k, v, tab = kp.cuda(), vp.cuda(), table.cuda()
+    a = A.make_paged_args(q, k, v, case.scale, tab.shape[1], out_dtype=_TDT[out_dtype],
+                          force_splits=force)
+    dev_lens = torch.tensor(now, dtype=torch.int32, device="cuda")
+    dv = A.make_dev(seq_lens=dev_lens, block_table=tab, k_pool=k, v_pool=v)
+    p = A.decode_attn_plan(a, lens)
+    ws = A.new_workspace(p)
+    ws.fill_(0xFF)
+    out = torch.empty(tuple(q.shape[:-1]) + (d,), dtype=_TDT[out_dtype], device="cuda")
+    A.decode_attn_splitk_dev(a, p, dv, q, k, v, out, ws)
+    torch.cuda.synchronize()
+    A.decode_attn_device_status(ws)
+    got = out.double().cpu().numpy().reshape(batch, q_len, hq, d)
+    assert np.all(np.isfinite(got))
+    ref = oracle.attention_multi(q4, case.k, case.v, torch.tensor(now, dtype=torch.int32),
+                                 case.scale, threads=0)
+    worst = 0.0
+    for b, L in enumerate(now):
+        for t in range(q_len):
+            vm = float(case.v[b, :L - q_len + 1 + t].float().abs().max())
+            err = float(np.max(np.abs(got[b, t] - ref[b, t])))
+            bound = TOL[dtype] * vm + _ROUND[out_dtype] * float(np.max(np.abs(ref[b, t])))
+            worst = max(worst, err / bound)
+    kernel = {N.DA_KERNEL_GQA_TMA: "simt", N.DA_KERNEL_GQA_TC: "tc"}[p.kernel]
+    assert worst <= 1.0, (dtype, d, hkv, gh, q_len, lens, now, block_size, out_dtype, force,
+                          kernel, worst)
