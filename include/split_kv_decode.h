@@ -340,12 +340,13 @@ int decode_attn_splitk_noalloc(const da_args_t *args, const da_plan_t *plan, con
  *   block_size    positions per block: a positive multiple of 16. Tiles run
  *                 across block ends, so every block size streams whole tiles:
  *                 the SIMT GQA kernel copies a tile that lies in one block as one
- *                 TMA box and one that spans a block end as a few boxes per
- *                 block, the tensor-core GQA kernel every tile as boxes of
- *                 gcd(64, block_size) rows; box heights are multiples of
- *                 gcd(tile, block_size), so the plan's chunks must be too (the
- *                 planner's are multiples of the tile; DA_EINVAL otherwise). The
- *                 MLA kernel looks up every row.
+ *                 TMA box and one that spans a block end as boxes of
+ *                 gcd(tile, block_size) rows, the tensor-core GQA kernel every
+ *                 tile as boxes of gcd(64, block_size) rows; boxes start at
+ *                 multiples of their height, so the plan's chunks must be
+ *                 multiples of gcd(tile, block_size) (the planner's are
+ *                 multiples of the tile; DA_EINVAL otherwise). The MLA kernel
+ *                 looks up every row.
  *   num_blocks    blocks in each pool; table entries must be < num_blocks.
  *   k_block_stride, v_block_stride  elements between blocks (16-byte multiples,
  *                 at least block_size * pos_stride).

@@ -96,7 +96,8 @@ __device__ __forceinline__ bool tc_bar_or(bool pred)
 
 // The (item, tile) sequence of a CTA, the same for every role: items
 // blockIdx.x, blockIdx.x + gridDim.x, ...; an item's tiles are T positions,
-// cut at its end and (paged caches) at block ends; items without positions
+// the last one cut at the item's end (block ends of a paged cache do not cut
+// tiles: the producer copies a tile box by box); items without positions
 // (device lengths shorter than the plan's) have no tiles and are skipped.
 template <int T> struct Walk {
     int item, b, kvh, s, p0, p1, t0, t1, gt;
