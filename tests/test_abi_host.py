@@ -594,3 +594,85 @@ def test_plan_odd_groups_on_the_simt_kernel(lib, hq, hkv, d, dt):
     assert rc == 0, lib.decode_attn_last_error().decode()
     assert p.kernel == N.DA_KERNEL_GQA_TMA
     check_invariants(a, p, [8192], 152)
+
+
+# ---------------------------------------------------------------------------
+# a seeded sweep over every kernel's shapes
+# ---------------------------------------------------------------------------
+def _random_shape(rnd):
+    """(kind, args, lens, sms) for one random shape that the planner must accept."""
+    kind = rnd.choice(["simt", "tc", "mla"])
+    batch = rnd.choice([1, 1, 2, 3, 4, 7, 16, 32, 64, 128, 256])
+    if kind == "mla":
+        hq, q_len = rnd.choice([(96, 1), (64, 1), (32, 1), (48, 2), (32, 2), (32, 3), (16, 4)])
+        cap = rnd.choice([64, 4096, 131072, 262144])
+        a = mla_args(batch=batch, hq=hq, cap=cap)
+        hkv = 1
+    else:
+        hkv = rnd.choice([1, 2, 4, 8])
+        d = rnd.choice([128, 256])
+        if kind == "simt":
+            dt = rnd.choice([N.DA_F32, N.DA_F16, N.DA_BF16])
+            rows = rnd.randint(1, 8)
+        else:
+            dt = rnd.choice([N.DA_F16, N.DA_BF16])
+            rows = rnd.randint(8, 128)
+        # rows per item = heads per KV head x new tokens
+        q_len = rnd.choice([q for q in range(1, min(rows, 64) + 1) if rows % q == 0])
+        gh = rows // q_len
+        cap = rnd.choice([64, 4096, 131072, 262144])
+        a = args(batch=batch, hq=gh * hkv, hkv=hkv, d=d, dt=dt, cap=cap,
+                 layout=rnd.choice(["pos", "head"]))
+        if kind == "simt" and rows == 8 and dt != N.DA_F32:
+            a.flags = N.DA_FLAG_GQA_SIMT          # 8 rows on a 16-bit cache stay on SIMT
+    a.q_len = q_len
+    if rnd.random() < 0.2:
+        a.force_splits = rnd.randint(1, 400)
+    short = rnd.random() < 0.3
+    lens = [rnd.randint(q_len, min(cap, 300) if short else cap) for _ in range(batch)]
+    sms = rnd.choice([1, 2, 3, 7, 76, 132, 148, 151, 152])
+    return kind, hkv, a, lens, sms
+
+
+def test_plan_random_shapes_on_every_kernel(lib):
+    """600 seeded shapes across the three split kernels (batch 1-256, 1-8 KV
+    heads, 1-64 new tokens, both cache layouts, 1-152 SMs, forced splits now
+    and then). Every plan must cover each sequence with non-empty splits of
+    whole tiles, keep its totals consistent with its tables, launch whole
+    clusters within the SMs it was given, and size a workspace that holds
+    every partial and stays 256-byte aligned when ranks are stacked."""
+    import random
+    rnd = random.Random(2024)
+    want_kernel = {"simt": N.DA_KERNEL_GQA_TMA, "tc": N.DA_KERNEL_GQA_TC,
+                   "mla": N.DA_KERNEL_MLA_TC}
+    for case in range(600):
+        kind, hkv, a, lens, sms = _random_shape(rnd)
+        rc, p = plan(lib, a, lens, sms)
+        where = f"case {case}: {kind} batch {a.batch} hq {a.n_heads} hkv {hkv} q_len {a.q_len} " \
+                f"sms {sms} force {a.force_splits}"
+        assert rc == 0, f"{where}: {lib.decode_attn_last_error().decode()}"
+        assert p.kernel == want_kernel[kind], where
+        assert p.batch == a.batch and p.tile >= 1, where
+        if kind == "tc":
+            assert p.tile == 64, where
+        if kind == "mla":
+            assert p.tile == 16, where
+        base = 0
+        for b, L in enumerate(lens):
+            c = p.chunk[b]
+            assert p.seq_lens[b] == L and c >= p.tile and c % p.tile == 0, where
+            assert p.n_splits[b] == -(-L // c) and (p.n_splits[b] - 1) * c < L, where
+            if a.force_splits:
+                assert p.n_splits[b] <= a.force_splits, where
+            assert p.split_base[b] == base, where
+            base += p.n_splits[b]
+        assert p.total_splits == base and p.n_items == base * hkv, where
+        cluster = 2 if kind == "mla" else 1
+        assert p.grid % cluster == 0 and cluster <= p.grid <= p.n_items * cluster, where
+        per_sm = max(cluster, (sms * p.ctas_per_sm) // cluster * cluster)
+        assert p.grid <= per_sm, where
+        rows = a.n_heads * a.q_len
+        partials = base * rows * (a.v_dim + 2) * 4
+        assert lib.decode_attn_workspace_bytes(ctypes.byref(p)) == p.workspace_bytes, where
+        assert partials <= p.workspace_bytes <= partials + 1024, where
+        assert p.workspace_bytes % 256 == 0, where
