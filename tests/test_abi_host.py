@@ -72,6 +72,61 @@ int main(void) {
     assert got == want
 
 
+
+def test_a_plain_c_program_plans_through_the_library(lib):
+    """The boundary needs no Python: a C program built against the header and
+    linked to libsplitkv.so plans the 151552-position 16/4-head workload, reads
+    the workspace size, gets a refusal with a reason for 15 heads over 4 KV
+    heads, and its plan equals the one the binding gets for the same arguments."""
+    src = r"""
+#include <stdio.h>
+#include <string.h>
+#include "split_kv_decode.h"
+int main(void) {
+  da_args_t a;
+  static da_plan_t p;
+  int32_t lens[1] = {151552};
+  memset(&a, 0, sizeof a);
+  a.batch = 1; a.n_heads = 16; a.n_kv_heads = 4; a.head_dim = 256; a.v_dim = 256;
+  a.capacity = 151552;
+  a.k_pos_stride = a.v_pos_stride = 4 * 256;
+  a.k_head_stride = a.v_head_stride = 256;
+  a.k_batch_stride = a.v_batch_stride = (int64_t)151552 * 4 * 256;
+  a.kv_dtype = DA_F16; a.out_dtype = DA_F32; a.scale = 1.0f / 16;
+  if (decode_attn_plan(&a, lens, 152, &p) != DA_OK) {
+    printf("plan failed: %s\n", decode_attn_last_error());
+    return 1;
+  }
+  printf("%d %d %d %d %d %d %lld %lld\n", p.kernel, p.tile, p.grid, p.n_items, p.n_splits[0],
+         p.chunk[0], (long long)p.workspace_bytes, (long long)decode_attn_workspace_bytes(&p));
+  a.n_heads = 15;
+  int rc = decode_attn_plan(&a, lens, 152, &p);
+  printf("%d\n", rc);
+  printf("%s\n", decode_attn_last_error());
+  printf("%s\n", decode_attn_version());
+  return 0;
+}
+"""
+    libdir = os.path.dirname(B.LIB)
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "plan.c")
+        open(c, "w").write(src)
+        exe = os.path.join(d, "plan")
+        subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        c, "-o", exe, "-L", libdir, "-lsplitkv", "-Wl,-rpath," + libdir],
+                       check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    lines = out.splitlines()
+    got = [int(x) for x in lines[0].split()]
+    a = args(cap=151552)
+    rc, p = plan(lib, a, [151552])
+    assert rc == 0
+    assert got == [p.kernel, p.tile, p.grid, p.n_items, p.n_splits[0], p.chunk[0],
+                   p.workspace_bytes, p.workspace_bytes]
+    assert int(lines[1]) == N.DA_EINVAL and "multiple" in lines[2]
+    assert "sm_103a" in lines[3]
+
+
 def args(batch=1, hq=16, hkv=4, d=256, dv=None, cap=262144, dt=N.DA_F16, out=N.DA_F32,
          force=0, layout="pos"):
     a = N.DaArgs()
