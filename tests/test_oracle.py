@@ -226,6 +226,30 @@ def test_partials_are_the_segment_triples():
             assert np.max(np.abs(pO[h, seg] - np.exp(ss - m) @ vv)) <= 1e-13 * np.abs(vv).max() * 10
 
 
+
+@pytest.mark.parametrize("form", [oracle.MERGE_ML, oracle.MERGE_LSE])
+@pytest.mark.parametrize("groups", [[4, 4, 4], [1, 11], [5, 2, 5], [3, 3, 3, 3]])
+def test_merging_in_groups_equals_merging_at_once(form, groups):
+    # Context-parallel decode merges each rank's splits and then the ranks
+    # ("The Kernel Level": DCP is split-KV at another scale). A merged row is a
+    # partial again -- (m, l, O = out * l), or (LSE*, 1, out) for the LSE form --
+    # so any grouping of the 12 segments must give the one-level result.
+    c = small(4, 2, 16, [120], cap=120, seed=61, scale=1.0)
+    ref, pm, pl, pO = oracle.attention_split(c.q, c.k, c.v, c.seq_lens, c.scale, 12, block=8,
+                                             return_partials=True)
+    ref = ref.reshape(4, -1)
+    for row in range(4):
+        mg, lg, Og, i = [], [], [], 0
+        for n in groups:
+            m1, l1, out1 = oracle.merge(pm[row, i:i + n], pl[row, i:i + n], pO[row, i:i + n],
+                                        form=form)
+            mg.append(m1)
+            lg.append(l1)
+            Og.append(out1 * l1)
+            i += n
+        _, _, out = oracle.merge(mg, lg, np.stack(Og), form=form)
+        assert np.max(np.abs(out - ref[row])) <= 1e-12 * np.abs(ref[row]).max()
+
 # ---------------------------------------------------------------------------
 # negative controls: the planted mistakes must be caught
 # ---------------------------------------------------------------------------
