@@ -75,6 +75,10 @@ MUTANTS = [
      "wgt * O[(int64_t)i * dv + e]"),
     ("LSE merge: log of the weight sum dropped", C, "double lse_star = lse_max + log(z);",
      "double lse_star = lse_max;"),
+    ("merge: merged m not returned", C, "if (m_out) *m_out = M;", "if (m_out) *m_out = 0.0;"),
+    ("merge: merged l not returned", C, "if (l_out) *l_out = L;", "if (l_out) *l_out = 1.0;"),
+    ("LSE merge: merged LSE taken from the largest partial", C, "if (m_out) *m_out = lse_star;",
+     "if (m_out) *m_out = lse_max;"),
     # the online recurrence inside a segment
     ("recurrence: O not rescaled by alpha", C,
      "for (int e = 0; e < s->v_dim; ++e) O[e] *= alpha;",
