@@ -2,7 +2,6 @@
 (heads per KV head, head_dim, storage type, batch, lengths from 1 to a few
 thousand, new tokens per sequence, output type, forced split count) runs through
 whichever kernel the plan picks, and every row is compared with the oracle."""
-import dataclasses
 
 import numpy as np
 import pytest

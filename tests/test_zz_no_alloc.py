@@ -9,7 +9,6 @@ workspace. This file is collected last on purpose.
 """
 import math
 
-import numpy as np
 import pytest
 import torch
 
