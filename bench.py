@@ -19,7 +19,9 @@ CPU oracle on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -44,6 +46,7 @@ WORKLOADS = {
     "gqa16x4_f16_L151552_q4": ("gqa_16x4", 151552, 4),
 }
 DEFAULT = "gqa16x4_f16_L151552"
+METRIC = "decode-attention us/layer-step (and KV GB/s)"   # both arms report this metric
 # the split kernel each workload runs, and the arithmetic type it computes in
 KERNEL = {"mla96_f32_L131072": ("mla_split_kernel", "bf16"),
           "gqa16x4_f16_L151552_q4": ("gqa_tc_kernel", "f16")}
@@ -226,43 +229,63 @@ def cpu_baseline(case, budget_s=12.0):
                       "scaled by attended positions"}
 
 
-def run_reference(args):
-    """The reference arm: the CPU oracle, timed on host cores, rank 0 only."""
+def run_reference(args, budget_s=150.0):
+    """The reference arm: the CPU oracle, timed on host cores, rank 0 only.
+
+    Each step times a bounded sample of the workload, sized from --steps and
+    --warmup so that the whole run takes about budget_s seconds of host work:
+    whole (b, h) rows while one row fits a step's share, else one row per core
+    over a prefix of each sampled sequence's context. The oracle's time per row
+    is linear in the attended positions, so every step is scaled to the full
+    layer-step by attended positions."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from split_kv_decode_gb300 import workloads as W  # noqa: F401
     case, _, _, _ = make_inputs(args.workload, "cpu")
     import oracle
     threads = oracle.max_threads()
     pairs_all = [(b, h) for b in range(case.batch) for h in range(case.n_heads)]
-    # each step: a bounded sample of rows (about 2 s of host work), scaled to a full step
+    pos_all = sum(int(case.seq_lens[b]) for b, _ in pairs_all)
     t0 = time.perf_counter()
     oracle_rows(case, [pairs_all[0]], 1)
-    t_row = time.perf_counter() - t0
-    n = max(1, min(len(pairs_all), int(2.0 / max(t_row, 1e-6) * threads)))
+    t_row = max(time.perf_counter() - t0, 1e-6)               # one full row, one thread
+    per_step = min(2.0, max(0.02, budget_s / (args.steps + args.warmup)))
+    if t_row <= per_step:
+        n = max(1, min(len(pairs_all), int(per_step / t_row) * threads))
+        frac = 1.0
+    else:
+        n = min(len(pairs_all), threads)
+        frac = per_step / t_row
     stride = max(1, len(pairs_all) // n)
     pairs = pairs_all[::stride][:n]
-    pos_sample = sum(int(case.seq_lens[b]) for b, _ in pairs)
-    pos_all = sum(int(case.seq_lens[b]) for b, _ in pairs_all)
+    q_len = int(case.q.shape[1]) if case.q.dim() == 4 else 1
+    lens = case.seq_lens.clone()
+    if frac < 1.0:
+        for b in range(case.batch):
+            L = int(case.seq_lens[b])
+            lens[b] = min(L, max(q_len, 64, int(math.ceil(L * frac))))
+    sample = dataclasses.replace(case, seq_lens=lens)
+    pos_sample = sum(int(lens[b]) for b, _ in pairs)
     for _ in range(args.warmup):
-        oracle_rows(case, pairs[:1], threads)
+        oracle_rows(sample, pairs[:1], threads)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_rows(case, pairs, threads)
+        oracle_rows(sample, pairs, threads)
         times.append((time.perf_counter() - t0) * pos_all / pos_sample)
     us = statistics.mean(times) * 1e6
+    what = "full context" if frac >= 1.0 else \
+        f"the first {frac:.1%} of each sampled sequence's positions"
     line = {
-        "impl": "reference", "metric": "decode-attention us/layer-step", "value": round(us, 1),
+        "impl": "reference", "metric": METRIC, "value": round(us, 1),
         "unit": "us/layer-step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args.workload, case),
         "cpu_baseline": {"value": round(us, 1), "unit": "us/layer-step", "cores": threads,
                          "kind": "oracle",
-                         "sample": f"{len(pairs)} of {len(pairs_all)} (b,h) rows per step, "
-                                   "scaled by attended positions"},
+                         "sample": f"{len(pairs)} of {len(pairs_all)} (b,h) rows per step at "
+                                   f"{what}, scaled by attended positions"},
         "e2e": {"value": round(us, 1), "unit": "us/layer-step", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -382,7 +405,7 @@ def main():
     kernel, arith = KERNEL.get(args.workload, DEFAULT_KERNEL)
 
     line = {
-        "metric": "decode-attention us/layer-step (and KV GB/s)", "value": round(value, 2),
+        "metric": METRIC, "value": round(value, 2),
         "unit": "us/layer-step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(value / 1e3, 5), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": arith, "data": "synthetic",
