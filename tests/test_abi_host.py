@@ -731,3 +731,46 @@ def test_plan_random_shapes_on_every_kernel(lib):
         assert lib.decode_attn_workspace_bytes(ctypes.byref(p)) == p.workspace_bytes, where
         assert partials <= p.workspace_bytes <= partials + 1024, where
         assert p.workspace_bytes % 256 == 0, where
+
+
+def test_plans_and_error_messages_are_per_thread(lib):
+    """decode_attn_plan is pure host code and its failure message is
+    thread-local: eight threads planning at once (ctypes releases the GIL for
+    the call), half of them with a bad head count, each get the plan a lone
+    call gets and only their own message."""
+    import threading
+    lens = [151552, 4096, 20000, 77777]
+    want = {}
+    for i, L in enumerate(lens):
+        rc, p = plan(lib, args(cap=262144), [L])
+        assert rc == 0
+        want[i] = (p.n_splits[0], p.chunk[0], p.grid, p.workspace_bytes)
+    errors, results = [], {}
+
+    def worker(t):
+        try:
+            for it in range(200):
+                i = (t + it) % len(lens)
+                a = args(cap=262144)
+                if t % 2:
+                    a.n_heads = 15 + 2 * (t % 3)          # 15, 17 or 19 over 4 KV heads
+                    rc, _ = plan(lib, a, [lens[i]])
+                    msg = lib.decode_attn_last_error().decode()
+                    if rc != N.DA_EINVAL or f"n_heads {a.n_heads} " not in msg:
+                        errors.append((t, rc, msg))
+                else:
+                    rc, p = plan(lib, a, [lens[i]])
+                    got = (p.n_splits[0], p.chunk[0], p.grid, p.workspace_bytes)
+                    if rc != 0 or got != want[i]:
+                        errors.append((t, rc, got, want[i]))
+            results[t] = True
+        except Exception as e:                          # pragma: no cover
+            errors.append((t, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(8)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors[:5]
+    assert len(results) == 8
