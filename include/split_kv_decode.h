@@ -271,6 +271,12 @@ int decode_attn_splitk_proj(const da_args_t *args, const da_plan_t *plan, const 
  * scratch). The first call on a device, and a call that needs a larger
  * workspace than before, allocates it with cudaMalloc (which synchronises);
  * decode_attn_release() frees them.
+ * Every short-form call on a device shares that one workspace. The library
+ * holds a lock while it enqueues, so no call launches on a workspace that
+ * another thread is replacing. But calls whose kernels overlap on the GPU
+ * (several streams, or several threads) race on the workspace's contents:
+ * serialise them, or give each stream its own workspace through
+ * decode_attn_splitk_ex.
  */
 int decode_attn_splitk(const float *q, const float *k_cache, const float *v_cache,
                        const int32_t *seq_lens, int n_heads, int n_kv_heads, int head_dim,

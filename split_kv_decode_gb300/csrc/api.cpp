@@ -776,25 +776,24 @@ int decode_attn_splitk(const float *q, const float *k, const float *v, const int
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(DA_ECUDA, "workspace", "%s", cudaGetErrorString(e));
-    void *ws = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(g_ws_mu);
-        if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1, {nullptr, 0});
-        auto &slot = g_ws[dev];
-        if (slot.second < (size_t)plan.workspace_bytes) {
-            if (slot.first) cudaFree(slot.first);
-            slot = {nullptr, 0};
-            size_t want = (size_t)plan.workspace_bytes * 2;
-            e = cudaMalloc(&slot.first, want);
-            if (e != cudaSuccess)
-                return fail(DA_ECUDA, "workspace", "cudaMalloc of %zu bytes: %s", want,
-                            cudaGetErrorString(e));
-            slot.second = want;
-        }
-        ws = slot.first;
+    // The lock is held until the launches are enqueued, so another thread
+    // cannot free (to grow) or release this workspace between the lookup and
+    // the launches; cudaFree then waits for the kernels already enqueued.
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1, {nullptr, 0});
+    auto &slot = g_ws[dev];
+    if (slot.second < (size_t)plan.workspace_bytes) {
+        if (slot.first) cudaFree(slot.first);
+        slot = {nullptr, 0};
+        size_t want = (size_t)plan.workspace_bytes * 2;
+        e = cudaMalloc(&slot.first, want);
+        if (e != cudaSuccess)
+            return fail(DA_ECUDA, "workspace", "cudaMalloc of %zu bytes: %s", want,
+                        cudaGetErrorString(e));
+        slot.second = want;
     }
-    return decode_attn_splitk_ex(&a, &plan, q, k, v, out, ws, (size_t)plan.workspace_bytes,
-                                 stream);
+    return decode_attn_splitk_ex(&a, &plan, q, k, v, out, slot.first,
+                                 (size_t)plan.workspace_bytes, stream);
 }
 
 int decode_attn_device_status(void *ws, da_stream_t stream)
