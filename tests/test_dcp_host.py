@@ -1,10 +1,10 @@
-"""Host-side tests of the multi-rank paths, run as world-size-2 gloo process
-groups on CPU (127.0.0.1):
+"""Host-side tests of the multi-rank paths, run as world-size-2 and -3 gloo
+process groups on CPU (127.0.0.1):
 
 * context-parallel decode (DCP): each rank takes its slice of every sequence
   (split_kv_decode_gb300.dcp), forms the slice's partial (m, l, acc) -- here with
   the oracle, standing in for the split kernel, which needs a GPU -- the ranks
-  exchange them with dcp.gather, and the merge of both ranks' partials equals
+  exchange them with dcp.gather, and the merge of all ranks' partials equals
   attention over the whole context ("The Kernel Level: Attention and MoE", the
   split-KV/DCP section);
 * the bench's timing: the job's time is the slowest rank's (max over ranks).
@@ -89,11 +89,13 @@ def _dcp_rank(rank, world, port, out_dir):
         dist.destroy_process_group()
 
 
-def test_dcp_merge_over_two_gloo_ranks():
+@pytest.mark.parametrize("world", [2, 3])
+def test_dcp_merge_over_gloo_ranks(world):
+    # three ranks cut every sequence unevenly (301 = 100 + 100 + 101, 64 = 21 + 21 + 22)
     oracle.build()                                           # once, before the ranks start
     with tempfile.TemporaryDirectory() as d:
-        mp.spawn(_dcp_rank, args=(2, _free_port(), d), nprocs=2, join=True)
-        errs = [float(open(os.path.join(d, f"rank{r}.txt")).read()) for r in range(2)]
+        mp.spawn(_dcp_rank, args=(world, _free_port(), d), nprocs=world, join=True)
+        errs = [float(open(os.path.join(d, f"rank{r}.txt")).read()) for r in range(world)]
     assert max(errs) < 1e-12, errs
 
 
