@@ -39,6 +39,16 @@ def test_every_declared_symbol_is_exported(lib):
         assert n in N.SIGNATURES, f"binding lacks {n}"
 
 
+
+def test_every_exported_c_entry_point_is_declared(lib):
+    # the reverse direction: the library exports no decode_attn_* function that
+    # the header does not declare (nm lists the dynamic symbol table)
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = sorted({l.split()[-1] for l in out.splitlines()
+                       if l.split()[-1].startswith("decode_attn_")})
+    assert exported == declared_functions()
+
 def test_struct_layout_matches_the_c_compiler():
     src = r"""
 #include <stdio.h>
