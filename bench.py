@@ -10,11 +10,13 @@ geometry at its rung nearest 128k; 620.8 MB of K+V per step).
                   [--impl ours|reference] [--no-extra]
 
 Timing: W untimed warm-up steps (plus a short soak so the clocks settle);
-then K steps, each bracketed by CUDA events on the launching stream
-(start | split kernel | mid | combine | end); an L2 flush (a write of
-2 x L2 bytes) runs between steps outside the events; barrier + synchronize
-on both sides; max over ranks. `--impl reference` times the double-precision
-CPU oracle on a bounded sample of the same workload instead.
+then K steps, each bracketed by CUDA events on the launching stream around
+its launches (the step's host plan is made first, while the L2 flush -- a
+write of 2 x L2 bytes between steps, outside the events -- runs on the
+GPU); barrier + synchronize on both sides; max over ranks. The default run
+adds `configs`: the same measurement, over 100 steps, for every workload of
+the pages' configurations. `--impl reference` times the double-precision CPU
+oracle on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -169,14 +171,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def make_inputs(workload, device):
+def make_inputs(workload, device, draw_on_device=False):
     """The workload's seeded case on `device`. With several new tokens per
-    sequence, case.q is [B, q_len, Hq, Dk]."""
+    sequence, case.q is [B, q_len, Hq, Dk]. draw_on_device: draw the caches on
+    `device` (same recipe, other values; for timing only)."""
     import dataclasses
     from split_kv_decode_gb300 import workloads as W
     name, L = WORKLOADS[workload][:2]
     q_len = WORKLOADS[workload][2] if len(WORKLOADS[workload]) > 2 else 1
-    case = W.named(name, seq_len=L) if L else W.named(name)
+    where = str(device) if draw_on_device else "cpu"
+    case = W.named(name, seq_len=L, device=where) if L else W.named(name, device=where)
     if q_len > 1:
         case = dataclasses.replace(case, q=W.multi_token_q(case.batch, q_len, case.n_heads,
                                                            case.head_dim))
@@ -344,10 +348,15 @@ def main():
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
 
-    def step():
-        p = A.decode_attn_plan(a_split, lens)           # host plan (no sync)
+    def make_plan():
+        return A.decode_attn_plan(a_split, lens)        # host plan (no sync)
+
+    def split(p):
         A.decode_attn_splitk_ex(a_split, p, q, k, v, out, ws, stream)
         return p
+
+    def step():
+        return split(make_plan())
 
     def combine(p):
         A.decode_attn_combine(a_split, p, ws, out, stream)
@@ -372,9 +381,12 @@ def main():
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
+        # each step plans on the host while the flush runs on the GPU, so the
+        # events bracket the device work of the step, not host scheduling
+        p = make_plan()
         flush.fill_(float(i))
         ev[i][0].record(stream)
-        combine(step())
+        combine(split(p))
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
@@ -382,9 +394,10 @@ def main():
     # around the split launch only, L2 flushed before each
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
+        p = make_plan()
         flush.fill_(float(i))
         evs[i][0].record(stream)
-        p = step()
+        split(p)
         evs[i][1].record(stream)
         combine(p)
     torch.cuda.synchronize()
@@ -426,6 +439,7 @@ def main():
         "wall_s_timed_region": round(t_wall, 3),
     }
     if rank == 0 and not args.no_extra:
+        line["configs"] = measure_configs(dev, peak)
         line["e2e"] = measure_e2e(case, q, out_dt, dev, stream, args)
         line["hot_l2"] = measure_hot(case, q, k, v, out_dt, dev, args)
         line["copy_probe"] = read_probe(dev, stream, max(case.kv_bytes, 512 << 20))
@@ -445,6 +459,88 @@ def main():
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+# every workload the pages' configurations name, in the default run
+CONFIG_SWEEP = ("gqa8x2_f32_L4096", "gqa16x4_f16_L4096", "gqa16x4_f16_L20480",
+                "gqa16x4_f16_L61440", "gqa16x4_f16_L151552", "gqa16x4_f16_L262144",
+                "mla96_f32_L131072", "gqa24x4_f32_b4", "ragged32_bf16", "gqa16x4_f16_L151552_q4")
+
+
+def time_split_and_step(workload, dev, steps):
+    """Step (split + combine) and split-kernel times of one workload, each over
+    `steps` runs with the L2 flushed before every run (CUDA events on the
+    launching stream; the host plan is made before the flush). The caches are
+    drawn on the device (same recipe as the parity cases, other values)."""
+    import torch
+    from split_kv_decode_gb300 import _native as N
+    from split_kv_decode_gb300 import api as A
+    case, q, k, v = make_inputs(workload, dev, draw_on_device=True)
+    out_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[case.out_dtype]
+    stream = torch.cuda.current_stream(dev)
+    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
+                    flags=N.DA_FLAG_NO_COMBINE)
+    lens = case.seq_lens.tolist()
+    p0 = A.decode_attn_plan(a, lens)
+    ws = torch.empty(A.decode_attn_workspace_bytes(p0), dtype=torch.uint8, device=dev)
+    out = torch.empty(out_shape(case), dtype=out_dt, device=dev)
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4 + 1024,
+                        dtype=torch.float32, device=dev)
+    for _ in range(3):
+        p = A.decode_attn_plan(a, lens)
+        A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
+        A.decode_attn_combine(a, p, ws, out, stream)
+    torch.cuda.synchronize()
+    st, sp = [], []
+    for i in range(steps):
+        p = A.decode_attn_plan(a, lens)
+        flush.fill_(float(i))
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
+        A.decode_attn_combine(a, p, ws, out, stream)
+        e[1].record(stream)
+        st.append(e)
+    for i in range(steps):
+        p = A.decode_attn_plan(a, lens)
+        flush.fill_(float(i))
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
+        e[1].record(stream)
+        A.decode_attn_combine(a, p, ws, out, stream)
+        sp.append(e)
+    torch.cuda.synchronize()
+    A.decode_attn_device_status(ws, stream)
+    step_us = [x.elapsed_time(y) * 1e3 for x, y in st]
+    split_us = [x.elapsed_time(y) * 1e3 for x, y in sp]
+    kernel = {N.DA_KERNEL_GQA_TMA: "gqa_split_kernel", N.DA_KERNEL_GQA_TC: "gqa_tc_kernel",
+              N.DA_KERNEL_MLA_TC: "mla_split_kernel"}.get(p0.kernel, str(p0.kernel))
+    res = (case, kernel, step_us, split_us, p0)
+    del q, k, v, ws, out, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_configs(dev, peak, steps=100):
+    """Every configuration of the sweep: step and split-kernel times (mean and
+    median), KV GB/s per step, and the split kernel's fraction of the measured
+    HBM bandwidth."""
+    res = {}
+    for w in CONFIG_SWEEP:
+        case, kernel, step_us, split_us, p = time_split_and_step(w, dev, steps)
+        sm = statistics.mean(split_us)
+        res[w] = {
+            "kernel": kernel, "kv_bytes": case.kv_bytes, "steps": steps,
+            "step_us_mean": round(statistics.mean(step_us), 2),
+            "step_us_median": round(statistics.median(step_us), 2),
+            "split_us_mean": round(sm, 2),
+            "split_us_median": round(statistics.median(split_us), 2),
+            "kv_gbs": round(case.kv_bytes / (statistics.mean(step_us) * 1e-6) / 1e9, 1),
+            "split_frac_of_measured_hbm": round(case.kv_bytes / (sm * 1e-6) / 1e9 / peak, 4),
+            "splits": p.n_splits[0], "items": p.n_items, "grid": p.grid,
+        }
+    return res
 
 
 def _timed_steps(launch, flush, steps, stream):

@@ -73,6 +73,11 @@ typedef enum {
                                     slice that lies wholly before the new tokens,
                                     e.g. every rank but the last of a
                                     context-parallel step                          */
+#define DA_FLAG_MLA_SIMT 0x8     /* MLA shape: every sequence on the f32 CUDA-core
+                                    kernel (see DA_MLA_EXACT_BELOW)                  */
+#define DA_FLAG_MLA_TC 0x10      /* MLA shape: every sequence on the tensor-core
+                                    kernel, whose operands are bf16 (see
+                                    DA_MLA_EXACT_BELOW)                              */
 #define DA_FLAG_TEST_NO_TMA 0x100 /* test hook: the producer issues no copy, so every
                                      consumer wait runs out after timeout_us and the
                                      kernel reports DA_ETIMEOUT through device_status */
@@ -82,9 +87,28 @@ typedef enum {
                                      to the context): the call returns DA_ELAUNCH and
                                      the message names the "split" phase             */
 
+/*
+ * MLA sequences shorter than this many positions (by the plan's length) run on
+ * an f32 CUDA-core kernel; longer ones on the tensor-core kernel.
+ * The tensor-core kernel rounds q, the latent rows and the probabilities to
+ * bf16 and accumulates in f32. Over thousands of attended positions those
+ * rounding errors average out: on caches drawn like the MLA workload (N(0,
+ * 0.5) latents, N(0, 1) queries), max|err| stays below 1e-4 of max|V| from
+ * about 1000 positions up. With few positions a single value row's rounding
+ * (up to 2^-9 of it) reaches the output, so short sequences take the f32
+ * kernel, which keeps every operand in f32 (within 2e-4 of max|V| at any
+ * length; the work there is small). Attention peaked on a few positions of a
+ * long context shows the bf16 rounding the same way: callers who need the f32
+ * bound there set DA_FLAG_MLA_SIMT. DA_FLAG_MLA_TC sends everything to the
+ * tensor cores.
+ */
+#define DA_MLA_EXACT_BELOW 2048
+
 /* Kernels the planner can choose (da_plan_t.kernel). */
 #define DA_KERNEL_GQA_TMA 1 /* SIMT split kernel, TMA-staged K/V tiles (GQA, MQA) */
-#define DA_KERNEL_MLA_TC 2  /* tcgen05/TMEM split kernel for MLA (576/512 latent)  */
+#define DA_KERNEL_MLA_TC 2  /* MLA (576/512 latent): the tcgen05/TMEM split kernel,
+                               and the f32 CUDA-core one for sequences shorter
+                               than DA_MLA_EXACT_BELOW                          */
 #define DA_KERNEL_GQA_TC 3  /* tcgen05/TMEM split kernel for GQA/MQA work items of
                                8 to 128 query rows ((n_heads / n_kv_heads) * q_len),
                                f16 or bf16 caches, head_dim 128 or 256; q and the
@@ -312,9 +336,14 @@ int decode_attn_device_status(void *workspace, da_stream_t stream);
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents: calls that overlap on the GPU (other streams, other threads)
  *     race and corrupt each other's partials. Serialise them.
- *   - A timed-out in-kernel wait is reported by decode_attn_device_status on a
- *     workspace pointer only; this entry point's status word is not reachable
- *     from the host, so use decode_attn_splitk_ex where that matters.
+ *   - DA_FLAG_NO_COMBINE is refused (DA_EINVAL): the partials would stay in
+ *     the private array, where no later call could combine them.
+ *   - Treat the output of this entry point as unchecked for in-kernel
+ *     timeouts. A bounded wait that runs out sets a status word inside the
+ *     private array, which the host cannot read and the next call clears; the
+ *     output of such a call is wrong and nothing reports it. Callers that need
+ *     that check use decode_attn_splitk_ex with a workspace and
+ *     decode_attn_device_status.
  */
 int decode_attn_splitk_noalloc(const da_args_t *args, const da_plan_t *plan, const float *q,
                                const void *k_cache, const void *v_cache, void *out,

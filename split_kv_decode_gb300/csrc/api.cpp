@@ -108,7 +108,18 @@ int check_args(const da_args_t *a)
     if (a->force_splits < 0) return fail(DA_EINVAL, "args", "force_splits < 0");
     if (a->timeout_us < 0) return fail(DA_EINVAL, "args", "timeout_us < 0");
     if (a->q_len < 0 || a->q_len > 64) return fail(DA_EINVAL, "args", "q_len %d outside [0, 64]", a->q_len);
+    if ((a->flags & DA_FLAG_MLA_SIMT) && (a->flags & DA_FLAG_MLA_TC))
+        return fail(DA_EINVAL, "args", "DA_FLAG_MLA_SIMT and DA_FLAG_MLA_TC exclude each other");
     return DA_OK;
+}
+
+// MLA: does sequence b (planned at `len` positions) run on the f32 CUDA-core
+// kernel rather than the tensor-core one?
+bool mla_exact_seq(const da_args_t *a, int len)
+{
+    if (a->flags & DA_FLAG_MLA_SIMT) return true;
+    if (a->flags & DA_FLAG_MLA_TC) return false;
+    return len < DA_MLA_EXACT_BELOW;
 }
 
 struct KernelChoice {
@@ -333,8 +344,27 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
             p.block_stride = dev->k_block_stride;
         }
     }
-    cudaError_t e = launch_mla_split(split_grid(a, pl), st, p);
-    if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
+    // each sequence on one of the two kernels (by the plan's length); both
+    // write their partials into the same workspace for the one combine
+    bool any_exact = false, any_tc = false;
+    for (int b = 0; b < a->batch; ++b) {
+        const bool ex = mla_exact_seq(a, pl->seq_lens[b]);
+        p.seq_exact[b] = ex ? 1 : 0;
+        any_exact |= ex;
+        any_tc |= !ex;
+    }
+    if (any_tc) {
+        cudaError_t e = launch_mla_split(split_grid(a, pl), st, p);
+        if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
+    }
+    if (any_exact) {
+        p.reset_status = any_tc ? 0 : 1;
+        const int grid = (a->flags & DA_FLAG_TEST_BAD_LAUNCH)
+                             ? 0
+                             : pl->n_items * mla_exact_groups(rows_of(a));
+        cudaError_t e = launch_mla_exact(grid, st, p);
+        if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
+    }
     return DA_OK;
 }
 
@@ -531,7 +561,14 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
             return fail(DA_ECUDA, "plan", "SM count query failed: %s", cudaGetErrorString(e));
     }
     PlanOut po;
-    const int slots = std::max(1, num_sms * kc.ctas_per_sm / kc.cluster);
+    int slots = std::max(1, num_sms * kc.ctas_per_sm / kc.cluster);
+    if (kc.kernel == DA_KERNEL_MLA_TC) {
+        // every sequence on the f32 kernel: its CTAs serve (item, group of 32
+        // rows), one per SM, so the items fill the SMs divided by the groups
+        bool all_exact = true;
+        for (int b = 0; b < a->batch; ++b) all_exact &= mla_exact_seq(a, lens[b]);
+        if (all_exact) slots = std::max(1, num_sms / mla_exact_groups(rows_of(a)));
+    }
     const int prc = plan_splits(lens, a->batch, a->n_kv_heads, kc.tile, slots, a->force_splits,
                                 1 << 22, &po);
     if (prc == 1) return fail(DA_EINVAL, "plan", "invalid lengths");

@@ -92,6 +92,11 @@ struct MlaParams {
     int32_t max_blocks;
     int32_t block_size;
     int64_t block_stride;
+    // Which kernel serves each sequence: the tensor-core kernel skips the
+    // sequences marked here (writing nothing for them) and the exact f32 kernel
+    // serves only those.
+    uint8_t seq_exact[DA_MAX_BATCH];
+    int32_t reset_status;    // the exact kernel runs alone in this call: it clears the status word
     ItemTable items;         // n_kv_heads = 1
 };
 
@@ -100,6 +105,10 @@ struct MlaParams {
 bool mla_supported_heads(int n_heads);
 int mla_smem_bytes(int n_heads);
 cudaError_t launch_mla_split(int grid, cudaStream_t stream, const MlaParams &p);
+// MLA split kernel in f32 on the CUDA cores: one CTA per (work item, group of
+// 32 rows); grid = n_items * mla_exact_groups(rows).
+int mla_exact_groups(int rows);
+cudaError_t launch_mla_exact(int grid, cudaStream_t stream, const MlaParams &p);
 
 struct CombineParams {
     const float2 *ml;

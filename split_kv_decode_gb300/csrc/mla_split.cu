@@ -131,6 +131,7 @@ __device__ __forceinline__ bool bar_or(int id, int threads, bool pred)
 
 struct Item {
     int b, s, p0, p1, ntiles, L; // L: the length the item's sequence attends over
+    bool skip;                   // the exact f32 kernel serves this sequence
 };
 
 // item -> (sequence, split, positions [p0, p1), tiles). With lengths read on
@@ -152,7 +153,8 @@ __device__ __forceinline__ Item get_item(const MlaParams &p, int item)
     if (p.dev_lens) L = max(p.q_len, min(__ldg(p.dev_lens + lo), L));
     x.L = L;
     x.p1 = min(L, x.p0 + it.chunk[lo]);
-    x.ntiles = x.p1 > x.p0 ? (x.p1 - x.p0 + kTile - 1) / kTile : 0;
+    x.skip = p.seq_exact[lo] != 0;
+    x.ntiles = (x.p1 > x.p0 && !x.skip) ? (x.p1 - x.p0 + kTile - 1) / kTile : 0;
     return x;
 }
 
@@ -514,6 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int item = cluster; !ab && item < it.n_items; item += nclusters) {
             const Item x = get_item(p, item);
             if (x.ntiles == 0) { // an empty item: a neutral partial, no MMA took part
+                if (x.skip) continue; // the exact kernel writes this item's partials
                 const size_t row0 = ((size_t)it.split_base[x.b] + x.s) * p.n_heads + hbase;
                 if (owner) p.ml[row0 + h] = make_float2(kNeutralM, 0.f);
                 continue;

@@ -58,7 +58,13 @@ extern "C" int decode_attn_splitk_noalloc(const da_args_t *args, const da_plan_t
                                           const float *q, const void *k_cache,
                                           const void *v_cache, void *out, da_stream_t stream)
 {
-    if (!plan) return skv::set_error(DA_EINVAL, "args", "plan is NULL");
+    if (!args || !plan) return skv::set_error(DA_EINVAL, "args", "args or plan is NULL");
+    // the partials stay in the library's private array, so a split-only call
+    // would hand the caller nothing: refuse it instead of returning DA_OK
+    if (args->flags & DA_FLAG_NO_COMBINE)
+        return skv::set_error(DA_EINVAL, "noalloc",
+                              "DA_FLAG_NO_COMBINE is refused here: the partials live in the "
+                              "library's private array and could not be combined later");
     if (plan->workspace_bytes < 0 || (size_t)plan->workspace_bytes > kNoallocScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,

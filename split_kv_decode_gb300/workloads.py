@@ -68,7 +68,7 @@ class Case:
 
 
 def _draw(gen: torch.Generator, shape, std: float, dtype: str) -> torch.Tensor:
-    x = torch.randn(shape, generator=gen, dtype=torch.float32)
+    x = torch.randn(shape, generator=gen, dtype=torch.float32, device=gen.device)
     if std != 1.0:
         x.mul_(std)
     return x.to(_TORCH[dtype])
@@ -78,22 +78,25 @@ def make_case(name: str, *, batch: int, n_heads: int, n_kv_heads: int, head_dim:
               seq_lens: Sequence[int], kv_dtype: str = F32, out_dtype: str = F32,
               v_dim: Optional[int] = None, scale: Optional[float] = None, seed: int = 1234,
               std: float = 1.0, shared_kv: bool = False, capacity: Optional[int] = None,
-              q_zero: bool = False, poison_tail: bool = True) -> Case:
+              q_zero: bool = False, poison_tail: bool = True, device: str = "cpu") -> Case:
     """Draw one seeded case. ``shared_kv`` builds an MLA-style cache where the
-    values are the first ``v_dim`` columns of each key row."""
+    values are the first ``v_dim`` columns of each key row. With a CUDA
+    ``device`` the same recipe is drawn there from a generator of that device
+    (other values of the same distributions, for timing large workloads
+    without a host round trip; parity checks use CPU draws)."""
     lens = torch.tensor(list(seq_lens), dtype=torch.int32)
     assert lens.numel() == batch and int(lens.min()) >= 1
     cap = int(capacity) if capacity is not None else int(lens.max())
     assert cap >= int(lens.max())
     dv = head_dim if v_dim is None else int(v_dim)
     sc = 1.0 / math.sqrt(head_dim) if scale is None else float(scale)
-    g = torch.Generator().manual_seed(int(seed))
-    q = torch.randn((batch, n_heads, head_dim), generator=g, dtype=torch.float32)
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    q = torch.randn((batch, n_heads, head_dim), generator=g, dtype=torch.float32, device=device)
     if q_zero:
         q.zero_()
     tdt = _TORCH[kv_dtype]
-    k = torch.empty((batch, cap, n_kv_heads, head_dim), dtype=tdt)
-    v = k if shared_kv else torch.empty((batch, cap, n_kv_heads, dv), dtype=tdt)
+    k = torch.empty((batch, cap, n_kv_heads, head_dim), dtype=tdt, device=device)
+    v = k if shared_kv else torch.empty((batch, cap, n_kv_heads, dv), dtype=tdt, device=device)
     for b in range(batch):
         L = int(lens[b])
         k[b, :L] = _draw(g, (L, n_kv_heads, head_dim), std, kv_dtype)
@@ -128,36 +131,40 @@ def ragged_lens(seed: int, batch: int = 32, lo: int = 1024, hi: int = 131072):
 
 
 def named(name: str, *, seed: Optional[int] = None, seq_len: Optional[int] = None,
-          scale_lens: float = 1.0) -> Case:
+          scale_lens: float = 1.0, device: str = "cpu") -> Case:
     """The named workloads. ``seq_len`` overrides the context of a batch-1 case;
-    ``scale_lens`` shrinks every length (for quick, oracle-sized variants)."""
+    ``scale_lens`` shrinks every length (for quick, oracle-sized variants);
+    ``device`` draws on that device (see make_case)."""
     def L(x):
         return max(1, int(round(x * scale_lens)))
 
+    def mk(*a, **kw):
+        return make_case(*a, device=device, **kw)
+
     if name == "gqa_8x2":
         s = 1234 if seed is None else seed
-        return make_case(name, batch=1, n_heads=8, n_kv_heads=2, head_dim=256,
-                         seq_lens=[L(seq_len or 4096)], kv_dtype=F32, scale=1.0 / 16, seed=s)
+        return mk(name, batch=1, n_heads=8, n_kv_heads=2, head_dim=256,
+                  seq_lens=[L(seq_len or 4096)], kv_dtype=F32, scale=1.0 / 16, seed=s)
     if name == "gqa_16x4":
         s = 1235 if seed is None else seed
-        return make_case(name, batch=1, n_heads=16, n_kv_heads=4, head_dim=256,
-                         seq_lens=[L(seq_len or 151552)], kv_dtype=F16, scale=1.0 / 16, seed=s)
+        return mk(name, batch=1, n_heads=16, n_kv_heads=4, head_dim=256,
+                  seq_lens=[L(seq_len or 151552)], kv_dtype=F16, scale=1.0 / 16, seed=s)
     if name == "mla_96":
         s = 1236 if seed is None else seed
-        return make_case(name, batch=1, n_heads=96, n_kv_heads=1, head_dim=576, v_dim=512,
-                         seq_lens=[L(seq_len or 131072)], kv_dtype=F32,
-                         scale=1.0 / math.sqrt(576.0), seed=s, std=0.5, shared_kv=True)
+        return mk(name, batch=1, n_heads=96, n_kv_heads=1, head_dim=576, v_dim=512,
+                  seq_lens=[L(seq_len or 131072)], kv_dtype=F32,
+                  scale=1.0 / math.sqrt(576.0), seed=s, std=0.5, shared_kv=True)
     if name == "gqa_24x4":
         s = 1237 if seed is None else seed
-        return make_case(name, batch=4, n_heads=24, n_kv_heads=4, head_dim=256,
-                         seq_lens=[L(x) for x in GQA24X4_LENS], kv_dtype=F32,
-                         scale=1.0 / 16, seed=s)
+        return mk(name, batch=4, n_heads=24, n_kv_heads=4, head_dim=256,
+                  seq_lens=[L(x) for x in GQA24X4_LENS], kv_dtype=F32,
+                  scale=1.0 / 16, seed=s)
     if name == "ragged_32":
         s = 1238 if seed is None else seed
         lens = [L(x) for x in ragged_lens(s)]
-        return make_case(name, batch=32, n_heads=32, n_kv_heads=8, head_dim=128,
-                         seq_lens=lens, kv_dtype=BF16, out_dtype=BF16,
-                         scale=1.0 / math.sqrt(128.0), seed=s)
+        return mk(name, batch=32, n_heads=32, n_kv_heads=8, head_dim=128,
+                  seq_lens=lens, kv_dtype=BF16, out_dtype=BF16,
+                  scale=1.0 / math.sqrt(128.0), seed=s)
     raise KeyError(name)
 
 

@@ -319,6 +319,23 @@ def test_run_validates_before_launch(lib):
     assert rc == N.DA_EINVAL and "plan" in lib.decode_attn_last_error().decode()
 
 
+def test_noalloc_refuses_a_split_only_call(lib):
+    # with DA_FLAG_NO_COMBINE the partials would stay in the library's private
+    # array, out of the caller's reach: the call is refused before any launch
+    a = args(cap=4096)
+    rc, p = plan(lib, a, [4096])
+    assert rc == 0
+    a.flags |= N.DA_FLAG_NO_COMBINE
+    fake = ctypes.c_void_p(1 << 20)          # never dereferenced: validation fails first
+    rc = lib.decode_attn_splitk_noalloc(ctypes.byref(a), ctypes.byref(p), fake, fake, fake,
+                                        fake, None)
+    assert rc == N.DA_EINVAL
+    msg = lib.decode_attn_last_error().decode()
+    assert "noalloc" in msg and "DA_FLAG_NO_COMBINE" in msg
+    assert lib.decode_attn_splitk_noalloc(None, ctypes.byref(p), fake, fake, fake, fake,
+                                          None) == N.DA_EINVAL
+
+
 def test_version_and_null_handling(lib):
     assert b"sm_103a" in lib.decode_attn_version()
     assert lib.decode_attn_plan(None, None, 152, None) == N.DA_EINVAL

@@ -128,7 +128,8 @@ def test_splitting_is_not_less_accurate_at_20000():
     _, rel_split = errors(case, g_split, ref)
     _, rel_one = errors(case, g_one, ref)
     print(f"relL2 split {rel_split:.3e} (S={da.plan.n_splits[0]}) vs unsplit {rel_one:.3e}")
-    assert rel_split <= 1.5 * rel_one + 1e-8
+    # measured on GB300: 2.3e-7 with 38 splits against 7.8e-7 unsplit
+    assert rel_split <= rel_one
 
 
 def test_f16_read_matches_the_same_values_widened_to_f32():
