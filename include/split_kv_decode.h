@@ -88,8 +88,10 @@ typedef enum {
                                      the message names the "split" phase             */
 
 /*
- * MLA sequences shorter than this many positions (by the plan's length) run on
- * an f32 CUDA-core kernel; longer ones on the tensor-core kernel.
+ * MLA sequences shorter than this many positions run on an f32 CUDA-core
+ * kernel, longer ones on the tensor-core kernel. The choice is made on the
+ * device from the current length (the plan's, or the one decode_attn_splitk_dev
+ * reads), so a captured launch follows a context that grows past it.
  * The tensor-core kernel rounds q, the latent rows and the probabilities to
  * bf16 and accumulates in f32. Over thousands of attended positions those
  * rounding errors average out: on caches drawn like the MLA workload (N(0,

@@ -20,6 +20,9 @@ DA_MAX_BATCH = 256
 DA_FLAG_NO_COMBINE = 0x1
 DA_FLAG_GQA_SIMT = 0x2
 DA_FLAG_NO_CAUSAL = 0x4
+DA_FLAG_MLA_SIMT = 0x8
+DA_FLAG_MLA_TC = 0x10
+DA_MLA_EXACT_BELOW = 2048
 DA_FLAG_TEST_NO_TMA = 0x100
 DA_FLAG_TEST_BAD_LAUNCH = 0x200
 DA_KERNEL_GQA_TMA, DA_KERNEL_MLA_TC, DA_KERNEL_GQA_TC = 1, 2, 3

@@ -113,13 +113,13 @@ int check_args(const da_args_t *a)
     return DA_OK;
 }
 
-// MLA: does sequence b (planned at `len` positions) run on the f32 CUDA-core
-// kernel rather than the tensor-core one?
-bool mla_exact_seq(const da_args_t *a, int len)
+// MLA: sequences shorter than this (current length) run on the f32
+// CUDA-core kernel, the others on the tensor-core kernel
+int mla_exact_below(const da_args_t *a)
 {
-    if (a->flags & DA_FLAG_MLA_SIMT) return true;
-    if (a->flags & DA_FLAG_MLA_TC) return false;
-    return len < DA_MLA_EXACT_BELOW;
+    if (a->flags & DA_FLAG_MLA_SIMT) return INT32_MAX;
+    if (a->flags & DA_FLAG_MLA_TC) return 0;
+    return DA_MLA_EXACT_BELOW;
 }
 
 struct KernelChoice {
@@ -344,14 +344,16 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
             p.block_stride = dev->k_block_stride;
         }
     }
-    // each sequence on one of the two kernels (by the plan's length); both
-    // write their partials into the same workspace for the one combine
+    // each sequence on one of the two kernels, chosen on the device from its
+    // current length; both write their partials into the same workspace for
+    // the one combine. A kernel is launched if any sequence may need it:
+    // lengths read on the device can be anything from q_len to the plan's.
+    p.exact_below = mla_exact_below(a);
     bool any_exact = false, any_tc = false;
     for (int b = 0; b < a->batch; ++b) {
-        const bool ex = mla_exact_seq(a, pl->seq_lens[b]);
-        p.seq_exact[b] = ex ? 1 : 0;
-        any_exact |= ex;
-        any_tc |= !ex;
+        const int L = pl->seq_lens[b];
+        any_tc |= L >= p.exact_below;
+        any_exact |= (p.dev_lens ? q_len_of(a) : L) < p.exact_below;
     }
     if (any_tc) {
         cudaError_t e = launch_mla_split(split_grid(a, pl), st, p);
@@ -566,7 +568,7 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
         // every sequence on the f32 kernel: its CTAs serve (item, group of 32
         // rows), one per SM, so the items fill the SMs divided by the groups
         bool all_exact = true;
-        for (int b = 0; b < a->batch; ++b) all_exact &= mla_exact_seq(a, lens[b]);
+        for (int b = 0; b < a->batch; ++b) all_exact &= lens[b] < mla_exact_below(a);
         if (all_exact) slots = std::max(1, num_sms / mla_exact_groups(rows_of(a)));
     }
     const int prc = plan_splits(lens, a->batch, a->n_kv_heads, kc.tile, slots, a->force_splits,
@@ -578,7 +580,11 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
     plan->num_sms = num_sms;
     plan->ctas_per_sm = kc.ctas_per_sm;
     plan->tile = kc.tile;
-    plan->grid = po.grid * kc.cluster;
+    // the split kernel's CTAs (for MLA, the tensor-core kernel's clusters, one
+    // CTA per SM, even when every sequence runs on the f32 kernel)
+    plan->grid = (int32_t)std::min<int64_t>(
+                     po.n_items, std::max(1, num_sms * kc.ctas_per_sm / kc.cluster)) *
+                 kc.cluster;
     plan->n_items = po.n_items;
     plan->batch = a->batch;
     int64_t base = 0;

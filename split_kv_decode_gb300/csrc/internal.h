@@ -92,10 +92,11 @@ struct MlaParams {
     int32_t max_blocks;
     int32_t block_size;
     int64_t block_stride;
-    // Which kernel serves each sequence: the tensor-core kernel skips the
-    // sequences marked here (writing nothing for them) and the exact f32 kernel
-    // serves only those.
-    uint8_t seq_exact[DA_MAX_BATCH];
+    // Which kernel serves a sequence, decided on the device from its current
+    // length L (the plan's, or the one read from dev_lens): the f32 kernel when
+    // L < exact_below, else the tensor-core kernel. Each kernel skips the other's
+    // sequences entirely (it writes nothing for them).
+    int32_t exact_below;
     int32_t reset_status;    // the exact kernel runs alone in this call: it clears the status word
     ItemTable items;         // n_kv_heads = 1
 };

@@ -8,9 +8,11 @@
 // The tensor-core kernel rounds all three to bf16, and with few attended
 // positions a single value row's rounding (up to 2^-9 of it) shows in the
 // output directly; here the scores and the weighted sum carry f32 rounding
-// only. The library sends sequences shorter than DA_MLA_EXACT_BELOW positions
-// here (where the work is small enough for the CUDA cores) and any sequence
-// when the caller asks for it.
+// only. The library sends sequences whose current length is below
+// DA_MLA_EXACT_BELOW positions here (where the work is small enough for the
+// CUDA cores), and any sequence when the caller asks for it; the choice is
+// made on the device, from the same length both kernels read, so a captured
+// launch follows a context that grows past the threshold.
 //
 // Work split: one CTA per (work item, group of 32 query rows); a work item is
 // a contiguous slice of one sequence's context ("Attention at 128k" §2). The
@@ -85,11 +87,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_exact_kernel(const __grid_con
         else hi = mid - 1;
     }
     const int b = lo;
-    if (!p.seq_exact[b]) return; // the tensor-core kernel serves this sequence
-    const int s = item - it.split_base[b];
-    const int p0 = s * it.chunk[b];
     int L = it.seq_lens[b];
     if (p.dev_lens) L = max(p.q_len, min(__ldg(p.dev_lens + b), L));
+    if (L >= p.exact_below) return; // the tensor-core kernel serves this sequence
+    const int s = item - it.split_base[b];
+    const int p0 = s * it.chunk[b];
     const int p1 = min(L, p0 + it.chunk[b]);
     const int row = group * kRows + lane;
     const bool row_ok = row < p.n_heads;
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_exact_kernel(const __grid_con
             l += pj[j];
         }
         // O[row][this warp's 64 columns] += sum_j p_j V[j][.]
-#pragma unroll 4
+#pragma unroll
         for (int j = 0; j < kTP; ++j) {
             const float4 *vr = reinterpret_cast<const float4 *>(K + j * kDk + warp * kESlice);
 #pragma unroll

@@ -153,7 +153,7 @@ __device__ __forceinline__ Item get_item(const MlaParams &p, int item)
     if (p.dev_lens) L = max(p.q_len, min(__ldg(p.dev_lens + lo), L));
     x.L = L;
     x.p1 = min(L, x.p0 + it.chunk[lo]);
-    x.skip = p.seq_exact[lo] != 0;
+    x.skip = L < p.exact_below;
     x.ntiles = (x.p1 > x.p0 && !x.skip) ? (x.p1 - x.p0 + kTile - 1) / kTile : 0;
     return x;
 }

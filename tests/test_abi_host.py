@@ -801,3 +801,36 @@ def test_plans_and_error_messages_are_per_thread(lib):
         th.join()
     assert not errors, errors[:5]
     assert len(results) == 8
+
+
+def test_header_constants_match_the_binding():
+    # every #define of the header that the binding mirrors has the same value
+    text = open(HEADER).read()
+    defs = dict(re.findall(r"^#define\s+(DA_\w+)\s+(0x[0-9a-fA-F]+|\d+)", text, flags=re.M))
+    mirrored = [k for k in defs if hasattr(N, k)]
+    assert len(mirrored) >= 10
+    for k in mirrored:
+        assert getattr(N, k) == int(defs[k], 0), k
+
+
+def test_mla_kernel_flags_exclude_each_other(lib):
+    a = mla_args(cap=4096)
+    a.flags = N.DA_FLAG_MLA_SIMT | N.DA_FLAG_MLA_TC
+    rc, _ = plan(lib, a, [1000])
+    assert rc == N.DA_EINVAL and "exclude" in lib.decode_attn_last_error().decode()
+
+
+@pytest.mark.parametrize("hq", [32, 64, 96])
+def test_mla_short_sequences_plan_for_the_f32_kernel(lib, hq):
+    # every sequence below DA_MLA_EXACT_BELOW: the f32 kernel runs one CTA per
+    # (item, group of 32 rows), so the items fill the SMs divided by the groups
+    a = mla_args(hq=hq, cap=4096)
+    groups = hq // 32
+    for L in (1, 100, 1000, N.DA_MLA_EXACT_BELOW - 1):
+        rc, p = plan(lib, a, [L], 152)
+        assert rc == 0
+        check_mla_invariants(a, p, [L], 152)
+        assert p.n_items <= max(1, 152 // groups) or p.n_splits[0] * 16 >= L
+    # at the threshold the tensor-core kernel's geometry: one item per SM pair
+    rc, p = plan(lib, a, [4096], 152)
+    assert rc == 0 and p.n_items <= 76 * 4

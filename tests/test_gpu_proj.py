@@ -24,7 +24,7 @@ from tests.gpu_util import TOL, to_device, vmax_per_batch
 pytestmark = pytest.mark.gpu
 
 _TDT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
-MLA_BAR = {"long": 2e-4, "short": 5e-3}
+MLA_BAR = {"long": 2e-4, "short": 2e-4}   # f32 latent cache: the f32 bar at every length
 
 
 def proj_weights(heads, out_dim, v_dim, seed, dtype=torch.float32):
