@@ -339,30 +339,32 @@ def main():
     out_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[case.out_dtype]
     stream = torch.cuda.current_stream(dev)
 
+    # a step: one call, which runs the split kernel and the combine; for
+    # comparison, the split kernel alone (DA_FLAG_NO_COMBINE) and the one-launch
+    # form (DA_FLAG_ONE_LAUNCH)
+    a_step = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
     a_split = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
                           flags=N.DA_FLAG_NO_COMBINE)
-    plan = A.decode_attn_plan(a_split, case.seq_lens.tolist())
+    plan = A.decode_attn_plan(a_step, case.seq_lens.tolist())
     ws = torch.empty(A.decode_attn_workspace_bytes(plan), dtype=torch.uint8, device=dev)
     out = torch.empty(out_shape(case), dtype=out_dt, device=dev)
     lens = case.seq_lens.tolist()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    launches = count_launches(a_step, plan)
 
     def make_plan():
-        return A.decode_attn_plan(a_split, lens)        # host plan (no sync)
+        return A.decode_attn_plan(a_step, lens)         # host plan (no sync)
+
+    def run_step(p):
+        A.decode_attn_splitk_ex(a_step, p, q, k, v, out, ws, stream)
 
     def split(p):
         A.decode_attn_splitk_ex(a_split, p, q, k, v, out, ws, stream)
         return p
 
-    def step():
-        return split(make_plan())
-
-    def combine(p):
-        A.decode_attn_combine(a_split, p, ws, out, stream)
-
     for _ in range(args.warmup):
-        combine(step())
+        run_step(make_plan())
     torch.cuda.synchronize()
     # clocks are sampled from here on: a short untimed soak brings them under
     # load, then the timed steps run; every sample is taken with the GPU busy
@@ -371,7 +373,7 @@ def main():
     t_end = time.time() + (0.0 if args.no_soak else 0.6)
     while time.time() < t_end:
         for _ in range(20):
-            combine(step())
+            run_step(make_plan())
         torch.cuda.synchronize()
     # the timed steps: events only around the whole step, so the combine's
     # programmatic launch overlaps the split kernel's tail as it does in use
@@ -386,12 +388,12 @@ def main():
         p = make_plan()
         flush.fill_(float(i))
         ev[i][0].record(stream)
-        combine(split(p))
+        run_step(p)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
-    # the split kernel alone (for its roofline): the same launches, events
-    # around the split launch only, L2 flushed before each
+    # the split kernel alone, without the merge (DA_FLAG_NO_COMBINE), for
+    # comparison; L2 flushed before each
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
         p = make_plan()
@@ -399,7 +401,6 @@ def main():
         evs[i][0].record(stream)
         split(p)
         evs[i][1].record(stream)
-        combine(p)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     clocks["window"] = "untimed soak (0.6 s) + timed steps + split-only steps"
@@ -408,12 +409,16 @@ def main():
     A.decode_attn_device_status(ws, stream)
 
     step_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(args.steps)]
+    one_us = time_one_launch(case, q, k, v, out_dt, dev, flush, args)
     split_us = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in range(args.steps)]
     total_us = max_over_ranks(sum(step_us), dev)
     value = total_us / (args.steps * world)                # µs per layer-step, whole job
     split_mean = statistics.mean(split_us)
     peak, peak_src = load_peaks()
-    achieved = case.kv_bytes / (split_mean * 1e-6) / 1e9
+    # the dominant kernel: the split kernel (with one launch per step, the step
+    # itself)
+    kernel_us = statistics.mean(step_us) if launches == 1 else split_mean
+    achieved = case.kv_bytes / (kernel_us * 1e-6) / 1e9
     kv_gbs_step = case.kv_bytes / (statistics.mean(step_us) * 1e-6) / 1e9
     kernel, arith = KERNEL.get(args.workload, DEFAULT_KERNEL)
 
@@ -426,16 +431,21 @@ def main():
         "kv_gbs": round(kv_gbs_step, 1),
         "hbm_frac_of_8tbs": round(kv_gbs_step / 8000.0, 4),
         "step_us_median": round(statistics.median(step_us), 2),
-        "split_us_median": round(statistics.median(split_us), 2),
+        "launches_per_step": launches,
+        "one_launch_step_us_median": one_us,
+        "split_only_us_median": round(statistics.median(split_us), 2),
         "plan": {"grid": plan.grid, "items": plan.n_items, "tile": plan.tile,
                  "chunk": plan.chunk[0], "n_splits": plan.n_splits[0]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(kernel, args.workload),
                      "kernel": kernel, "peak_source": peak_src,
+                     "kernel_us_mean": round(kernel_us, 2),
+                     "what": ("split kernel merging its own partials (the whole step, one launch)"
+                              if launches == 1 else "split kernel (a combine launch follows)"),
                      "bytes_per_launch": case.kv_bytes},
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches * args.steps,
         "wall_s_timed_region": round(t_wall, 3),
     }
     if rank == 0 and not args.no_extra:
@@ -461,6 +471,48 @@ def main():
     return 0
 
 
+def count_launches(a, p):
+    """Kernel launches of one decode_attn_splitk_ex call with args `a` and plan
+    `p`: the split kernel(s) -- for the MLA shape the tensor-core kernel and/or
+    the f32 kernel, by the lengths -- and the combine, unless the split kernel
+    merges its own partials (DA_FLAG_ONE_LAUNCH). Mirrors the library's rules
+    (documented in its header); the counter memset of the one-launch form is not
+    a kernel of ours and is not counted."""
+    from split_kv_decode_gb300 import _native as N
+    if p.kernel != N.DA_KERNEL_MLA_TC:
+        split, exact = 1, False
+    else:
+        below = (1 << 31) if a.flags & N.DA_FLAG_MLA_SIMT else (
+            0 if a.flags & N.DA_FLAG_MLA_TC else N.DA_MLA_EXACT_BELOW)
+        lens = [p.seq_lens[b] for b in range(p.batch)]
+        exact = any(L < below for L in lens)
+        split = int(any(L >= below for L in lens)) + int(exact)
+    if a.flags & N.DA_FLAG_NO_COMBINE:
+        return split
+    fused = bool(a.flags & N.DA_FLAG_ONE_LAUNCH) and not exact
+    return split + (0 if fused else 1)
+
+
+def time_one_launch(case, q, k, v, out_dt, dev, flush, args):
+    """Median step time with the merge folded into the split kernel
+    (DA_FLAG_ONE_LAUNCH), for comparison with the default two launches."""
+    import torch
+    from split_kv_decode_gb300 import _native as N
+    from split_kv_decode_gb300 import api as A
+    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
+                    flags=N.DA_FLAG_ONE_LAUNCH)
+    lens = case.seq_lens.tolist()
+    p = A.decode_attn_plan(a, lens)
+    ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    out = torch.empty(out_shape(case), dtype=out_dt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        A.decode_attn_splitk_ex(a, A.decode_attn_plan(a, lens), q, k, v, out, ws, stream)
+    us = _timed_steps(lambda: A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream), flush,
+                      max(20, min(args.steps, 200)), stream)
+    return round(us, 2)
+
+
 # every workload the pages' configurations name, in the default run
 CONFIG_SWEEP = ("gqa8x2_f32_L4096", "gqa16x4_f16_L4096", "gqa16x4_f16_L20480",
                 "gqa16x4_f16_L61440", "gqa16x4_f16_L151552", "gqa16x4_f16_L262144",
@@ -478,8 +530,9 @@ def time_split_and_step(workload, dev, steps):
     case, q, k, v = make_inputs(workload, dev, draw_on_device=True)
     out_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[case.out_dtype]
     stream = torch.cuda.current_stream(dev)
-    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
-                    flags=N.DA_FLAG_NO_COMBINE)
+    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
+    a_split = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
+                          flags=N.DA_FLAG_NO_COMBINE)
     lens = case.seq_lens.tolist()
     p0 = A.decode_attn_plan(a, lens)
     ws = torch.empty(A.decode_attn_workspace_bytes(p0), dtype=torch.uint8, device=dev)
@@ -487,9 +540,7 @@ def time_split_and_step(workload, dev, steps):
     flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4 + 1024,
                         dtype=torch.float32, device=dev)
     for _ in range(3):
-        p = A.decode_attn_plan(a, lens)
-        A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
-        A.decode_attn_combine(a, p, ws, out, stream)
+        A.decode_attn_splitk_ex(a, A.decode_attn_plan(a, lens), q, k, v, out, ws, stream)
     torch.cuda.synchronize()
     st, sp = [], []
     for i in range(steps):
@@ -498,25 +549,30 @@ def time_split_and_step(workload, dev, steps):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         e[0].record(stream)
         A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
-        A.decode_attn_combine(a, p, ws, out, stream)
         e[1].record(stream)
         st.append(e)
     for i in range(steps):
-        p = A.decode_attn_plan(a, lens)
+        p = A.decode_attn_plan(a_split, lens)
         flush.fill_(float(i))
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         e[0].record(stream)
-        A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
+        A.decode_attn_splitk_ex(a_split, p, q, k, v, out, ws, stream)
         e[1].record(stream)
-        A.decode_attn_combine(a, p, ws, out, stream)
         sp.append(e)
+    a_one = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
+                        flags=N.DA_FLAG_ONE_LAUNCH)
+    for _ in range(3):
+        A.decode_attn_splitk_ex(a_one, A.decode_attn_plan(a_one, lens), q, k, v, out, ws, stream)
+    p1 = A.decode_attn_plan(a_one, lens)
+    one_us = _timed_steps(lambda: A.decode_attn_splitk_ex(a_one, p1, q, k, v, out, ws, stream),
+                          flush, max(20, steps // 2), stream)
     torch.cuda.synchronize()
     A.decode_attn_device_status(ws, stream)
     step_us = [x.elapsed_time(y) * 1e3 for x, y in st]
     split_us = [x.elapsed_time(y) * 1e3 for x, y in sp]
     kernel = {N.DA_KERNEL_GQA_TMA: "gqa_split_kernel", N.DA_KERNEL_GQA_TC: "gqa_tc_kernel",
               N.DA_KERNEL_MLA_TC: "mla_split_kernel"}.get(p0.kernel, str(p0.kernel))
-    res = (case, kernel, step_us, split_us, p0)
+    res = (case, kernel, step_us, split_us, p0, count_launches(a, p0), one_us)
     del q, k, v, ws, out, flush
     torch.cuda.empty_cache()
     return res
@@ -528,16 +584,19 @@ def measure_configs(dev, peak, steps=100):
     HBM bandwidth."""
     res = {}
     for w in CONFIG_SWEEP:
-        case, kernel, step_us, split_us, p = time_split_and_step(w, dev, steps)
+        case, kernel, step_us, split_us, p, launches, one_us = time_split_and_step(w, dev, steps)
         sm = statistics.mean(split_us)
+        km = statistics.mean(step_us) if launches == 1 else sm
         res[w] = {
             "kernel": kernel, "kv_bytes": case.kv_bytes, "steps": steps,
+            "launches_per_step": launches,
             "step_us_mean": round(statistics.mean(step_us), 2),
             "step_us_median": round(statistics.median(step_us), 2),
-            "split_us_mean": round(sm, 2),
-            "split_us_median": round(statistics.median(split_us), 2),
+            "split_only_us_mean": round(sm, 2),
+            "split_only_us_median": round(statistics.median(split_us), 2),
+            "one_launch_step_us_median": round(one_us, 2),
             "kv_gbs": round(case.kv_bytes / (statistics.mean(step_us) * 1e-6) / 1e9, 1),
-            "split_frac_of_measured_hbm": round(case.kv_bytes / (sm * 1e-6) / 1e9 / peak, 4),
+            "kernel_frac_of_measured_hbm": round(case.kv_bytes / (km * 1e-6) / 1e9 / peak, 4),
             "splits": p.n_splits[0], "items": p.n_items, "grid": p.grid,
         }
     return res
@@ -583,7 +642,7 @@ def measure_graph(case, q, k, v, out_dt, dev, flush, args):
     with torch.cuda.stream(s):
         us = _timed_steps(g.replay, flush, n, s)
     return {"value": round(us, 2), "unit": "us/layer-step", "steps": n,
-            "what": "split + combine replayed from one CUDA graph, lengths read on the device"}
+            "what": "whole step replayed from one CUDA graph, lengths read on the device"}
 
 
 def measure_paged(case, q, k, v, out_dt, dev, flush, args, block_size):
@@ -622,7 +681,7 @@ def measure_paged(case, q, k, v, out_dt, dev, flush, args, block_size):
     torch.cuda.empty_cache()
     return {"value": round(us, 2), "unit": "us/layer-step", "steps": n, "block_size": block_size,
             "kv_gbs": round(gbs, 1),
-            "what": "split + combine with the caches in a pool of blocks, random block order"}
+            "what": "whole step with the caches in a pool of blocks, random block order"}
 
 
 def measure_wv_b(case, q, k, v, out_dt, dev, flush, args, wdt):
@@ -684,7 +743,7 @@ def measure_multi_token(case, k, v, out_dt, dev, flush, args):
             "kv_gbs": round(case.kv_bytes / (us * 1e-6) / 1e9, 1)}
     if not res:
         return None
-    res["what"] = ("split + combine for q_len new tokens per sequence, causal among "
+    res["what"] = ("whole step for q_len new tokens per sequence, causal among "
                    "themselves, sharing every K/V tile")
     return res
 
@@ -692,14 +751,11 @@ def measure_multi_token(case, k, v, out_dt, dev, flush, args):
 def measure_hot(case, q, k, v, out_dt, dev, args, reps=10):
     """The step with no L2 flush between steps (labelled: inputs that fit the
     129 MB L2 are then served from it). The device time alone: `reps`
-    consecutive steps (split with the lengths read on the device, then the
-    combine) are captured in one CUDA graph and replayed, so host work does not
-    show."""
+    consecutive steps (with the lengths read on the device) are captured in one
+    CUDA graph and replayed, so host work does not show."""
     import torch
-    from split_kv_decode_gb300 import _native as N
     from split_kv_decode_gb300 import api as A
-    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt,
-                    flags=N.DA_FLAG_NO_COMBINE)
+    a = A.make_args(q, k, v, case.scale, v_dim=case.v_dim, out_dtype=out_dt)
     p = A.decode_attn_plan(a, case.seq_lens.tolist())
     ws = torch.empty(A.decode_attn_workspace_bytes(p), dtype=torch.uint8, device=dev)
     out = torch.empty(out_shape(case), dtype=out_dt, device=dev)
@@ -709,7 +765,6 @@ def measure_hot(case, q, k, v, out_dt, dev, args, reps=10):
 
     def one():
         A.decode_attn_splitk_dev(a, p, d, q, k, v, out, ws, s)
-        A.decode_attn_combine(a, p, ws, out, s)
 
     with torch.cuda.stream(s):
         for _ in range(3):
@@ -732,7 +787,7 @@ def measure_hot(case, q, k, v, out_dt, dev, args, reps=10):
     torch.cuda.synchronize()
     us = statistics.median(x.elapsed_time(y) * 1e3 for x, y in ts) / reps
     return {"value": round(us, 2), "unit": "us/layer-step", "steps": len(ts) * reps,
-            "what": f"split + combine, {reps} steps per CUDA graph replay, no L2 flush",
+            "what": f"whole step, {reps} steps per CUDA graph replay, no L2 flush",
             "fits_l2": case.kv_bytes < 120 * (1 << 20)}
 
 

@@ -78,6 +78,17 @@ typedef enum {
 #define DA_FLAG_MLA_TC 0x10      /* MLA shape: every sequence on the tensor-core
                                     kernel, whose operands are bf16 (see
                                     DA_MLA_EXACT_BELOW)                              */
+#define DA_FLAG_ONE_LAUNCH 0x20  /* the split kernel merges its own partials (no
+                                    combine launch): the last split of a (sequence,
+                                    KV head) group to finish merges the group (GQA
+                                    kernels), or the CTAs merge shares of the rows
+                                    once all have finished (MLA tensor-core kernel,
+                                    when the GPU holds all its clusters at once); a
+                                    memset of the workspace's arrival counters
+                                    precedes the launch. Measured slower than the
+                                    default two launches on GB300 (the merge runs in
+                                    one CTA per group instead of hundreds), so it is
+                                    an option, not the default                     */
 #define DA_FLAG_TEST_NO_TMA 0x100 /* test hook: the producer issues no copy, so every
                                      consumer wait runs out after timeout_us and the
                                      kernel reports DA_ETIMEOUT through device_status */

@@ -113,6 +113,13 @@ int check_args(const da_args_t *a)
     return DA_OK;
 }
 
+// Does a split + combine call let the split kernel merge its own partials?
+// Only when the caller asks for one launch (and never for a split-only call).
+bool want_fuse(const da_args_t *a)
+{
+    return (a->flags & DA_FLAG_ONE_LAUNCH) && !(a->flags & DA_FLAG_NO_COMBINE);
+}
+
 // MLA: sequences shorter than this (current length) run on the f32
 // CUDA-core kernel, the others on the tensor-core kernel
 int mla_exact_below(const da_args_t *a)
@@ -292,7 +299,8 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
     if (pl->total_splits != base || pl->n_items != items || pl->grid < kc->cluster ||
         pl->grid > items * kc->cluster || pl->grid % kc->cluster)
         return fail(DA_EINVAL, "plan", "inconsistent plan totals");
-    if (pl->workspace_bytes != ws_total(pl->total_splits, rows_of(a), a->v_dim))
+    if (pl->workspace_bytes != ws_total(pl->total_splits, rows_of(a), a->v_dim,
+                                        ws_counters(a->batch, a->n_kv_heads)))
         return fail(DA_EINVAL, "plan", "inconsistent workspace size");
     return DA_OK;
 }
@@ -306,8 +314,31 @@ int split_grid(const da_args_t *a, const da_plan_t *pl)
     return (a->flags & DA_FLAG_TEST_BAD_LAUNCH) ? 0 : pl->grid;
 }
 
+FusedOut fused_out(const da_args_t *a, const da_plan_t *pl, void *ws, void *out)
+{
+    FusedOut f;
+    std::memset(&f, 0, sizeof f);
+    f.ctr = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) +
+                                         ws_ctr_offset(pl->total_splits, rows_of(a), a->v_dim));
+    f.out = out;
+    f.out_dtype = a->out_dtype;
+    return f;
+}
+
+// The arrival counters start every call at zero: one memset on the stream,
+// before the split kernel that counts on them.
+int zero_counters(const da_args_t *a, const da_plan_t *pl, const FusedOut &f, cudaStream_t st)
+{
+    const cudaError_t e =
+        cudaMemsetAsync(f.ctr, 0, (size_t)ws_counters(a->batch, a->n_kv_heads) * 4, st);
+    if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "counter reset: %s", cudaGetErrorString(e));
+    (void)pl;
+    return DA_OK;
+}
+
 int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
-               const void *v, void *ws, cudaStream_t st, const da_dev_t *dev)
+               const void *v, void *ws, cudaStream_t st, const da_dev_t *dev, void *out,
+               bool want_fuse, bool *fused)
 {
     (void)v; // the same buffer as k (checked with the arguments)
     MlaParams p;
@@ -355,6 +386,16 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
         any_tc |= L >= p.exact_below;
         any_exact |= (p.dev_lens ? q_len_of(a) : L) < p.exact_below;
     }
+    // the tensor-core kernel merges its own partials when it serves every
+    // sequence and the GPU holds all its clusters at once (its grid-wide
+    // arrival count must not wait on a cluster that cannot start)
+    p.fused = fused_out(a, pl, ws, out);
+    p.fused.on = want_fuse && !any_exact && pl->grid / 2 <= mla_max_clusters(rows_of(a));
+    *fused = p.fused.on != 0;
+    if (p.fused.on) {
+        const int rc = zero_counters(a, pl, p.fused, st);
+        if (rc) return rc;
+    }
     if (any_tc) {
         cudaError_t e = launch_mla_split(split_grid(a, pl), st, p);
         if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
@@ -370,10 +411,15 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
     return DA_OK;
 }
 
+// Launches the split kernel(s). want_fuse: the kernels may merge their own
+// partials into `out` (no combine launch); *fused says whether they will.
 int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
-                 const void *v, void *ws, cudaStream_t st, const da_dev_t *dev)
+                 const void *v, void *ws, cudaStream_t st, const da_dev_t *dev, void *out,
+                 bool want_fuse, bool *fused)
 {
-    if (pl->kernel == DA_KERNEL_MLA_TC) return launch_mla(a, pl, q, k, v, ws, st, dev);
+    *fused = false;
+    if (pl->kernel == DA_KERNEL_MLA_TC)
+        return launch_mla(a, pl, q, k, v, ws, st, dev, out, want_fuse, fused);
     SplitParams p;
     std::memset(&p, 0, sizeof p);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -396,6 +442,13 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
         p.items.split_base[b] = pl->split_base[b];
     }
     p.items.split_base[a->batch] = pl->total_splits;
+    p.fused = fused_out(a, pl, ws, out);
+    p.fused.on = want_fuse;
+    *fused = want_fuse;
+    if (want_fuse) {
+        const int rc = zero_counters(a, pl, p.fused, st);
+        if (rc) return rc;
+    }
 
     GqaMaps m;
     std::memset(&m, 0, sizeof m);
@@ -599,7 +652,7 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
     }
     plan->total_splits = (int32_t)base;
     plan->max_splits = mx;
-    plan->workspace_bytes = ws_total(base, rows_of(a), a->v_dim);
+    plan->workspace_bytes = ws_total(base, rows_of(a), a->v_dim, ws_counters(a->batch, a->n_kv_heads));
     plan->est_cost = po.est_cost;
     return DA_OK;
 }
@@ -629,9 +682,10 @@ int decode_attn_splitk_ex(const da_args_t *a, const da_plan_t *plan, const float
     if (pre != cudaSuccess)
         return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = launch_split(a, plan, q, k, v, ws, st, nullptr);
+    bool fused = false;
+    rc = launch_split(a, plan, q, k, v, ws, st, nullptr, out, want_fuse(a), &fused);
     if (rc) return rc;
-    if (a->flags & DA_FLAG_NO_COMBINE) return DA_OK;
+    if (fused || (a->flags & DA_FLAG_NO_COMBINE)) return DA_OK;
     return launch_combine_phase(a, plan, ws, out, st);
 }
 
@@ -696,9 +750,10 @@ int decode_attn_splitk_dev(const da_args_t *a, const da_plan_t *plan, const da_d
     if (pre != cudaSuccess)
         return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = launch_split(a, plan, q, k, v, ws, st, dev);
+    bool fused = false;
+    rc = launch_split(a, plan, q, k, v, ws, st, dev, out, want_fuse(a), &fused);
     if (rc) return rc;
-    if (a->flags & DA_FLAG_NO_COMBINE) return DA_OK;
+    if (fused || (a->flags & DA_FLAG_NO_COMBINE)) return DA_OK;
     return launch_combine_phase(a, plan, ws, out, st);
 }
 
@@ -768,7 +823,8 @@ int decode_attn_splitk_proj(const da_args_t *a, const da_plan_t *plan, const da_
     if (pre != cudaSuccess)
         return fail(DA_ECUDA, "before split", "pending CUDA error: %s", cudaGetErrorString(pre));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = launch_split(a, plan, q, k, v, ws, st, nullptr);
+    bool fused = false; // the projection runs in its own combine launch
+    rc = launch_split(a, plan, q, k, v, ws, st, nullptr, out, false, &fused);
     if (rc) return rc;
     return launch_combine_phase(a, plan, ws, out, st, 1, &pj);
 }

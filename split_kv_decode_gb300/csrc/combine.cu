@@ -20,6 +20,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace skv {
@@ -30,28 +31,6 @@ constexpr int kCombineCols = 128;   // value columns per CTA (one float4 per lan
 constexpr int kCombinePrefetch = 10; // acc vectors per lane loaded before the weights
                                      // (all of them for up to 80 splits)
 
-template <typename OT> __device__ __forceinline__ void store4(OT *p, float4 v);
-template <> __device__ __forceinline__ void store4<float>(float *p, float4 v)
-{
-    *reinterpret_cast<float4 *>(p) = v;
-}
-template <> __device__ __forceinline__ void store4<__half>(__half *p, float4 v)
-{
-    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t *>(&a);
-    u.y = *reinterpret_cast<uint32_t *>(&b);
-    *reinterpret_cast<uint2 *>(p) = u;
-}
-template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v)
-{
-    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t *>(&a);
-    u.y = *reinterpret_cast<uint32_t *>(&b);
-    *reinterpret_cast<uint2 *>(p) = u;
-}
-
 template <typename OT> __device__ __forceinline__ void store1(OT *p, float v);
 template <> __device__ __forceinline__ void store1<float>(float *p, float v) { *p = v; }
 template <> __device__ __forceinline__ void store1<__half>(__half *p, float v)
@@ -61,14 +40,6 @@ template <> __device__ __forceinline__ void store1<__half>(__half *p, float v)
 template <> __device__ __forceinline__ void store1<__nv_bfloat16>(__nv_bfloat16 *p, float v)
 {
     *p = __float2bfloat16_rn(v);
-}
-
-__device__ __forceinline__ void fma4(float4 &a, float w, const float4 &v)
-{
-    a.x = fmaf(w, v.x, a.x);
-    a.y = fmaf(w, v.y, a.y);
-    a.z = fmaf(w, v.z, a.z);
-    a.w = fmaf(w, v.w, a.w);
 }
 
 // Merge the partials of row h of sequence b over the 128 value columns of

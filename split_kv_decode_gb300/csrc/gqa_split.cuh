@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace skv {
@@ -723,6 +724,33 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             }
             if (lane < G)
                 p.ml[row0 + row_off(lane)] = make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
+        }
+        if (p.fused.on) {
+            // The last partial of this (sequence, KV head) group to arrive merges
+            // the group's rows into out, so no combine launch is needed. Warp 0
+            // publishes its partial before the arrival is counted.
+            volatile int *last_flag = abort_flag + 1; // the header's spare word
+            if (warp == 0) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t n = (uint32_t)(it.split_base[b + 1] - it.split_base[b]);
+                    const bool last = arrive(p.fused.ctr + (size_t)b * it.n_kv_heads + kvh) == n;
+                    if (last) __threadfence(); // the other partials, before they are read
+                    *last_flag = last ? 1 : 0;
+                }
+            }
+            named_bar_sync(1, K::CONSUMERS);
+            if (*last_flag) {
+                constexpr int NB = (D + 127) / 128; // 128-column blocks of a row
+                const int S = it.split_base[b + 1] - it.split_base[b];
+                for (int u = warp; u < G * NB; u += NCW) {
+                    const int row = kvh * Gh + row_off(u / NB);
+                    warp_merge_row(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D,
+                                   (u % NB) * 128, out_row_ptr(p.fused, b, p.n_heads, row, D),
+                                   p.fused.out_dtype);
+                }
+            }
         }
     }
     if (threadIdx.x == 0) griddep_launch_dependents();

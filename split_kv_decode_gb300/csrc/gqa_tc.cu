@@ -43,6 +43,7 @@
 
 #include "gqa_split.cuh"
 #include "internal.h"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace skv {
@@ -372,6 +373,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t sph = 0, pfp = 0, qfp = 0, oph = 0;
         bool ab = false;
         int items = 0, gt = 0;
+        // After an item's partial is written: the last partial of its (sequence,
+        // KV head) group to arrive merges the group's rows into out (no combine
+        // launch). The four warps publish their writes before the arrival.
+        auto arrive_merge = [&](int b, int kvh) {
+            volatile int *last_flag = abort_flag + 1;
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (threadIdx.x == 0) {
+                const uint32_t n = (uint32_t)(p.items.split_base[b + 1] - p.items.split_base[b]);
+                const bool last = arrive(p.fused.ctr + (size_t)b * p.items.n_kv_heads + kvh) == n;
+                if (last) __threadfence(); // the other partials, before they are read
+                *last_flag = last ? 1 : 0;
+            }
+            named_bar_sync(1, 128);
+            if (*last_flag) {
+                const int S = p.items.split_base[b + 1] - p.items.split_base[b];
+                for (int u = warp; u < R * NBLK; u += 4) {
+                    const int rr = u / NBLK, tk = rr / Gh;
+                    const int row = kvh * Gh + tk * p.hq + (rr - tk * Gh);
+                    warp_merge_row(p.ml, p.acc, (size_t)p.items.split_base[b], S, p.n_heads, row,
+                                   D, (u % NBLK) * 128, out_row_ptr(p.fused, b, p.n_heads, row, D),
+                                   p.fused.out_dtype);
+                }
+            }
+        };
         for (int item = blockIdx.x; !ab && item < p.items.n_items; item += gridDim.x) {
             int b, kvh, s;
             decode_item(p.items, item, b, kvh, s);
@@ -382,6 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const size_t wrow = slot_id * p.n_heads + (size_t)kvh * Gh + row_off;
             if (p1 <= p0) { // an empty item: a neutral partial, no MMA took part
                 if (owner) p.ml[wrow] = make_float2(kNeutralM, 0.f);
+                if (p.fused.on) arrive_merge(b, kvh);
                 continue;
             }
             // ---- Q of this item's rows, once the previous item's QK is done with Q
@@ -549,6 +576,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar + TB_OFREE);
             if (owner) p.ml[wrow] = make_float2(l > 0.f ? m * kLn2 : kNeutralM, l);
+            if (p.fused.on) arrive_merge(b, kvh);
         }
         if (ab && threadIdx.x == 0 && !*abort_flag) {
             *abort_flag = 1;

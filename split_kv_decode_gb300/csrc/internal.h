@@ -10,9 +10,12 @@
 namespace skv {
 
 // Workspace layout (all offsets from the workspace base, bytes):
-//   [0, 256)                status header; int32 status word at offset 0
+//   [0, 256)                status header: int32 status word at offset 0
 //   [256, 256 + ml_bytes)   float2 (m, l) per (slot, query head)
 //   then                    float acc[slot][n_heads][v_dim]
+//   then                    uint32 arrival counters, zeroed by the library at the
+//                           start of a call that uses them: one per (sequence,
+//                           KV head) group, at least two
 // A slot is one split of one sequence: slot = split_base[b] + s.
 constexpr int64_t kWsHeader = 256;
 
@@ -22,13 +25,33 @@ inline int64_t ws_acc_offset(int64_t total_splits, int n_heads)
     int64_t ml = total_splits * n_heads * 8;
     return kWsHeader + ((ml + 255) / 256) * 256;
 }
-// rounded to 256 bytes, so that workspaces placed back to back (one per rank
-// of a context-parallel step) keep every region aligned
-inline int64_t ws_total(int64_t total_splits, int n_heads, int v_dim)
+inline int64_t ws_ctr_offset(int64_t total_splits, int n_heads, int v_dim)
 {
     const int64_t t = ws_acc_offset(total_splits, n_heads) + total_splits * n_heads * v_dim * 4;
     return (t + 255) / 256 * 256;
 }
+inline int64_t ws_counters(int batch, int n_kv_heads)
+{
+    const int64_t n = (int64_t)batch * n_kv_heads;
+    return n < 2 ? 2 : n;
+}
+// rounded to 256 bytes, so that workspaces placed back to back (one per rank
+// of a context-parallel step) keep every region aligned
+inline int64_t ws_total(int64_t total_splits, int n_heads, int v_dim, int64_t n_counters)
+{
+    return ws_ctr_offset(total_splits, n_heads, v_dim) + (n_counters * 4 + 255) / 256 * 256;
+}
+
+// A split kernel that merges its own partials (no combine launch): the last
+// partial of a (sequence, KV head) group to arrive merges the group's rows
+// (GQA kernels); every CTA merges a share of the rows once all CTAs have
+// arrived (MLA tensor-core kernel).
+struct FusedOut {
+    void *out;                   // [B][rows][v_dim] in out_dtype
+    uint32_t *ctr;               // arrival counters (workspace tail), zero at launch
+    int32_t out_dtype;           // DA_F32 / DA_F16 / DA_BF16
+    int32_t on;                  // 0: partials only (a combine launch merges them)
+};
 
 // Status word codes written by kernels (low byte = da_status_t, next byte = kernel).
 constexpr int kStatusTimeoutGqa = DA_ETIMEOUT | (DA_KERNEL_GQA_TMA << 8);
@@ -60,6 +83,7 @@ struct SplitParams {
     // Optional, read on the device (so that one captured launch serves changing
     // contexts): current lengths (each clamped to [1, items.seq_lens[b]]), and
     // a block table for paged caches. NULL: the plan's lengths / contiguous caches.
+    FusedOut fused;
     const int32_t *dev_lens;
     const int32_t *block_table; // [batch][max_blocks] pool block of each block_size positions
     int32_t max_blocks;
@@ -98,6 +122,7 @@ struct MlaParams {
     // sequences entirely (it writes nothing for them).
     int32_t exact_below;
     int32_t reset_status;    // the exact kernel runs alone in this call: it clears the status word
+    FusedOut fused;
     ItemTable items;         // n_kv_heads = 1
 };
 
@@ -106,6 +131,9 @@ struct MlaParams {
 bool mla_supported_heads(int n_heads);
 int mla_smem_bytes(int n_heads);
 cudaError_t launch_mla_split(int grid, cudaStream_t stream, const MlaParams &p);
+// 2-CTA clusters of the MLA tensor-core kernel the current device holds at once
+// (0 if unknown): its merge without a combine launch needs every cluster resident.
+int mla_max_clusters(int n_heads);
 // MLA split kernel in f32 on the CUDA cores: one CTA per (work item, group of
 // 32 rows); grid = n_items * mla_exact_groups(rows).
 int mla_exact_groups(int rows);

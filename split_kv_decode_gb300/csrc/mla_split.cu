@@ -52,10 +52,12 @@
 // tile holds a score above m + 8 (log2 units), so P <= 2^8 and l, O^T cannot
 // overflow, and O^T (whose column h spans all lanes) is rescaled only then.
 // Any reference gives the same partial after normalisation.
+#include <atomic>
 #include <climits>
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace skv {
@@ -656,6 +658,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync_all();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, LY::TMEM_COLS);
+
+    if (p.fused.on) {
+        // The merge without a combine launch: once every CTA of the launch has
+        // written its partials (a grid-wide arrival count; the library fuses
+        // only when the GPU holds all the launch's clusters at once), every warp
+        // of the grid merges a share of the (sequence, row, 128 columns) units.
+        volatile int *go = abort_flag + 1;
+        uint32_t *arrived = p.fused.ctr;
+        __threadfence(); // this thread's partial writes, before the arrival
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            (void)arrive(arrived);
+            const uint64_t t0 = global_ns();
+            bool ok = true;
+            while (*reinterpret_cast<volatile uint32_t *>(arrived) < gridDim.x) {
+                if (global_ns() - t0 > p.timeout_ns) {
+                    ok = false;
+                    atomicCAS(p.status, 0, kStatusTimeoutMla);
+                    break;
+                }
+                __nanosleep(100);
+            }
+            __threadfence();
+            *go = ok && *reinterpret_cast<volatile int *>(p.status) == 0;
+        }
+        __syncthreads();
+        if (*go) {
+            const int rows = p.n_heads, units = it.batch * rows * (kDv / 128);
+            const int nw = (int)gridDim.x * (kThreads / 32);
+            for (int u = (int)blockIdx.x * (kThreads / 32) + warp; u < units; u += nw) {
+                const int b = u / (rows * (kDv / 128)), r = u % (rows * (kDv / 128));
+                const int row = r / (kDv / 128), z = r % (kDv / 128);
+                warp_merge_row(p.ml, p.acc, (size_t)it.split_base[b],
+                               it.split_base[b + 1] - it.split_base[b], rows, row, kDv, z * 128,
+                               out_row_ptr(p.fused, b, rows, row, kDv), p.fused.out_dtype);
+            }
+        }
+    }
     if (threadIdx.x == 0) griddep_launch_dependents();
 }
 
@@ -681,6 +721,49 @@ template <int N> static cudaError_t launch_n(int grid, cudaStream_t st, const Ml
     if (e != cudaSuccess) return e;
     fn<<<grid, kThreads, Layout<N>::ALLOC, st>>>(p);
     return cudaGetLastError();
+}
+
+// How many of the kernel's 2-CTA clusters the current device holds at once
+// (cached per device and row count; 0 if the query fails).
+template <int N> static int max_clusters_n()
+{
+    constexpr int kDevs = 64;
+    static std::atomic<int> cache[kDevs]; // 0: not asked yet; -1: the query failed
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return 0;
+    if (cache[dev] == 0) {
+        auto *fn = mla_split_kernel<N>;
+        int n = -1;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Layout<N>::ALLOC) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = Layout<N>::ALLOC;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, (void *)fn, &cfg) != cudaSuccess || n < 1) n = -1;
+        }
+        (void)cudaGetLastError();
+        cache[dev].store(n);
+    }
+    const int n = cache[dev].load();
+    return n > 0 ? n : 0;
+}
+
+int mla_max_clusters(int n_heads)
+{
+    switch (n_heads) {
+    case 32: return max_clusters_n<16>();
+    case 64: return max_clusters_n<32>();
+    case 96: return max_clusters_n<48>();
+    default: return 0;
+    }
 }
 
 cudaError_t launch_mla_split(int grid, cudaStream_t st, const MlaParams &p)

@@ -16,7 +16,6 @@ from typing import List, Optional, Sequence
 
 import torch
 
-from . import _native as N
 from . import api as A
 
 
@@ -59,16 +58,16 @@ class BucketedDecode:
         self.stream.wait_stream(torch.cuda.current_stream(q.device))
         for b in self.buckets:
             a = A.make_args(q[:b], k_cache[:b], v_cache[:b], scale, v_dim=v_dim,
-                            out_dtype=out_dtype, flags=N.DA_FLAG_NO_COMBINE)
+                            out_dtype=out_dtype)
             p = A.decode_attn_plan(a, [self.capacity] * b)
             ws = A.new_workspace(p, device=q.device)
             d = A.make_dev(seq_lens=self.lens[:b])
             out = self.out[:b]
 
             def step(a=a, p=p, ws=ws, d=d, out=out, b=b):
+                # split, then the combine launch (the library's default)
                 A.decode_attn_splitk_dev(a, p, d, q[:b], k_cache[:b], v_cache[:b], out, ws,
                                          self.stream)
-                A.decode_attn_combine(a, p, ws, out, self.stream)
 
             with torch.cuda.stream(self.stream):
                 step()                                   # warm-up outside the capture
