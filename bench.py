@@ -44,6 +44,8 @@ WORKLOADS = {
     "gqa24x4_f32_b4": ("gqa_24x4", None),
     "ragged32_bf16": ("ragged_32", None),
     "mla96_f32_L131072": ("mla_96", None),
+    "mla128_f32_L131072": ("mla_128", None),
+    "mla96_f16_L131072": ("mla_96_f16", None),
     # four new tokens per sequence on the default cache: 16 query rows per KV head
     "gqa16x4_f16_L151552_q4": ("gqa_16x4", 151552, 4),
 }
@@ -51,6 +53,8 @@ DEFAULT = "gqa16x4_f16_L151552"
 METRIC = "decode-attention us/layer-step (and KV GB/s)"   # both arms report this metric
 # the split kernel each workload runs, and the arithmetic type it computes in
 KERNEL = {"mla96_f32_L131072": ("mla_split_kernel", "bf16"),
+          "mla128_f32_L131072": ("mla_split_kernel", "bf16"),
+          "mla96_f16_L131072": ("mla_split_kernel", "f16"),
           "gqa16x4_f16_L151552_q4": ("gqa_tc_kernel", "f16")}
 DEFAULT_KERNEL = ("gqa_split_kernel", "f32")
 
@@ -83,9 +87,10 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "gqa_split_kernel": ("gqa_split.cuh", "gqa_inst.cuh", "gqa_f32.cu", "gqa_f16.cu", "gqa_bf16.cu"),
-    "gqa_tc_kernel": ("gqa_tc.cu", "gqa_split.cuh"),
-    "mla_split_kernel": ("mla_split.cu",),
+    "gqa_split_kernel": ("gqa_split.cuh", "gqa_inst.cuh", "gqa_f32.cu", "gqa_f16.cu", "gqa_bf16.cu",
+                         "merge.cuh"),
+    "gqa_tc_kernel": ("gqa_tc.cu", "gqa_split.cuh", "merge.cuh"),
+    "mla_split_kernel": ("mla_split.cu", "merge.cuh"),
 }
 
 
@@ -516,7 +521,8 @@ def time_one_launch(case, q, k, v, out_dt, dev, flush, args):
 # every workload the pages' configurations name, in the default run
 CONFIG_SWEEP = ("gqa8x2_f32_L4096", "gqa16x4_f16_L4096", "gqa16x4_f16_L20480",
                 "gqa16x4_f16_L61440", "gqa16x4_f16_L151552", "gqa16x4_f16_L262144",
-                "mla96_f32_L131072", "gqa24x4_f32_b4", "ragged32_bf16", "gqa16x4_f16_L151552_q4")
+                "mla96_f32_L131072", "gqa24x4_f32_b4", "ragged32_bf16", "gqa16x4_f16_L151552_q4",
+                "mla128_f32_L131072", "mla96_f16_L131072")
 
 
 def time_split_and_step(workload, dev, steps):

@@ -124,6 +124,7 @@ bool want_fuse(const da_args_t *a)
 // CUDA-core kernel, the others on the tensor-core kernel
 int mla_exact_below(const da_args_t *a)
 {
+    if (a->kv_dtype != DA_F32) return 0; // 16-bit caches: the stored values are the operands
     if (a->flags & DA_FLAG_MLA_SIMT) return INT32_MAX;
     if (a->flags & DA_FLAG_MLA_TC) return 0;
     return DA_MLA_EXACT_BELOW;
@@ -142,17 +143,19 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
     const int G = a->n_heads / a->n_kv_heads * q_len_of(a);
     const int es = dtype_size(a->kv_dtype);
     if (a->head_dim == 576 && a->v_dim == 512 && a->n_kv_heads == 1) {
-        if (a->kv_dtype != DA_F32)
-            return fail(DA_EUNSUPPORTED, "plan", "the MLA kernel reads an f32 latent cache");
         // the rows of an item are (query token, head) pairs, like heads of MQA
         if (!mla_supported_heads(rows_of(a)))
             return fail(DA_EUNSUPPORTED, "plan",
-                        "the MLA kernel serves 32, 64 or 96 query rows (heads x q_len; got %d)",
+                        "the MLA kernel serves 32, 64, 96 or 128 query rows (heads x q_len; "
+                        "got %d)",
                         rows_of(a));
-        if (a->k_pos_stride < 576 || (a->k_pos_stride * 4) % 16 ||
-            (a->batch > 1 && (a->k_batch_stride * 4) % 16))
+        if (a->k_pos_stride < 576 || (a->k_pos_stride * es) % 16 ||
+            (a->batch > 1 && (a->k_batch_stride * es) % 16))
             return fail(DA_EUNSUPPORTED, "plan",
                         "MLA latent rows need >= 576 elements and 16-byte aligned strides");
+        if ((a->flags & DA_FLAG_MLA_SIMT) && a->kv_dtype != DA_F32)
+            return fail(DA_EUNSUPPORTED, "plan",
+                        "DA_FLAG_MLA_SIMT: the f32 CUDA-core MLA kernel reads an f32 cache");
         if (a->v_pos_stride != a->k_pos_stride || (a->batch > 1 && a->v_batch_stride != a->k_batch_stride))
             return fail(DA_EUNSUPPORTED, "plan",
                         "MLA values must be the first 512 columns of the key rows (same strides)");
@@ -345,7 +348,7 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
     std::memset(&p, 0, sizeof p);
     uint8_t *w = static_cast<uint8_t *>(ws);
     p.q = q;
-    p.cache = static_cast<const float *>(k);
+    p.cache = k;
     p.pos_stride = a->k_pos_stride;
     p.batch_stride = a->batch > 1 ? a->k_batch_stride : 0;
     p.ml = reinterpret_cast<float2 *>(w + ws_ml_offset());
@@ -397,7 +400,7 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
         if (rc) return rc;
     }
     if (any_tc) {
-        cudaError_t e = launch_mla_split(split_grid(a, pl), st, p);
+        cudaError_t e = launch_mla_split(split_grid(a, pl), st, p, a->kv_dtype);
         if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
     }
     if (any_exact) {
@@ -700,7 +703,8 @@ int decode_attn_splitk_dev(const da_args_t *a, const da_plan_t *plan, const da_d
     rc = check_plan(a, plan, &kc);
     if (rc) return rc;
     if (kc.kernel == DA_KERNEL_MLA_TC && dev->block_table &&
-        (dev->v_block_stride != dev->k_block_stride || (dev->k_block_stride * 4) % 16))
+        (dev->v_block_stride != dev->k_block_stride ||
+         (dev->k_block_stride * dtype_size(a->kv_dtype)) % 16))
         return fail(DA_EUNSUPPORTED, "args",
                     "MLA latent pools: one pool for keys and values (equal block strides, "
                     "16-byte multiples)");

@@ -96,7 +96,8 @@ struct SplitParams {
 
 struct MlaParams {
     const float *q;          // [B][Hq][576]
-    const float *cache;      // latent rows: element (b, pos, d) at b*batch_stride + pos*pos_stride + d
+    const void *cache;       // latent rows (f32, f16 or bf16): element (b, pos, d) at
+                             // b*batch_stride + pos*pos_stride + d (elements)
     int64_t pos_stride;      // elements between positions (>= 576)
     int64_t batch_stride;    // elements between sequences
     float2 *ml;              // workspace (m, l) per (slot, head)
@@ -127,10 +128,11 @@ struct MlaParams {
 };
 
 // MLA tensor-core split kernel: rows per CTA = rows / 2 (a 2-CTA cluster
-// shares every tile); supported rows (heads x q_len): 32, 64, 96.
+// shares every tile); supported rows (heads x q_len): 32, 64, 96, 128; an f32,
+// f16 or bf16 latent cache (kv_dtype).
 bool mla_supported_heads(int n_heads);
 int mla_smem_bytes(int n_heads);
-cudaError_t launch_mla_split(int grid, cudaStream_t stream, const MlaParams &p);
+cudaError_t launch_mla_split(int grid, cudaStream_t stream, const MlaParams &p, int kv_dtype);
 // 2-CTA clusters of the MLA tensor-core kernel the current device holds at once
 // (0 if unknown): its merge without a combine launch needs every cluster resident.
 int mla_max_clusters(int n_heads);

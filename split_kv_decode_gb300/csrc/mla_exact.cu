@@ -104,14 +104,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_exact_kernel(const __grid_con
     const int lim = (p.flags & DA_FLAG_NO_CAUSAL) ? (INT_MAX >> 1)
                                                    : L - p.q_len + 1 + row / p.hq;
 
+    const float *cache = static_cast<const float *>(p.cache); // an f32 cache
     auto row_src = [&](int pos) -> const float * {
         if (p.block_table) {
             const int idx = pos / p.block_size;
             const int blk = __ldg(p.block_table + (size_t)b * p.max_blocks + idx);
-            return p.cache + (size_t)blk * p.block_stride +
+            return cache + (size_t)blk * p.block_stride +
                    (size_t)(pos - idx * p.block_size) * p.pos_stride;
         }
-        return p.cache + (size_t)b * p.batch_stride + (size_t)pos * p.pos_stride;
+        return cache + (size_t)b * p.batch_stride + (size_t)pos * p.pos_stride;
     };
     // tile t -> buffer: rows past the slice repeat its last row (finite; their
     // probabilities are zero)

@@ -55,6 +55,7 @@
 #include <atomic>
 #include <climits>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "merge.cuh"
@@ -80,13 +81,20 @@ constexpr int kGroups = 3;                        // a tile is released to the M
 constexpr int kGroupChunks = kChunks / kGroups;
 constexpr int kPeerTx = kGroupChunks * kConvWarps * kRowsPerConv * 128; // bytes the peer ships per group
 
+// P of a tile (N rows of 64 positions, 128 B each) lives in the tile's own
+// slot, over its last chunk (the 64 rope columns): that chunk is read by the
+// tile's QK product and, for this CTA's rows, by the bulk copy to the peer. The
+// softmax writes P once the QK products of both CTAs are done (the peer's waited
+// for the copy), and the slot is refilled only after both CTAs' PV products of
+// the tile are done.
+constexpr int kPChunk = kChunks - 1;
+
 template <int N> struct Layout {
     static constexpr int TILE = 0;                          // 2 slots x 72 KB
     static constexpr int QCH = N * 128;                     // one Q chunk (N rows)
     static constexpr int Q = TILE + 2 * kSlotBytes;
     static constexpr int QEND = Q + kChunks * QCH + (kTile * 128 - QCH); // 64-row reads stay inside
-    static constexpr int PT = (QEND + 1023) / 1024 * 1024;  // P: 2 slots of N rows x 128 B
-    static constexpr int BAR = PT + 2 * QCH;
+    static constexpr int BAR = (QEND + 15) / 16 * 16;
     static constexpr int NBAR = 28;
     static constexpr int MISC = BAR + NBAR * 8;             // tmem base, abort flag
     static constexpr int ALPHA = (MISC + 16 + 15) / 16 * 16; // float alpha[N]
@@ -94,8 +102,8 @@ template <int N> struct Layout {
     static constexpr int ALLOC = USED + 1024;
     static constexpr int O_COL = 128;                       // O^T block j at O_COL + j*N
     static constexpr int TMEM_COLS = O_COL + 4 * N <= 256 ? 256 : 512;
-    static_assert(N % 16 == 0 && N >= 16 && N <= 48, "heads per CTA");
-    static_assert(QCH % 1024 == 0 && Q % 1024 == 0 && PT % 1024 == 0, "swizzle atoms");
+    static_assert(N % 16 == 0 && N >= 16 && N <= 64, "heads per CTA");
+    static_assert(QCH % 1024 == 0 && Q % 1024 == 0, "swizzle atoms");
     static_assert(ALLOC <= 232448, "shared memory");
 };
 
@@ -112,11 +120,24 @@ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t byte)
     return (row >> 3) * 1024 + (row & 7) * 128 + ((((byte >> 4) ^ row) & 7) << 4) + (byte & 15);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
-{
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
+// The cache's element type CT and the MMA operand type: an f32 or bf16 cache
+// feeds bf16 operands (q and P rounded to bf16), an f16 cache f16 operands.
+template <typename CT> struct Operand {
+    static constexpr bool kF16 = false;
+    static __device__ __forceinline__ uint32_t pack(float a, float b)
+    {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+template <> struct Operand<__half> {
+    static constexpr bool kF16 = true;
+    static __device__ __forceinline__ uint32_t pack(float a, float b)
+    {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
 
 __device__ __forceinline__ bool bar_or(int id, int threads, bool pred)
 {
@@ -213,11 +234,13 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag, uint32_t a
     }
 }
 
-template <int N>
+template <int N, typename CT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_split_kernel(const __grid_constant__ MlaParams p)
 {
     using LY = Layout<N>;
+    using OP = Operand<CT>;
+    constexpr bool kWide = sizeof(CT) == 4; // an f32 cache: 32 bytes per lane and chunk
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -242,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_init(bar + B_CONV + kGroups * s + g, kConvWarps);
             }
             mbar_init(bar + B_EMPTY + s, 2);
-            mbar_init(bar + B_SFULL + s, 1);
+            mbar_init(bar + B_SFULL + s, 2); // both CTAs' QK products (see kPChunk)
             mbar_init(bar + B_SFREE + s, kSoftWarps);
             mbar_init(bar + B_PFULL + s, kSoftWarps);
             mbar_init(bar + B_PFREE + s, 1);
@@ -269,9 +292,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int cw = warp - kSoftWarps;
         const uint32_t row0 = rank * 32 + cw * kRowsPerConv; // this warp's rows of every tile
         const int trow = lane >> 3, q8 = lane & 7;            // this lane's row and 8 columns
-        // lane q8 takes floats [4*q8, 4*q8 + 4) and [32 + 4*q8, 36 + 4*q8) of each
-        // 64-column chunk: each load instruction reads whole 128-byte halves of 4 rows
-        const uint32_t off_lo = sw128(row0 + trow, q8 * 8), off_hi = sw128(row0 + trow, 64 + q8 * 8);
+        // f32 cache: lane q8 takes floats [4*q8, 4*q8 + 4) and [32 + 4*q8, 36 + 4*q8)
+        // of each 64-column chunk, so each load instruction reads whole 128-byte
+        // halves of 4 rows; 16-bit cache: elements [8*q8, 8*q8 + 8), whole 128-byte
+        // rows, stored as they are
+        const uint32_t off_lo = sw128(row0 + trow, q8 * (kWide ? 8 : 16));
+        const uint32_t off_hi = sw128(row0 + trow, 64 + q8 * 8);
         uint32_t eph = 0, qph = 0;
         bool ok = true;
         // A whole tile of this lane's row (9 chunks) is in flight in registers:
@@ -279,28 +305,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // and the unrolled body has no branch. Rows past the item's end are
         // loaded from its last row and stored as zeros (the cache may hold
         // anything there; the zero rows keep the PV product finite).
-        float4 ld[kChunks][2];
+        constexpr int kLd = kWide ? 2 : 1;      // 16-byte loads per lane and chunk
+        constexpr int kChunkV4 = 64 * (int)sizeof(CT) / 16; // 16-byte units per chunk of a row
+        float4 ld[kChunks][kLd];
+        const CT *cache = static_cast<const CT *>(p.cache);
         auto row_src = [&](const Cursor &u) {
             const int pos = min(u.x.p0 + u.t * kTile + (int)row0 + trow, u.x.p1 - 1);
             if (p.block_table) { // paged: the row's block from the table
                 const int idx = pos / p.block_size;
                 const int blk = __ldg(p.block_table + (size_t)u.x.b * p.max_blocks + idx);
                 return reinterpret_cast<const float4 *>(
-                    p.cache + (size_t)blk * p.block_stride +
-                    (size_t)(pos - idx * p.block_size) * p.pos_stride + q8 * 4);
+                    cache + (size_t)blk * p.block_stride +
+                    (size_t)(pos - idx * p.block_size) * p.pos_stride) + q8;
             }
-            return reinterpret_cast<const float4 *>(p.cache + (size_t)u.x.b * p.batch_stride +
-                                                    (size_t)pos * p.pos_stride + q8 * 4);
+            return reinterpret_cast<const float4 *>(cache + (size_t)u.x.b * p.batch_stride +
+                                                    (size_t)pos * p.pos_stride) + q8;
         };
         Cursor cur;
         cur.start(p, cluster, nclusters);
         if (!cur.done) {
             const float4 *src = row_src(cur);
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                ld[c][0] = ldg_stream_v4(src + 16 * c);
-                ld[c][1] = ldg_stream_v4(src + 16 * c + 8);
-            }
+            for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+                for (int i = 0; i < kLd; ++i) ld[c][i] = ldg_stream_v4(src + kChunkV4 * c + 8 * i);
         }
         while (!cur.done) {
             Cursor nxt = cur;
@@ -321,8 +349,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const float4 b = __ldg(reinterpret_cast<const float4 *>(qb + h * kDk + g * 8 + 4));
                     const float sc = p.scale_log2;
                     sts_v4(sm_base + LY::Q + c * LY::QCH + sw128(h, j * 16),
-                           pack_bf16(a.x * sc, a.y * sc), pack_bf16(a.z * sc, a.w * sc),
-                           pack_bf16(b.x * sc, b.y * sc), pack_bf16(b.z * sc, b.w * sc));
+                           OP::pack(a.x * sc, a.y * sc), OP::pack(a.z * sc, a.w * sc),
+                           OP::pack(b.x * sc, b.y * sc), OP::pack(b.z * sc, b.w * sc));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -343,14 +371,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // converters run unchanged)
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
-                const uint32_t a0 = pack_bf16(ld[c][0].x, ld[c][0].y);
-                const uint32_t a1 = pack_bf16(ld[c][0].z, ld[c][0].w);
-                const uint32_t b0 = pack_bf16(ld[c][1].x, ld[c][1].y);
-                const uint32_t b1 = pack_bf16(ld[c][1].z, ld[c][1].w);
-                sts_v2(tile + c * kChunkBytes + off_lo, valid ? a0 : 0u, valid ? a1 : 0u);
-                sts_v2(tile + c * kChunkBytes + off_hi, valid ? b0 : 0u, valid ? b1 : 0u);
-                ld[c][0] = ldg_stream_v4(nsrc + 16 * c);
-                ld[c][1] = ldg_stream_v4(nsrc + 16 * c + 8);
+                if constexpr (kWide) {
+                    const uint32_t a0 = OP::pack(ld[c][0].x, ld[c][0].y);
+                    const uint32_t a1 = OP::pack(ld[c][0].z, ld[c][0].w);
+                    const uint32_t b0 = OP::pack(ld[c][1].x, ld[c][1].y);
+                    const uint32_t b1 = OP::pack(ld[c][1].z, ld[c][1].w);
+                    sts_v2(tile + c * kChunkBytes + off_lo, valid ? a0 : 0u, valid ? a1 : 0u);
+                    sts_v2(tile + c * kChunkBytes + off_hi, valid ? b0 : 0u, valid ? b1 : 0u);
+                } else {
+                    const float4 v = ld[c][0];
+                    sts_v4(tile + c * kChunkBytes + off_lo, valid ? __float_as_uint(v.x) : 0u,
+                           valid ? __float_as_uint(v.y) : 0u, valid ? __float_as_uint(v.z) : 0u,
+                           valid ? __float_as_uint(v.w) : 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < kLd; ++i) ld[c][i] = ldg_stream_v4(nsrc + kChunkV4 * c + 8 * i);
                 if (c % kGroupChunks == kGroupChunks - 1) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar + B_CONV + kGroups * slot + c / kGroupChunks);
@@ -367,8 +402,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ============================ MMA issue (1 thread) ============================
         if (lane == 0) {
-            constexpr uint32_t IDESC_QK = idesc_bf16_f32(64, kTile, 0, 0);
-            constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, N, 1, 0);
+            constexpr uint32_t IDESC_QK = idesc_f16kind(64, kTile, 0, 0, !OP::kF16);
+            constexpr uint32_t IDESC_PV = idesc_f16kind(128, N, 1, 0, !OP::kF16);
             uint32_t fph = 0, sph = 0, pph = 0, oph = 0, qph = 0;
             bool ok = true, q_ready = false;
             int qg = 0; // next chunk group of the current QK tile
@@ -396,8 +431,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         const uint64_t vd = smem_desc_sw128(sm_base + LY::TILE + slot * kSlotBytes,
                                                             kChunkBytes, 1024);
-                        const uint64_t pd =
-                            smem_desc_sw128(sm_base + LY::PT + slot * LY::QCH, 16, 1024);
+                        const uint64_t pd = smem_desc_sw128(
+                            sm_base + LY::TILE + slot * kSlotBytes + kPChunk * kChunkBytes, 16, 1024);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -445,7 +480,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         progress = true;
                         if (++qg == kGroups) {
                             qg = 0;
-                            tc_commit(bar + B_SFULL + slot);
+                            // to both CTAs: P overwrites the tile's last chunk only
+                            // once the peer has its copy of this CTA's rows too (the
+                            // peer's QK waited for them), so the outgoing bulk copy
+                            // has read them
+                            tc_commit_mc(bar + B_SFULL + slot, 3);
                             if (qk.t == qk.x.ntiles - 1) {
                                 tc_commit(bar + B_QFREE);
                                 q_ready = false;
@@ -595,7 +634,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ppf ^= 1u << slot;
-                const uint32_t prow = sm_base + LY::PT + slot * LY::QCH;
+                const uint32_t prow = sm_base + LY::TILE + slot * kSlotBytes + kPChunk * kChunkBytes;
                 if (owner) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
@@ -606,7 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const float p1 =
                                 (16 * g + i + 1 < nvalid) ? ex2(sc[16 * g + i + 1] - m) : 0.f;
                             l += p0 + p1;
-                            w[i >> 1] = pack_bf16(p0, p1);
+                            w[i >> 1] = OP::pack(p0, p1);
                         }
                         sts_v4(prow + sw128(h, 32 * g), w[0], w[1], w[2], w[3]);
                         sts_v4(prow + sw128(h, 32 * g + 16), w[4], w[5], w[6], w[7]);
@@ -701,7 +740,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 } // namespace
 
-bool mla_supported_heads(int n_heads) { return n_heads == 32 || n_heads == 64 || n_heads == 96; }
+bool mla_supported_heads(int n_heads)
+{
+    return n_heads == 32 || n_heads == 64 || n_heads == 96 || n_heads == 128;
+}
 
 int mla_smem_bytes(int n_heads)
 {
@@ -709,18 +751,31 @@ int mla_smem_bytes(int n_heads)
     case 32: return Layout<16>::ALLOC;
     case 64: return Layout<32>::ALLOC;
     case 96: return Layout<48>::ALLOC;
+    case 128: return Layout<64>::ALLOC;
     default: return 0;
     }
 }
 
-template <int N> static cudaError_t launch_n(int grid, cudaStream_t st, const MlaParams &p)
+template <int N, typename CT>
+static cudaError_t launch_n(int grid, cudaStream_t st, const MlaParams &p)
 {
-    auto *fn = mla_split_kernel<N>;
+    auto *fn = mla_split_kernel<N, CT>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<N>::ALLOC);
     if (e != cudaSuccess) return e;
     fn<<<grid, kThreads, Layout<N>::ALLOC, st>>>(p);
     return cudaGetLastError();
+}
+
+template <int N> static cudaError_t launch_dt(int kv_dtype, int grid, cudaStream_t st,
+                                             const MlaParams &p)
+{
+    switch (kv_dtype) {
+    case DA_F32: return launch_n<N, float>(grid, st, p);
+    case DA_F16: return launch_n<N, __half>(grid, st, p);
+    case DA_BF16: return launch_n<N, __nv_bfloat16>(grid, st, p);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 // How many of the kernel's 2-CTA clusters the current device holds at once
@@ -732,7 +787,7 @@ template <int N> static int max_clusters_n()
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return 0;
     if (cache[dev] == 0) {
-        auto *fn = mla_split_kernel<N>;
+        auto *fn = mla_split_kernel<N, float>; // the same resources for every cache type
         int n = -1;
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Layout<N>::ALLOC) == cudaSuccess) {
@@ -762,16 +817,18 @@ int mla_max_clusters(int n_heads)
     case 32: return max_clusters_n<16>();
     case 64: return max_clusters_n<32>();
     case 96: return max_clusters_n<48>();
+    case 128: return max_clusters_n<64>();
     default: return 0;
     }
 }
 
-cudaError_t launch_mla_split(int grid, cudaStream_t st, const MlaParams &p)
+cudaError_t launch_mla_split(int grid, cudaStream_t st, const MlaParams &p, int kv_dtype)
 {
     switch (p.n_heads) {
-    case 32: return launch_n<16>(grid, st, p);
-    case 64: return launch_n<32>(grid, st, p);
-    case 96: return launch_n<48>(grid, st, p);
+    case 32: return launch_dt<16>(kv_dtype, grid, st, p);
+    case 64: return launch_dt<32>(kv_dtype, grid, st, p);
+    case 96: return launch_dt<48>(kv_dtype, grid, st, p);
+    case 128: return launch_dt<64>(kv_dtype, grid, st, p);
     default: return cudaErrorInvalidValue;
     }
 }

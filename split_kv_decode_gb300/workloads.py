@@ -25,6 +25,11 @@ The named cases follow the geometries the pages work with:
                    lengths 8192 / 20480 / 61440 / 131072
   * ``ragged_32``  batch 32, 32 / 8 heads, head_dim 128, bf16 KV, lengths
                    uniform in [1024, 131072] from the seed, bf16 output
+Two MLA variants the pages name beside the 96-head f32 cache:
+  * ``mla_128``    128 heads over the same latent ("The Kernel Level", absorbed
+                   MLA decode: one latent for 128 heads)
+  * ``mla_96_f16`` 96 heads over an f16 latent cache ("Attention at 128k" §1:
+                   the reference engine's compressed cache is f16)
 """
 from __future__ import annotations
 
@@ -154,6 +159,16 @@ def named(name: str, *, seed: Optional[int] = None, seq_len: Optional[int] = Non
         return mk(name, batch=1, n_heads=96, n_kv_heads=1, head_dim=576, v_dim=512,
                   seq_lens=[L(seq_len or 131072)], kv_dtype=F32,
                   scale=1.0 / math.sqrt(576.0), seed=s, std=0.5, shared_kv=True)
+    if name == "mla_128":   # the absorbed MLA shape with 128 heads ("The Kernel Level")
+        s = 1239 if seed is None else seed
+        return mk(name, batch=1, n_heads=128, n_kv_heads=1, head_dim=576, v_dim=512,
+                  seq_lens=[L(seq_len or 131072)], kv_dtype=F32,
+                  scale=1.0 / math.sqrt(576.0), seed=s, std=0.5, shared_kv=True)
+    if name == "mla_96_f16":  # the compressed cache in f16 ("Attention at 128k", §1)
+        s = 1240 if seed is None else seed
+        return mk(name, batch=1, n_heads=96, n_kv_heads=1, head_dim=576, v_dim=512,
+                  seq_lens=[L(seq_len or 131072)], kv_dtype=F16,
+                  scale=1.0 / math.sqrt(576.0), seed=s, std=0.5, shared_kv=True)
     if name == "gqa_24x4":
         s = 1237 if seed is None else seed
         return mk(name, batch=4, n_heads=24, n_kv_heads=4, head_dim=256,
@@ -168,4 +183,4 @@ def named(name: str, *, seed: Optional[int] = None, seq_len: Optional[int] = Non
     raise KeyError(name)
 
 
-NAMES = ("gqa_8x2", "gqa_16x4", "mla_96", "gqa_24x4", "ragged_32")
+NAMES = ("gqa_8x2", "gqa_16x4", "mla_96", "gqa_24x4", "ragged_32", "mla_128", "mla_96_f16")

@@ -370,9 +370,10 @@ def check_mla_invariants(a, p, lens, sms):
     assert p.workspace_bytes >= base * a.n_heads * (a.v_dim + 2) * 4
 
 
-@pytest.mark.parametrize("hq", [32, 64, 96])
-def test_mla_plan_one_cluster_per_sm_pair(lib, hq):
-    a = mla_args(hq=hq)
+@pytest.mark.parametrize("hq,dt", [(32, N.DA_F32), (64, N.DA_F32), (96, N.DA_F32),
+                                   (128, N.DA_F32), (96, N.DA_F16), (128, N.DA_BF16)])
+def test_mla_plan_one_cluster_per_sm_pair(lib, hq, dt):
+    a = mla_args(hq=hq, dt=dt)
     rc, p = plan(lib, a, [131072])
     assert rc == 0, lib.decode_attn_last_error()
     check_mla_invariants(a, p, [131072], 152)
@@ -401,9 +402,10 @@ def test_mla_plan_short_context_and_forced_splits(lib):
 
 
 @pytest.mark.parametrize("mutate,msg", [
-    (lambda a: setattr(a, "kv_dtype", N.DA_F16), "f32"),
+    (lambda a: setattr(a, "kv_dtype", N.DA_F16) or setattr(a, "flags", N.DA_FLAG_MLA_SIMT),
+     "f32"),
     (lambda a: setattr(a, "n_heads", 48), "heads"),
-    (lambda a: setattr(a, "n_heads", 128), "heads"),
+    (lambda a: setattr(a, "n_heads", 160), "heads"),
     (lambda a: setattr(a, "k_pos_stride", 575) or setattr(a, "v_pos_stride", 575), "576"),
     (lambda a: setattr(a, "k_pos_stride", 577) or setattr(a, "v_pos_stride", 577), "aligned"),
     (lambda a: setattr(a, "v_pos_stride", 1152), "first 512"),
@@ -618,7 +620,8 @@ def test_plan_multi_token_needs_q_len_positions(lib):
 
 
 @pytest.mark.parametrize("hq,q_len,ok", [(48, 2, True), (16, 4, True), (32, 3, True),
-                                         (16, 6, True), (96, 2, False), (24, 2, False)])
+                                         (16, 6, True), (64, 2, True), (32, 4, True),
+                                         (96, 2, False), (24, 2, False)])
 def test_mla_multi_token_rows(lib, hq, q_len, ok):
     # the rows of an MLA item are (token, head) pairs: 32, 64 or 96 of them
     a = mla_args(hq=hq, cap=4096)

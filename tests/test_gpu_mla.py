@@ -29,9 +29,9 @@ F32_BAR = 2e-4
 BF16_BAR = 5e-3
 
 
-def mla_case(lens, heads=96, seed=2000, cap=None):
+def mla_case(lens, heads=96, seed=2000, cap=None, dtype="f32"):
     return W.make_case("mla", batch=len(lens), n_heads=heads, n_kv_heads=1, head_dim=576,
-                       v_dim=512, seq_lens=lens, kv_dtype="f32", scale=1 / math.sqrt(576.0),
+                       v_dim=512, seq_lens=lens, kv_dtype=dtype, scale=1 / math.sqrt(576.0),
                        seed=seed, std=0.5, shared_kv=True, capacity=cap)
 
 
@@ -233,3 +233,58 @@ def test_mla_padded_latent_rows():
     A.decode_attn_device_status(da.workspace)
     worst, rel = errors(case, out.double().cpu().numpy(), oracle_rows(case))
     assert worst <= F32_BAR, (worst, rel)
+
+
+# ---------------------------------------------------------------------------
+# the other MLA shapes the pages name: 128 heads, and an f16 (or bf16) latent
+# cache, whose stored values are the MMA operands (the 16-bit bar, 5e-3)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("L", [4096, 20000])
+def test_mla_128_heads(L):
+    check(mla_case([L], heads=128, seed=6000 + L), F32_BAR)
+
+
+def test_mla_128_heads_L131072_sampled():
+    case = W.named("mla_128")
+    got, da = run(case)
+    assert da.plan.kernel == N.DA_KERNEL_MLA_TC
+    pairs = sample_pairs(case, per_batch=8, seed=4)
+    worst, rel = errors(case, got, oracle_rows(case, pairs=pairs), pairs)
+    assert worst <= F32_BAR, (worst, rel)
+
+
+def test_mla_128_heads_short_contexts_on_both_kernels():
+    case = mla_case([700, 129], heads=128, seed=6100)
+    check(case, F32_BAR)                                  # the f32 kernel
+    check(case, BF16_BAR, flags=N.DA_FLAG_MLA_TC)         # the tensor cores
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("lens", [[4096], [1, 33, 1000], [20000, 129]])
+def test_mla_16bit_latent_cache(dtype, lens):
+    case = mla_case(lens, heads=96, seed=6200 + len(lens), dtype=dtype)
+    check(case, BF16_BAR)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_mla_16bit_latent_cache_L131072_sampled(dtype):
+    case = W.named("mla_96_f16") if dtype == "f16" else mla_case([131072], dtype="bf16",
+                                                                   seed=6300)
+    got, da = run(case)
+    pairs = sample_pairs(case, per_batch=8, seed=5)
+    worst, rel = errors(case, got, oracle_rows(case, pairs=pairs), pairs)
+    print(f"MLA {dtype} latent L=131072: max|err|/max|V| {worst:.2e}, relL2 {rel:.2e}")
+    assert worst <= BF16_BAR, (worst, rel)
+
+
+def test_mla_16bit_latent_cache_forced_splits_and_128_heads():
+    case = mla_case([3000], heads=128, seed=6400, dtype="f16")
+    for s in (1, 9, 150):
+        check(case, BF16_BAR, force_splits=s)
+
+
+def test_mla_128_rows_as_64_heads_by_2_new_tokens():
+    case = mla_case([5000, 70], heads=64, seed=6500)
+    q4 = W.multi_token_q(2, 2, 64, 576, seed=6501)
+    got = _run_multi(case, q4)
+    assert _multi_errors(case, q4, got) <= F32_BAR
