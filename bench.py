@@ -176,16 +176,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def make_inputs(workload, device, draw_on_device=False):
+def make_inputs(workload, device, draw_on_device=False, scale_lens=1.0):
     """The workload's seeded case on `device`. With several new tokens per
     sequence, case.q is [B, q_len, Hq, Dk]. draw_on_device: draw the caches on
-    `device` (same recipe, other values; for timing only)."""
+    `device` (same recipe, other values; for timing only). scale_lens shrinks
+    every length (a smaller case of the same workload, for profiler captures)."""
     import dataclasses
     from split_kv_decode_gb300 import workloads as W
     name, L = WORKLOADS[workload][:2]
     q_len = WORKLOADS[workload][2] if len(WORKLOADS[workload]) > 2 else 1
     where = str(device) if draw_on_device else "cpu"
-    case = W.named(name, seq_len=L, device=where) if L else W.named(name, device=where)
+    case = (W.named(name, seq_len=L, device=where, scale_lens=scale_lens) if L else
+            W.named(name, device=where, scale_lens=scale_lens))
     if q_len > 1:
         case = dataclasses.replace(case, q=W.multi_token_q(case.batch, q_len, case.n_heads,
                                                            case.head_dim))
@@ -324,6 +326,8 @@ def main():
                     help="skip the e2e and cpu_baseline measurements")
     ap.add_argument("--no-soak", action="store_true",
                     help="skip the clock soak (for profiler runs, which serialise launches)")
+    ap.add_argument("--scale-lens", type=float, default=1.0,
+                    help="shrink every length by this factor (smaller profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -340,7 +344,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
-    case, q, k, v = make_inputs(args.workload, dev)
+    case, q, k, v = make_inputs(args.workload, dev, scale_lens=args.scale_lens)
     out_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[case.out_dtype]
     stream = torch.cuda.current_stream(dev)
 
@@ -414,7 +418,7 @@ def main():
     A.decode_attn_device_status(ws, stream)
 
     step_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(args.steps)]
-    one_us = time_one_launch(case, q, k, v, out_dt, dev, flush, args)
+    one_us = None if args.no_extra else time_one_launch(case, q, k, v, out_dt, dev, flush, args)
     split_us = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in range(args.steps)]
     total_us = max_over_ranks(sum(step_us), dev)
     value = total_us / (args.steps * world)                # µs per layer-step, whole job
