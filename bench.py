@@ -48,6 +48,8 @@ WORKLOADS = {
     "mla96_f16_L131072": ("mla_96_f16", None),
     # four new tokens per sequence on the default cache: 16 query rows per KV head
     "gqa16x4_f16_L151552_q4": ("gqa_16x4", 151552, 4),
+    # two new tokens on the 27B-like f32 cache: 12 rows per KV head (f32 kernel)
+    "gqa24x4_f32_b4_q2": ("gqa_24x4", None, 2),
 }
 DEFAULT = "gqa16x4_f16_L151552"
 METRIC = "decode-attention us/layer-step (and KV GB/s)"   # both arms report this metric
@@ -55,7 +57,8 @@ METRIC = "decode-attention us/layer-step (and KV GB/s)"   # both arms report thi
 KERNEL = {"mla96_f32_L131072": ("mla_split_kernel", "bf16"),
           "mla128_f32_L131072": ("mla_split_kernel", "bf16"),
           "mla96_f16_L131072": ("mla_split_kernel", "f16"),
-          "gqa16x4_f16_L151552_q4": ("gqa_tc_kernel", "f16")}
+          "gqa16x4_f16_L151552_q4": ("gqa_tc_kernel", "f16"),
+          "gqa24x4_f32_b4_q2": ("f32_split_kernel", "f32")}
 DEFAULT_KERNEL = ("gqa_split_kernel", "f32")
 
 
@@ -91,6 +94,7 @@ KERNEL_SOURCES = {
                          "merge.cuh"),
     "gqa_tc_kernel": ("gqa_tc.cu", "gqa_split.cuh", "merge.cuh"),
     "mla_split_kernel": ("mla_split.cu", "merge.cuh"),
+    "f32_split_kernel": ("f32_split.cu",),
 }
 
 
@@ -526,7 +530,7 @@ def time_one_launch(case, q, k, v, out_dt, dev, flush, args):
 CONFIG_SWEEP = ("gqa8x2_f32_L4096", "gqa16x4_f16_L4096", "gqa16x4_f16_L20480",
                 "gqa16x4_f16_L61440", "gqa16x4_f16_L151552", "gqa16x4_f16_L262144",
                 "mla96_f32_L131072", "gqa24x4_f32_b4", "ragged32_bf16", "gqa16x4_f16_L151552_q4",
-                "mla128_f32_L131072", "mla96_f16_L131072")
+                "mla128_f32_L131072", "mla96_f16_L131072", "gqa24x4_f32_b4_q2")
 
 
 def time_split_and_step(workload, dev, steps):
@@ -581,7 +585,8 @@ def time_split_and_step(workload, dev, steps):
     step_us = [x.elapsed_time(y) * 1e3 for x, y in st]
     split_us = [x.elapsed_time(y) * 1e3 for x, y in sp]
     kernel = {N.DA_KERNEL_GQA_TMA: "gqa_split_kernel", N.DA_KERNEL_GQA_TC: "gqa_tc_kernel",
-              N.DA_KERNEL_MLA_TC: "mla_split_kernel"}.get(p0.kernel, str(p0.kernel))
+              N.DA_KERNEL_MLA_TC: "mla_split_kernel",
+              N.DA_KERNEL_GQA_F32: "f32_split_kernel"}.get(p0.kernel, str(p0.kernel))
     res = (case, kernel, step_us, split_us, p0, count_launches(a, p0), one_us)
     del q, k, v, ws, out, flush
     torch.cuda.empty_cache()

@@ -126,6 +126,9 @@ typedef enum {
                                8 to 128 query rows ((n_heads / n_kv_heads) * q_len),
                                f16 or bf16 caches, head_dim 128 or 256; q and the
                                probabilities are rounded to the cache type         */
+#define DA_KERNEL_GQA_F32 4 /* f32 CUDA-core split kernel for GQA/MQA work items of
+                               9 to 128 query rows on an f32 cache, head_dim 128 or
+                               256: one CTA per (item, 32 rows), every operand f32  */
 
 typedef struct {
     int32_t batch;       /* 1 .. DA_MAX_BATCH                                  */

@@ -185,12 +185,20 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
         kc->cluster = 1;
         return DA_OK;
     }
+    // many rows per item on an f32 cache: the f32 CUDA-core kernel (32 rows per CTA)
+    if (a->kv_dtype == DA_F32 && (a->head_dim == 128 || a->head_dim == 256) && G > 8 &&
+        G <= 128) {
+        kc->kernel = DA_KERNEL_GQA_F32;
+        kc->tile = 32;
+        kc->ctas_per_sm = f32_split_ctas_per_sm(a->head_dim);
+        kc->cluster = 1;
+        return DA_OK;
+    }
     GqaConfig cfg;
     if (!gqa_config_any(a->kv_dtype, a->head_dim, G, &cfg))
         return fail(DA_EUNSUPPORTED, "plan",
                     "no GQA kernel for head_dim %d, group %d (heads per KV head x q_len), "
-                    "%s KV (head_dim 128 or 256; group 1 to 8, or 8 to 128 for a 16-bit "
-                    "cache)",
+                    "%s KV (head_dim 128 or 256; group 1 to 128)",
                     a->head_dim, G, dtype_name(a->kv_dtype));
     kc->kernel = DA_KERNEL_GQA_TMA;
     kc->tile = cfg.tile;
@@ -339,6 +347,54 @@ int zero_counters(const da_args_t *a, const da_plan_t *pl, const FusedOut &f, cu
     return DA_OK;
 }
 
+// Parameters of the f32 CUDA-core split kernel (f32 caches only).
+F32Params f32_params(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
+                     const void *v, void *ws, const da_dev_t *dev)
+{
+    F32Params f;
+    std::memset(&f, 0, sizeof f);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    f.q = q;
+    f.k = static_cast<const float *>(k);
+    f.v = static_cast<const float *>(v);
+    f.k_pos_stride = a->k_pos_stride;
+    f.k_head_stride = a->k_head_stride;
+    f.k_batch_stride = a->batch > 1 ? a->k_batch_stride : 0;
+    f.v_pos_stride = a->v_pos_stride;
+    f.v_head_stride = a->v_head_stride;
+    f.v_batch_stride = a->batch > 1 ? a->v_batch_stride : 0;
+    f.ml = reinterpret_cast<float2 *>(w + ws_ml_offset());
+    f.acc = reinterpret_cast<float *>(w + ws_acc_offset(pl->total_splits, rows_of(a)));
+    f.status = reinterpret_cast<int *>(w);
+    f.n_heads = rows_of(a);
+    f.q_len = q_len_of(a);
+    f.hq = a->n_heads;
+    f.scale_log2 = a->scale * 1.4426950408889634f;
+    f.flags = a->flags;
+    f.exact_below = INT32_MAX;
+    f.reset_status = 1;
+    f.items.batch = a->batch;
+    f.items.n_items = pl->n_items;
+    f.items.n_kv_heads = a->n_kv_heads;
+    for (int b = 0; b < a->batch; ++b) {
+        f.items.seq_lens[b] = pl->seq_lens[b];
+        f.items.chunk[b] = pl->chunk[b];
+        f.items.split_base[b] = pl->split_base[b];
+    }
+    f.items.split_base[a->batch] = pl->total_splits;
+    if (dev) {
+        f.dev_lens = dev->seq_lens;
+        if (dev->block_table) {
+            f.block_table = dev->block_table;
+            f.max_blocks = dev->max_blocks_per_seq;
+            f.block_size = dev->block_size;
+            f.k_block_stride = dev->k_block_stride;
+            f.v_block_stride = dev->v_block_stride;
+        }
+    }
+    return f;
+}
+
 int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const void *k,
                const void *v, void *ws, cudaStream_t st, const da_dev_t *dev, void *out,
                bool want_fuse, bool *fused)
@@ -404,11 +460,13 @@ int launch_mla(const da_args_t *a, const da_plan_t *pl, const float *q, const vo
         if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
     }
     if (any_exact) {
-        p.reset_status = any_tc ? 0 : 1;
+        F32Params f = f32_params(a, pl, q, k, k, ws, dev);
+        f.exact_below = p.exact_below;
+        f.reset_status = any_tc ? 0 : 1;
         const int grid = (a->flags & DA_FLAG_TEST_BAD_LAUNCH)
                              ? 0
-                             : pl->n_items * mla_exact_groups(rows_of(a));
-        cudaError_t e = launch_mla_exact(grid, st, p);
+                             : pl->n_items * f32_split_groups(rows_of(a));
+        cudaError_t e = launch_f32_split(576, 512, true, grid, st, f);
         if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
     }
     return DA_OK;
@@ -423,6 +481,15 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     *fused = false;
     if (pl->kernel == DA_KERNEL_MLA_TC)
         return launch_mla(a, pl, q, k, v, ws, st, dev, out, want_fuse, fused);
+    if (pl->kernel == DA_KERNEL_GQA_F32) {
+        const F32Params f = f32_params(a, pl, q, k, v, ws, dev);
+        const int grid = (a->flags & DA_FLAG_TEST_BAD_LAUNCH)
+                             ? 0
+                             : pl->n_items * f32_split_groups(rows_of(a) / a->n_kv_heads);
+        cudaError_t e = launch_f32_split(a->head_dim, a->v_dim, false, grid, st, f);
+        if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
+        return DA_OK;
+    }
     SplitParams p;
     std::memset(&p, 0, sizeof p);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -625,8 +692,10 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
         // rows), one per SM, so the items fill the SMs divided by the groups
         bool all_exact = true;
         for (int b = 0; b < a->batch; ++b) all_exact &= lens[b] < mla_exact_below(a);
-        if (all_exact) slots = std::max(1, num_sms / mla_exact_groups(rows_of(a)));
+        if (all_exact) slots = std::max(1, num_sms / f32_split_groups(rows_of(a)));
     }
+    if (kc.kernel == DA_KERNEL_GQA_F32) // one CTA per (item, group of 32 rows)
+        slots = std::max(1, num_sms * kc.ctas_per_sm / f32_split_groups(rows_of(a) / a->n_kv_heads));
     const int prc = plan_splits(lens, a->batch, a->n_kv_heads, kc.tile, slots, a->force_splits,
                                 1 << 22, &po);
     if (prc == 1) return fail(DA_EINVAL, "plan", "invalid lengths");

@@ -136,10 +136,34 @@ cudaError_t launch_mla_split(int grid, cudaStream_t stream, const MlaParams &p, 
 // 2-CTA clusters of the MLA tensor-core kernel the current device holds at once
 // (0 if unknown): its merge without a combine launch needs every cluster resident.
 int mla_max_clusters(int n_heads);
-// MLA split kernel in f32 on the CUDA cores: one CTA per (work item, group of
-// 32 rows); grid = n_items * mla_exact_groups(rows).
-int mla_exact_groups(int rows);
-cudaError_t launch_mla_exact(int grid, cudaStream_t stream, const MlaParams &p);
+// Split kernel in f32 on the CUDA cores (f32_split.cu): MLA sequences below the
+// exactness threshold, and f32 GQA items of 9-128 rows. One CTA per (work item,
+// group of 32 rows): grid = n_items * f32_split_groups(rows per item).
+struct F32Params {
+    const float *q;          // [B][q_len][hq][DK]
+    const float *k, *v;      // f32 caches; for MLA v == k (values: the first DV columns)
+    int64_t k_pos_stride, k_head_stride, k_batch_stride, k_block_stride; // elements
+    int64_t v_pos_stride, v_head_stride, v_batch_stride, v_block_stride;
+    float2 *ml;
+    float *acc;
+    int *status;
+    int32_t n_heads;         // rows per sequence: q_len * hq
+    int32_t q_len;
+    int32_t hq;
+    float scale_log2;
+    int32_t flags;
+    int32_t exact_below;     // sequences at or past this current length are skipped
+    int32_t reset_status;    // this kernel runs alone in the call: it clears the status word
+    const int32_t *dev_lens;
+    const int32_t *block_table;
+    int32_t max_blocks;
+    int32_t block_size;
+    ItemTable items;
+};
+int f32_split_groups(int rows_per_item);
+int f32_split_ctas_per_sm(int head_dim);
+cudaError_t launch_f32_split(int head_dim, int v_dim, bool shared_kv, int grid,
+                             cudaStream_t stream, const F32Params &p);
 
 struct CombineParams {
     const float2 *ml;

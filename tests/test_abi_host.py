@@ -567,15 +567,31 @@ def test_plan_multi_token_groups(lib, hq, hkv, q_len):
     assert p.kernel == (N.DA_KERNEL_GQA_TC if rows >= 8 else N.DA_KERNEL_GQA_TMA)
 
 
-@pytest.mark.parametrize("hq,hkv,q_len,dt", [(16, 4, 3, N.DA_F32), (8, 2, 4, N.DA_F32),
-                                             (16, 1, 2, N.DA_F32), (64, 1, 4, N.DA_F16),
-                                             (128, 1, 2, N.DA_BF16)])
+@pytest.mark.parametrize("hq,hkv,q_len,dt", [(64, 1, 4, N.DA_F16), (128, 1, 2, N.DA_BF16),
+                                             (64, 1, 3, N.DA_F32)])
 def test_plan_multi_token_rejects_large_groups(lib, hq, hkv, q_len, dt):
+    # more than 128 rows per work item: no kernel holds them
     a = args(hq=hq, hkv=hkv, cap=8192, dt=dt)
     a.q_len = q_len
     rc, _ = plan(lib, a, [8192])
     assert rc == N.DA_EUNSUPPORTED
     assert "q_len" in lib.decode_attn_last_error().decode()
+
+
+@pytest.mark.parametrize("hq,hkv,q_len,d", [(16, 4, 3, 256), (8, 2, 4, 256), (16, 1, 2, 128),
+                                            (24, 4, 2, 256), (32, 1, 1, 128), (64, 2, 4, 128)])
+def test_plan_f32_cache_with_many_rows_takes_the_f32_kernel(lib, hq, hkv, q_len, d):
+    # 9 to 128 rows per item on an f32 cache: one CTA per (item, 32 rows), and
+    # the items fill the SMs divided by the groups of 32 rows
+    a = args(hq=hq, hkv=hkv, d=d, cap=65536, dt=N.DA_F32)
+    a.q_len = q_len
+    rows = hq // hkv * q_len
+    rc, p = plan(lib, a, [65536], 152)
+    assert rc == 0, lib.decode_attn_last_error()
+    assert p.kernel == N.DA_KERNEL_GQA_F32 and p.tile == 32
+    groups = -(-rows // 32)
+    assert p.n_items * groups <= 2 * 152 * p.ctas_per_sm
+    assert p.chunk[0] % 32 == 0
 
 
 @pytest.mark.parametrize("hq,hkv,q_len,d,dt", [(32, 1, 1, 128, N.DA_F16), (16, 4, 4, 256, N.DA_BF16),
