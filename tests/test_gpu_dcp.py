@@ -102,7 +102,7 @@ def test_tensor_core_gqa_context_parallel(world):
     assert np.all(np.isfinite(got)) and worst <= TOL["f16"], (worst, rel)
 
 
-@pytest.mark.parametrize("shape,world", [("simt", 2), ("tc", 3), ("mla", 2)])
+@pytest.mark.parametrize("shape,world", [("simt", 2), ("tc", 3), ("mla", 2), ("f32rows", 3)])
 def test_context_parallel_several_new_tokens(shape, world):
     # the new tokens fall in the last rank's slice; the other ranks' slices lie
     # before them and run without the causal limit (DA_FLAG_NO_CAUSAL)
@@ -116,6 +116,10 @@ def test_context_parallel_several_new_tokens(shape, world):
         case = W.make_case("t", batch=2, n_heads=16, n_kv_heads=4, head_dim=256,
                            seq_lens=[7001, 2999], kv_dtype="f16", scale=1 / 16, seed=751)
         q_len, v_dim, bar = 4, None, TOL["f16"]
+    elif shape == "f32rows":   # 12 rows per KV head on an f32 cache: the f32 kernel
+        case = W.make_case("t", batch=2, n_heads=24, n_kv_heads=4, head_dim=256,
+                           seq_lens=[7001, 2999], kv_dtype="f32", scale=1 / 16, seed=754)
+        q_len, v_dim, bar = 2, None, TOL["f32"]
     else:
         case = W.make_case("t", batch=2, n_heads=8, n_kv_heads=4, head_dim=256,
                            seq_lens=[7001, 2999], kv_dtype="f32", scale=1 / 16, seed=752)

@@ -28,7 +28,8 @@ STEPS = [[2500], [10, 3000, 777], [1, 2, 3, 2999, 1500, 64], [700, 1, 2048, 5, 3
 @pytest.mark.parametrize("hq,hkv,d,dtype,v_dim,mla", [
     (16, 4, 256, "f16", None, False),    # SIMT kernel
     (32, 1, 128, "bf16", None, False),   # tensor-core GQA kernel
-    (32, 1, 576, "f32", 512, True),      # MLA kernel
+    (32, 1, 576, "f32", 512, True),      # MLA kernels (f32 below 2048 positions, tensor cores above)
+    (32, 2, 128, "f32", None, False),    # f32 CUDA-core kernel (16 rows per KV head)
 ])
 def test_bucketed_graph_steps(hq, hkv, d, dtype, v_dim, mla):
     cap = 3000
