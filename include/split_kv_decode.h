@@ -156,8 +156,10 @@ typedef struct {
                             Capstone", Lesson). The rows of a work item are
                             (n_heads / n_kv_heads) * q_len (token, head)
                             pairs: 1 to 8 (SIMT GQA kernel), 8 to 128
-                            (tensor-core GQA kernel, 16-bit caches), or 32, 64
-                            or 96 (MLA). Every seq_len >= q_len; at most 64.  */
+                            (tensor-core GQA kernel, 16-bit caches), 9 to
+                            128 (f32 CUDA-core kernel, f32 caches), or 32,
+                            64, 96 or 128 (MLA). Every seq_len >= q_len; at
+                            most 64.                                          */
 } da_args_t;
 
 /* A host-side plan (plan/run separation): which kernel, how the context is
@@ -216,9 +218,9 @@ int64_t decode_attn_workspace_bytes(const da_plan_t *plan);
  *               one pointer must never serve two devices). Contents need no
  *               initialisation.
  * Validation before any launch: DA_EINVAL / DA_EUNSUPPORTED / DA_ENOSPACE.
- * The MLA kernel (head_dim 576, v_dim 512, one KV head) needs an f32 cache,
- * 32, 64 or 96 query rows (heads x q_len), and k_cache == v_cache; otherwise
- * DA_EUNSUPPORTED.
+ * The MLA shape (head_dim 576, v_dim 512, one KV head) needs an f32, f16 or
+ * bf16 latent cache, 32, 64, 96 or 128 query rows (heads x q_len), and
+ * k_cache == v_cache; otherwise DA_EUNSUPPORTED.
  * A failed launch: DA_ELAUNCH, message names the phase ("split"/"combine").
  * Asynchronous: a timed-out wait inside the kernel is reported later by
  * decode_attn_device_status().
