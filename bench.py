@@ -57,8 +57,7 @@ METRIC = "decode-attention us/layer-step (and KV GB/s)"   # both arms report thi
 KERNEL = {"mla96_f32_L131072": ("mla_split_kernel", "bf16"),
           "mla128_f32_L131072": ("mla_split_kernel", "bf16"),
           "mla96_f16_L131072": ("mla_split_kernel", "f16"),
-          "gqa16x4_f16_L151552_q4": ("gqa_tc_kernel", "f16"),
-          "gqa24x4_f32_b4_q2": ("f32_split_kernel", "f32")}
+          "gqa16x4_f16_L151552_q4": ("gqa_tc_kernel", "f16")}
 DEFAULT_KERNEL = ("gqa_split_kernel", "f32")
 
 
@@ -585,8 +584,7 @@ def time_split_and_step(workload, dev, steps):
     step_us = [x.elapsed_time(y) * 1e3 for x, y in st]
     split_us = [x.elapsed_time(y) * 1e3 for x, y in sp]
     kernel = {N.DA_KERNEL_GQA_TMA: "gqa_split_kernel", N.DA_KERNEL_GQA_TC: "gqa_tc_kernel",
-              N.DA_KERNEL_MLA_TC: "mla_split_kernel",
-              N.DA_KERNEL_GQA_F32: "f32_split_kernel"}.get(p0.kernel, str(p0.kernel))
+              N.DA_KERNEL_MLA_TC: "mla_split_kernel"}.get(p0.kernel, str(p0.kernel))
     res = (case, kernel, step_us, split_us, p0, count_launches(a, p0), one_us)
     del q, k, v, ws, out, flush
     torch.cuda.empty_cache()

@@ -126,9 +126,7 @@ typedef enum {
                                8 to 128 query rows ((n_heads / n_kv_heads) * q_len),
                                f16 or bf16 caches, head_dim 128 or 256; q and the
                                probabilities are rounded to the cache type         */
-#define DA_KERNEL_GQA_F32 4 /* f32 CUDA-core split kernel for GQA/MQA work items of
-                               9 to 128 query rows on an f32 cache, head_dim 128 or
-                               256: one CTA per (item, 32 rows), every operand f32  */
+
 
 typedef struct {
     int32_t batch;       /* 1 .. DA_MAX_BATCH                                  */
@@ -155,11 +153,11 @@ typedef struct {
                             tile of "Decoder Block 6: Online Attention, the
                             Capstone", Lesson). The rows of a work item are
                             (n_heads / n_kv_heads) * q_len (token, head)
-                            pairs: 1 to 8 (SIMT GQA kernel), 8 to 128
-                            (tensor-core GQA kernel, 16-bit caches), 9 to
-                            128 (f32 CUDA-core kernel, f32 caches), or 32,
-                            64, 96 or 128 (MLA). Every seq_len >= q_len; at
-                            most 64.                                          */
+                            pairs: 1 to 8 (SIMT GQA kernel; 9 to 128 on an
+                            f32 cache, cut into row groups of up to 8, one
+                            work item each), 8 to 128 (tensor-core GQA
+                            kernel, 16-bit caches), or 32, 64, 96 or 128
+                            (MLA). Every seq_len >= q_len; at most 64.        */
 } da_args_t;
 
 /* A host-side plan (plan/run separation): which kernel, how the context is

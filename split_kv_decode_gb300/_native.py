@@ -26,7 +26,7 @@ DA_FLAG_ONE_LAUNCH = 0x20
 DA_MLA_EXACT_BELOW = 2048
 DA_FLAG_TEST_NO_TMA = 0x100
 DA_FLAG_TEST_BAD_LAUNCH = 0x200
-DA_KERNEL_GQA_TMA, DA_KERNEL_MLA_TC, DA_KERNEL_GQA_TC, DA_KERNEL_GQA_F32 = 1, 2, 3, 4
+DA_KERNEL_GQA_TMA, DA_KERNEL_MLA_TC, DA_KERNEL_GQA_TC = 1, 2, 3
 
 
 class DaArgs(ctypes.Structure):

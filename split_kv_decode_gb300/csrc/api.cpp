@@ -135,7 +135,29 @@ struct KernelChoice {
     int tile;        // planner quantum: chunks are multiples of it
     int ctas_per_sm;
     int cluster;     // CTAs that share one work item
+    int row_groups = 1; // SIMT GQA kernel: work items per (sequence, KV head, split)
 };
+
+// Rows of a (sequence, KV head) group that one SIMT work item holds when the
+// group has more than 8: the largest divisor of the group's rows up to 8.
+int simt_rows_per_item(int rows)
+{
+    for (int g = 8; g > 1; --g)
+        if (rows % g == 0) return g;
+    return 1;
+}
+
+// Work items per (sequence, KV head, split) on the SIMT kernel: more than one
+// for an f32 cache whose groups hold 9 to 128 rows (16-bit caches take such
+// groups on the tensor cores)
+int simt_row_groups(const da_args_t *a)
+{
+    const int G = a->n_heads / a->n_kv_heads * (a->q_len > 1 ? a->q_len : 1);
+    if (a->kv_dtype == DA_F32 && (a->head_dim == 128 || a->head_dim == 256) && G > 8 &&
+        G <= 128)
+        return G / simt_rows_per_item(G);
+    return 1;
+}
 
 int select_kernel(const da_args_t *a, KernelChoice *kc)
 {
@@ -185,17 +207,13 @@ int select_kernel(const da_args_t *a, KernelChoice *kc)
         kc->cluster = 1;
         return DA_OK;
     }
-    // many rows per item on an f32 cache: the f32 CUDA-core kernel (32 rows per CTA)
-    if (a->kv_dtype == DA_F32 && (a->head_dim == 128 || a->head_dim == 256) && G > 8 &&
-        G <= 128) {
-        kc->kernel = DA_KERNEL_GQA_F32;
-        kc->tile = 32;
-        kc->ctas_per_sm = f32_split_ctas_per_sm(a->head_dim);
-        kc->cluster = 1;
-        return DA_OK;
-    }
+    // more rows per group than the SIMT kernel holds (an f32 cache): the group's
+    // rows are cut into row groups of up to 8, one work item each; the items of a
+    // slice run side by side, so the slice is read from HBM once and from L2 again
+    kc->row_groups = simt_row_groups(a);
+    const int g = G / kc->row_groups;
     GqaConfig cfg;
-    if (!gqa_config_any(a->kv_dtype, a->head_dim, G, &cfg))
+    if (!gqa_config_any(a->kv_dtype, a->head_dim, g, &cfg))
         return fail(DA_EUNSUPPORTED, "plan",
                     "no GQA kernel for head_dim %d, group %d (heads per KV head x q_len), "
                     "%s KV (head_dim 128 or 256; group 1 to 128)",
@@ -305,7 +323,7 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
             pl->split_base[b] != base)
             return fail(DA_EINVAL, "plan", "inconsistent split table at b = %d", b);
         base += pl->n_splits[b];
-        items += (int64_t)pl->n_splits[b] * a->n_kv_heads;
+        items += (int64_t)pl->n_splits[b] * a->n_kv_heads * kc->row_groups;
     }
     if (pl->total_splits != base || pl->n_items != items || pl->grid < kc->cluster ||
         pl->grid > items * kc->cluster || pl->grid % kc->cluster)
@@ -481,15 +499,7 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     *fused = false;
     if (pl->kernel == DA_KERNEL_MLA_TC)
         return launch_mla(a, pl, q, k, v, ws, st, dev, out, want_fuse, fused);
-    if (pl->kernel == DA_KERNEL_GQA_F32) {
-        const F32Params f = f32_params(a, pl, q, k, v, ws, dev);
-        const int grid = (a->flags & DA_FLAG_TEST_BAD_LAUNCH)
-                             ? 0
-                             : pl->n_items * f32_split_groups(rows_of(a) / a->n_kv_heads);
-        cudaError_t e = launch_f32_split(a->head_dim, a->v_dim, false, grid, st, f);
-        if (e != cudaSuccess) return fail(DA_ELAUNCH, "split", "%s", cudaGetErrorString(e));
-        return DA_OK;
-    }
+
     SplitParams p;
     std::memset(&p, 0, sizeof p);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -563,7 +573,8 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
         return DA_OK;
     }
 
-    const int G = a->n_heads / a->n_kv_heads * q_len_of(a);
+    p.items.row_groups = simt_row_groups(a);
+    const int G = a->n_heads / a->n_kv_heads * q_len_of(a) / p.items.row_groups;
     cudaError_t e;
     switch (a->kv_dtype) {
     case DA_F32: e = gqa_launch_f32(a->head_dim, G, split_grid(a, pl), st, m, p); break;
@@ -694,10 +705,9 @@ int decode_attn_plan(const da_args_t *a, const int32_t *lens, int num_sms, da_pl
         for (int b = 0; b < a->batch; ++b) all_exact &= lens[b] < mla_exact_below(a);
         if (all_exact) slots = std::max(1, num_sms / f32_split_groups(rows_of(a)));
     }
-    if (kc.kernel == DA_KERNEL_GQA_F32) // one CTA per (item, group of 32 rows)
-        slots = std::max(1, num_sms * kc.ctas_per_sm / f32_split_groups(rows_of(a) / a->n_kv_heads));
-    const int prc = plan_splits(lens, a->batch, a->n_kv_heads, kc.tile, slots, a->force_splits,
-                                1 << 22, &po);
+
+    const int prc = plan_splits(lens, a->batch, a->n_kv_heads * kc.row_groups, kc.tile, slots,
+                                a->force_splits, 1 << 22, &po);
     if (prc == 1) return fail(DA_EINVAL, "plan", "invalid lengths");
     if (prc == 2) return fail(DA_EUNSUPPORTED, "plan", "too many work items");
     std::memset(plan, 0, sizeof *plan);

@@ -1,8 +1,9 @@
-// Split kernel in f32 on the CUDA cores, for work items with many query rows
-// over an f32 cache, sm_103a.
+// Split kernel in f32 on the CUDA cores, for MLA work items over an f32
+// latent cache, sm_103a.
 //
-// It serves two shapes whose rows outnumber what the warp-per-row SIMT kernel
-// holds in registers:
+// It serves MLA as MQA, whose rows outnumber what the warp-per-row SIMT kernel
+// holds in registers (the template also takes separate K and V caches of one
+// width; the library instantiates the MLA shape only):
 //   * MLA as MQA: every query row attends over one shared 576-wide latent row
 //     per position, and the values are the first 512 columns of the same rows
 //     ("Attention at 128k", §1.1 and §4; "The Kernel Level", absorbed MLA
@@ -13,8 +14,6 @@
 //     sequence when the caller asks for it). The choice is made on the device,
 //     from the same length both kernels read, so a captured launch follows a
 //     context that grows past the threshold.
-//   * GQA/MQA with 9 to 128 rows per work item (heads per KV head x new tokens)
-//     over an f32 cache, where q, K, V and the probabilities stay in f32.
 // Every operand is f32: the scores and the weighted sum carry f32 rounding only.
 //
 // Work split: one CTA per (work item, group of 32 rows); a work item is a
@@ -288,17 +287,10 @@ cudaError_t launch_t(int grid, cudaStream_t st, const F32Params &p)
 
 int f32_split_groups(int rows_per_item) { return (rows_per_item + kRows - 1) / kRows; }
 
-int f32_split_ctas_per_sm(int head_dim)
-{
-    return head_dim == 128 ? 232448 / Shape<128, 128, false>::SMEM : 1;
-}
-
 cudaError_t launch_f32_split(int head_dim, int v_dim, bool shared_kv, int grid, cudaStream_t st,
                              const F32Params &p)
 {
     if (shared_kv && head_dim == 576 && v_dim == 512) return launch_t<576, 512, true>(grid, st, p);
-    if (!shared_kv && head_dim == 256 && v_dim == 256) return launch_t<256, 256, false>(grid, st, p);
-    if (!shared_kv && head_dim == 128 && v_dim == 128) return launch_t<128, 128, false>(grid, st, p);
     return cudaErrorInvalidValue;
 }
 

@@ -158,12 +158,17 @@ __device__ __forceinline__ bool named_bar_or(int id, int threads, bool pred)
     return r != 0;
 }
 
-// item -> (b, kv head, split)
+// item -> (b, kv head, split[, row group]); the row groups of a (b, kv head,
+// split) are consecutive items, so the CTAs that read the same slice run at
+// the same time (the later reads are L2 hits)
 __device__ __forceinline__ void decode_item(const ItemTable &it, int item, int &b, int &kvh,
-                                            int &s)
+                                            int &s, int &rg)
 {
-    const int t = item / it.n_kv_heads;
-    kvh = item - t * it.n_kv_heads;
+    const int rgs = it.row_groups > 1 ? it.row_groups : 1;
+    const int u = item / rgs;
+    rg = item - u * rgs;
+    const int t = u / it.n_kv_heads;
+    kvh = u - t * it.n_kv_heads;
     int lo = 0, hi = it.batch - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -172,6 +177,13 @@ __device__ __forceinline__ void decode_item(const ItemTable &it, int item, int &
     }
     b = lo;
     s = t - it.split_base[lo];
+}
+
+__device__ __forceinline__ void decode_item(const ItemTable &it, int item, int &b, int &kvh,
+                                            int &s)
+{
+    int rg;
+    decode_item(it, item, b, kvh, s, rg);
 }
 
 // the length an item of sequence b attends over: the plan's, or the current
@@ -414,24 +426,29 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     const int tbase = tr_base<K::NVL, LPR / 2>(lane);
     const bool twriter = tr_writer<K::NVL, LPR / 2>(lane);
 
-    // The G rows of an item are (query token, head) pairs: row j is token
-    // j / Gh and head kvh * Gh + j % Gh of that token, Gh = heads per KV head.
-    // Offsets of row j from the (sequence, group) base, in q and workspace rows:
-    const int Gh = G / p.q_len;
-    auto row_off = [&](int j) { return p.q_len == 1 ? j : (j / Gh) * p.hq + j % Gh; };
+    // The rows of a (sequence, KV head) group are (query token, head) pairs:
+    // row jf is token jf / Gh and head kvh * Gh + jf % Gh of that token, Gh =
+    // heads per KV head. A work item holds G of them: rows [rg G, rg G + G) of
+    // its row group rg (all of them when there is one group). Offsets of row jf
+    // from the (sequence, group) base, in q and workspace rows:
+    const int Gh = p.hq / it.n_kv_heads;
+    const int rows_grp = Gh * p.q_len; // rows of a (sequence, KV head) group
+    auto row_off = [&](int jf) { return p.q_len == 1 ? jf : (jf / Gh) * p.hq + jf % Gh; };
     // the token of each (step, row) value this lane writes after the reduce;
-    // constant over the tiles, so the causal test in the tile loop is an add
+    // constant over an item's tiles, so the causal test in the tile loop is an add
     int tok_r[K::R];
+    auto set_tokens = [&](int rg) {
 #pragma unroll
-    for (int r = 0; r < K::R; ++r) tok_r[r] = ((tbase + r) % G) / Gh;
+        for (int r = 0; r < K::R; ++r) tok_r[r] = (rg * G + (tbase + r) % G) / Gh;
+    };
 
     // q for the G rows of an item's group, pre-scaled into log2 units. The
     // next item's q is loaded right after the last tile of the current one,
     // so the load overlaps the merge.
     float q[G][K::EPL];
     auto load_q = [&](int item) {
-        int qb_b, qb_kvh, qb_s;
-        decode_item(it, item, qb_b, qb_kvh, qb_s);
+        int qb_b, qb_kvh, qb_s, qb_rg;
+        decode_item(it, item, qb_b, qb_kvh, qb_s, qb_rg);
         const float *qb = p.q + ((size_t)qb_b * p.n_heads + (size_t)qb_kvh * Gh) * D;
 #pragma unroll
         for (int h = 0; h < G; ++h)
@@ -439,8 +456,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             for (int c = 0; c < K::NCH; ++c)
 #pragma unroll
                 for (int e = 0; e < K::EPC; e += 4) {
-                    float4 x = *reinterpret_cast<const float4 *>(qb + (size_t)row_off(h) * D +
-                                                                 (c * LPR + sub) * K::EPC + e);
+                    float4 x = *reinterpret_cast<const float4 *>(
+                        qb + (size_t)row_off(qb_rg * G + h) * D + (c * LPR + sub) * K::EPC + e);
                     q[h][c * K::EPC + e + 0] = x.x * p.scale_log2;
                     q[h][c * K::EPC + e + 1] = x.y * p.scale_log2;
                     q[h][c * K::EPC + e + 2] = x.z * p.scale_log2;
@@ -452,8 +469,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     int stage = 0;
     uint32_t phase = 0;
     for (int item = blockIdx.x; item < it.n_items; item += gridDim.x) {
-        int b, kvh, s;
-        decode_item(it, item, b, kvh, s);
+        int b, kvh, s, rg;
+        decode_item(it, item, b, kvh, s, rg);
+        set_tokens(rg);
+        const int jg = rg * G; // the item's first row of its (sequence, KV head) group
         const int p0 = s * it.chunk[b];
         const int Lb = item_len(p, b);
         const int p1 = min(Lb, p0 + it.chunk[b]); // p1 <= p0: an empty item
@@ -717,13 +736,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                     for (int c = 0; c < K::NCH; ++c)
 #pragma unroll
                         for (int e = 0; e < K::EPC; e += 4)
-                            *reinterpret_cast<float4 *>(dst + (size_t)row_off(h) * D +
+                            *reinterpret_cast<float4 *>(dst + (size_t)row_off(jg + h) * D +
                                                         (c * LPR + sub) * K::EPC + e) =
                                 make_float4(acc[h][c * K::EPC + e], acc[h][c * K::EPC + e + 1],
                                             acc[h][c * K::EPC + e + 2], acc[h][c * K::EPC + e + 3]);
             }
             if (lane < G)
-                p.ml[row0 + row_off(lane)] = make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
+                p.ml[row0 + row_off(jg + lane)] =
+                    make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
         }
         if (p.fused.on) {
             // The last partial of this (sequence, KV head) group to arrive merges
@@ -734,7 +754,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) {
-                    const uint32_t n = (uint32_t)(it.split_base[b + 1] - it.split_base[b]);
+                    const int rgs = it.row_groups > 1 ? it.row_groups : 1;
+                    const uint32_t n = (uint32_t)((it.split_base[b + 1] - it.split_base[b]) * rgs);
                     const bool last = arrive(p.fused.ctr + (size_t)b * it.n_kv_heads + kvh) == n;
                     if (last) __threadfence(); // the other partials, before they are read
                     *last_flag = last ? 1 : 0;
@@ -744,7 +765,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             if (*last_flag) {
                 constexpr int NB = (D + 127) / 128; // 128-column blocks of a row
                 const int S = it.split_base[b + 1] - it.split_base[b];
-                for (int u = warp; u < G * NB; u += NCW) {
+                for (int u = warp; u < rows_grp * NB; u += NCW) {
                     const int row = kvh * Gh + row_off(u / NB);
                     warp_merge_row(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D,
                                    (u % NB) * 128, out_row_ptr(p.fused, b, p.n_heads, row, D),

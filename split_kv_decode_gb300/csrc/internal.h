@@ -64,6 +64,8 @@ struct ItemTable {
     int32_t batch;
     int32_t n_items;
     int32_t n_kv_heads;
+    int32_t row_groups;      // SIMT GQA kernel: the rows of a (sequence, KV head, split)
+                             // are cut into this many groups, one work item each (1 elsewhere)
     int32_t seq_lens[DA_MAX_BATCH];
     int32_t chunk[DA_MAX_BATCH];
     int32_t split_base[DA_MAX_BATCH + 1];
@@ -137,8 +139,8 @@ cudaError_t launch_mla_split(int grid, cudaStream_t stream, const MlaParams &p, 
 // (0 if unknown): its merge without a combine launch needs every cluster resident.
 int mla_max_clusters(int n_heads);
 // Split kernel in f32 on the CUDA cores (f32_split.cu): MLA sequences below the
-// exactness threshold, and f32 GQA items of 9-128 rows. One CTA per (work item,
-// group of 32 rows): grid = n_items * f32_split_groups(rows per item).
+// exactness threshold. One CTA per (work item, group of 32 rows): grid =
+// n_items * f32_split_groups(rows per item).
 struct F32Params {
     const float *q;          // [B][q_len][hq][DK]
     const float *k, *v;      // f32 caches; for MLA v == k (values: the first DV columns)
@@ -161,7 +163,6 @@ struct F32Params {
     ItemTable items;
 };
 int f32_split_groups(int rows_per_item);
-int f32_split_ctas_per_sm(int head_dim);
 cudaError_t launch_f32_split(int head_dim, int v_dim, bool shared_kv, int grid,
                              cudaStream_t stream, const F32Params &p);
 

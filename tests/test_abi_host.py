@@ -578,20 +578,22 @@ def test_plan_multi_token_rejects_large_groups(lib, hq, hkv, q_len, dt):
     assert "q_len" in lib.decode_attn_last_error().decode()
 
 
-@pytest.mark.parametrize("hq,hkv,q_len,d", [(16, 4, 3, 256), (8, 2, 4, 256), (16, 1, 2, 128),
-                                            (24, 4, 2, 256), (32, 1, 1, 128), (64, 2, 4, 128)])
-def test_plan_f32_cache_with_many_rows_takes_the_f32_kernel(lib, hq, hkv, q_len, d):
-    # 9 to 128 rows per item on an f32 cache: one CTA per (item, 32 rows), and
-    # the items fill the SMs divided by the groups of 32 rows
+@pytest.mark.parametrize("hq,hkv,q_len,d,per", [(16, 4, 3, 256, 6), (8, 2, 4, 256, 8),
+                                                (16, 1, 2, 128, 8), (24, 4, 2, 256, 6),
+                                                (32, 1, 1, 128, 8), (64, 2, 4, 128, 8),
+                                                (11, 1, 1, 128, 1), (27, 1, 1, 256, 3)])
+def test_plan_f32_cache_with_many_rows_takes_simt_row_groups(lib, hq, hkv, q_len, d, per):
+    # 9 to 128 rows per (sequence, KV head) on an f32 cache: the SIMT kernel
+    # with the rows cut into groups of the largest divisor up to 8, one work
+    # item per (sequence, KV head, split, row group)
     a = args(hq=hq, hkv=hkv, d=d, cap=65536, dt=N.DA_F32)
     a.q_len = q_len
     rows = hq // hkv * q_len
     rc, p = plan(lib, a, [65536], 152)
     assert rc == 0, lib.decode_attn_last_error()
-    assert p.kernel == N.DA_KERNEL_GQA_F32 and p.tile == 32
-    groups = -(-rows // 32)
-    assert p.n_items * groups <= 2 * 152 * p.ctas_per_sm
-    assert p.chunk[0] % 32 == 0
+    assert p.kernel == N.DA_KERNEL_GQA_TMA
+    assert p.n_items == p.total_splits * hkv * (rows // per)
+    assert p.chunk[0] % p.tile == 0
 
 
 @pytest.mark.parametrize("hq,hkv,q_len,d,dt", [(32, 1, 1, 128, N.DA_F16), (16, 4, 4, 256, N.DA_BF16),

@@ -1,9 +1,10 @@
-"""GPU parity of the f32 CUDA-core split kernel (DA_KERNEL_GQA_F32) on GQA/MQA
-work items of 9 to 128 rows over an f32 cache: large head groups, or several
-new tokens per group ("Decoder Block 6: Online Attention, the Capstone",
-Lesson: a tile of query rows consumes each K/V tile once). Every operand stays
-in f32, so every case is held to the f32 bar, 2e-4 of max|V|, against the
-oracle."""
+"""GPU parity of GQA/MQA over an f32 cache with 9 to 128 rows per (sequence,
+KV head): large head groups, or several new tokens per group ("Decoder Block 6:
+Online Attention, the Capstone", Lesson: a tile of query rows consumes each K/V
+tile once). The SIMT kernel takes them with the rows cut into row groups of up
+to 8, one work item each, side by side on the same K/V slice. Every operand
+stays in f32, so every case is held to the f32 bar, 2e-4 of max|V|, against the
+oracle, and the one-token cases to what f32 arithmetic gives."""
 import math
 
 import numpy as np
@@ -28,11 +29,11 @@ def case_of(hq, hkv, d, lens, seed, cap=None, layout_seed=None):
 
 
 @pytest.mark.parametrize("hq,hkv,d", [(32, 1, 128), (24, 2, 256), (64, 4, 128), (128, 1, 128),
-                                      (12, 1, 256)])
+                                      (12, 1, 256), (11, 1, 128), (27, 1, 256)])
 def test_one_token_large_groups(hq, hkv, d):
     case = case_of(hq, hkv, d, [1, 33, 2047, 9000], seed=9100 + hq + d)
     got, da = run(case, poison_ws=True)
-    assert da.plan.kernel == N.DA_KERNEL_GQA_F32
+    assert da.plan.kernel == N.DA_KERNEL_GQA_TMA
     worst, rel = errors(case, got, oracle_rows(case))
     assert worst <= TOL["f32"], (worst, rel)
     # f32 arithmetic throughout: far inside the bar (f32 rounding of the sums
@@ -46,7 +47,7 @@ def test_several_new_tokens(hq, hkv, q_len, d):
     case = case_of(hq, hkv, d, [q_len, 70, 3001], seed=9200 + hq + q_len)
     q4 = W.multi_token_q(case.batch, q_len, hq, d, seed=9201)
     got, da = run_multi(case, q4)
-    assert da.plan.kernel == N.DA_KERNEL_GQA_F32
+    assert da.plan.kernel == N.DA_KERNEL_GQA_TMA
     assert compare(case, q4, got) <= TOL["f32"]
 
 
@@ -67,7 +68,7 @@ def test_head_major_cache_and_device_lengths():
     vh = v.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
     a = A.make_args(q, kh, vh, case.scale)
     p = A.decode_attn_plan(a, [5000, 600])
-    assert p.kernel == N.DA_KERNEL_GQA_F32
+    assert p.kernel == N.DA_KERNEL_GQA_TMA
     ws = A.new_workspace(p)
     out = torch.empty(2, 32, 128, device="cuda")
     now = [4321, 17]
@@ -99,7 +100,7 @@ def test_paged_pool():
     kpd, vpd = kp.cuda(), vp.cuda()
     a = A.make_paged_args(q, kpd, vpd, case.scale, nb)
     p = A.decode_attn_plan(a, [3000, 129])
-    assert p.kernel == N.DA_KERNEL_GQA_F32
+    assert p.kernel == N.DA_KERNEL_GQA_TMA
     ws = A.new_workspace(p)
     out = torch.empty(2, 16, 256, device="cuda")
     d = A.make_dev(block_table=table.cuda(), k_pool=kpd, v_pool=vpd)
@@ -115,6 +116,17 @@ def test_long_context_sampled():
     case = W.named("gqa_24x4", scale_lens=0.5)
     q4 = W.multi_token_q(case.batch, 2, 24, 256, seed=9601)
     got, da = run_multi(case, q4)
-    assert da.plan.kernel == N.DA_KERNEL_GQA_F32
+    assert da.plan.kernel == N.DA_KERNEL_GQA_TMA
     pairs = [(b, h) for b in range(case.batch) for h in (0, 11, 23)]
     assert compare(case, q4, got, pairs=pairs) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("hq,hkv,splits", [(24, 2, 0), (32, 1, 5), (12, 1, 1)])
+def test_one_launch_counts_every_row_group(hq, hkv, splits):
+    # in one launch the last of a group's (split, row group) partials merges the
+    # group, so the arrival count spans the row groups too
+    case = case_of(hq, hkv, 256, [4000, 9, 20000], seed=9700 + hq)
+    got, da = run(case, flags=N.DA_FLAG_ONE_LAUNCH, force_splits=splits, poison_ws=True)
+    assert da.plan.kernel == N.DA_KERNEL_GQA_TMA
+    worst, rel = errors(case, got, oracle_rows(case))
+    assert worst <= F32_EXACT, (worst, rel)
