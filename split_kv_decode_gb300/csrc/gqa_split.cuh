@@ -243,6 +243,7 @@ template <typename DT, int D, int G, int T, int NCW, int NST, int LPR> struct Gq
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(WARP_SCR % 4 == 0 && NV % 4 == 0, "16-byte aligned per-warp scratch");
     static_assert(TILE_BYTES % 128 == 0, "TMA destination alignment");
+    static_assert(NCW * G * D * 4 <= NST * STAGE_BYTES, "flat merge slots in the stage ring");
 };
 
 template <typename DT, int D, int G, int T, int NCW, int NST, int LPR>
@@ -263,7 +264,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     const int lane = threadIdx.x & 31;
     const ItemTable &it = p.items;
 
-    if (threadIdx.x == 0) {
+    // The producer sets the stage barriers up and goes straight on to its first
+    // copies; the consumers wait for the set-up on named barrier 2 (after loading
+    // their first q), so the copies start without a CTA-wide barrier in front.
+    if (warp == NCW && lane == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, NCW);
@@ -272,9 +276,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
         if (blockIdx.x == 0) *p.status = 0;
         fence_mbar_init();
     }
-    __syncthreads();
 
     if (warp == NCW) {
+        __syncwarp();
+        named_bar_arrive(2, K::CONSUMERS + 32);
         // ------------------------------- producer -------------------------------
         // Lane 0 waits on the stage barriers and issues the copies. For paged
         // caches the whole warp walks the items and tiles: the lanes hold a
@@ -465,6 +470,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                 }
     };
     if (blockIdx.x < it.n_items) load_q(blockIdx.x);
+    named_bar_sync(2, K::CONSUMERS + 32); // the producer's barrier set-up
 
     int stage = 0;
     uint32_t phase = 0;
@@ -689,8 +695,49 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
 #pragma unroll
                 for (int e = 0; e < K::EPL; ++e) acc[h][e] *= f;
             }
-            // ... and a pairwise tree in a fixed order sums the warps into warp 0,
-            // so the merged partial does not depend on timing (bit-reproducible)
+            // ... and the warps are summed in a fixed order, so the merged partial
+            // does not depend on timing (bit-reproducible). A CTA's last item finds
+            // the stage ring idle (every copy has landed and been consumed): all
+            // warps store their acc there and every consumer thread sums one
+            // float4 of the item over the warps and writes it. Earlier items,
+            // whose next tiles may be landing in the ring, sum through a pairwise
+            // tree of slots into warp 0, which writes the partial.
+        }
+        const size_t slot_id = (size_t)it.split_base[b] + s;
+        const size_t row0 = slot_id * p.n_heads + (size_t)kvh * Gh;
+        if (item + (int)gridDim.x >= it.n_items) {
+            float *flat = reinterpret_cast<float *>(smem);
+            if (half == 0) {
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int c = 0; c < K::NCH; ++c)
+#pragma unroll
+                        for (int e = 0; e < K::EPC; e += 4)
+                            *reinterpret_cast<float4 *>(flat + (warp * G + h) * D +
+                                                        (c * LPR + sub) * K::EPC + e) =
+                                make_float4(acc[h][c * K::EPC + e], acc[h][c * K::EPC + e + 1],
+                                            acc[h][c * K::EPC + e + 2], acc[h][c * K::EPC + e + 3]);
+            }
+            named_bar_sync(1, K::CONSUMERS);
+            const float4 *flat4 = reinterpret_cast<const float4 *>(flat);
+            for (int i = threadIdx.x; i < G * D / 4; i += K::CONSUMERS) {
+                float4 y = flat4[i];
+#pragma unroll
+                for (int w = 1; w < NCW; ++w) {
+                    const float4 z = flat4[w * (G * D / 4) + i];
+                    y.x += z.x;
+                    y.y += z.y;
+                    y.z += z.z;
+                    y.w += z.w;
+                }
+                const int h = i / (D / 4);
+                *reinterpret_cast<float4 *>(p.acc + (row0 + row_off(jg + h)) * D +
+                                            (i - h * (D / 4)) * 4) = y;
+            }
+            if (warp == 0 && lane < G)
+                p.ml[row0 + row_off(jg + lane)] = make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
+        } else {
 #pragma unroll
             for (int d = 1, lvl = 0; d < NCW; d *= 2, ++lvl) {
                 float *set = sm_tree + ((lvl & 1) ? K::TREE_EVEN : 0) * G * D;
@@ -723,36 +770,34 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
                             }
                 }
             }
-        }
-        // warp 0 writes the partial: acc from its registers, (m, l) per head
-        if (warp == 0) {
-            const size_t slot_id = (size_t)it.split_base[b] + s;
-            const size_t row0 = slot_id * p.n_heads + (size_t)kvh * Gh;
-            if (half == 0) {
-                float *dst = p.acc + row0 * D;
+            // warp 0 writes the partial: acc from its registers, (m, l) per head
+            if (warp == 0) {
+                if (half == 0) {
+                    float *dst = p.acc + row0 * D;
 #pragma unroll
-                for (int h = 0; h < G; ++h)
+                    for (int h = 0; h < G; ++h)
 #pragma unroll
-                    for (int c = 0; c < K::NCH; ++c)
+                        for (int c = 0; c < K::NCH; ++c)
 #pragma unroll
-                        for (int e = 0; e < K::EPC; e += 4)
-                            *reinterpret_cast<float4 *>(dst + (size_t)row_off(jg + h) * D +
-                                                        (c * LPR + sub) * K::EPC + e) =
-                                make_float4(acc[h][c * K::EPC + e], acc[h][c * K::EPC + e + 1],
-                                            acc[h][c * K::EPC + e + 2], acc[h][c * K::EPC + e + 3]);
+                            for (int e = 0; e < K::EPC; e += 4)
+                                *reinterpret_cast<float4 *>(dst + (size_t)row_off(jg + h) * D +
+                                                            (c * LPR + sub) * K::EPC + e) =
+                                    make_float4(acc[h][c * K::EPC + e], acc[h][c * K::EPC + e + 1],
+                                                acc[h][c * K::EPC + e + 2], acc[h][c * K::EPC + e + 3]);
+                }
+                if (lane < G)
+                    p.ml[row0 + row_off(jg + lane)] =
+                        make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
             }
-            if (lane < G)
-                p.ml[row0 + row_off(jg + lane)] =
-                    make_float2(Lh > 0.f ? Mh * kLn2 : kNeutralM, Lh);
         }
         if (p.fused.on) {
             // The last partial of this (sequence, KV head) group to arrive merges
             // the group's rows into out, so no combine launch is needed. Warp 0
             // publishes its partial before the arrival is counted.
             volatile int *last_flag = abort_flag + 1; // the header's spare word
+            __threadfence(); // this thread's share of the partial, before the arrival
+            named_bar_sync(1, K::CONSUMERS);
             if (warp == 0) {
-                __threadfence();
-                __syncwarp();
                 if (lane == 0) {
                     const int rgs = it.row_groups > 1 ? it.row_groups : 1;
                     const uint32_t n = (uint32_t)((it.split_base[b + 1] - it.split_base[b]) * rgs);

@@ -152,6 +152,13 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// arrive on a named barrier without waiting for it (the waiting side uses
+// named_bar_sync with the same thread count)
+__device__ __forceinline__ void named_bar_arrive(int id, int threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ void griddep_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
