@@ -12,7 +12,8 @@ geometry at its rung nearest 128k; 620.8 MB of K+V per step).
 Timing: W untimed warm-up steps (plus a short soak so the clocks settle);
 then K steps, each bracketed by CUDA events on the launching stream around
 its launches (the step's host plan is made first, while the L2 flush -- a
-write of 2 x L2 bytes between steps, outside the events -- runs on the
+write of 2 x L2 bytes, then a read of 2 x L2 bytes so that the write's dirty
+lines are written back before the step, all outside the events -- runs on the
 GPU); barrier + synchronize on both sides; max over ranks. The default run
 adds `configs`: the same measurement, over 100 steps, for every workload of
 the pages' configurations. `--impl reference` times the double-precision CPU
@@ -315,7 +316,7 @@ def workload_config(workload, case):
             "q_len": int(case.q.shape[1]) if case.q.dim() == 4 else 1,
             "kv_dtype": case.kv_dtype, "q_dtype": "f32", "out_dtype": case.out_dtype,
             "kv_bytes_per_step": case.kv_bytes, "parallelism": "replicas",
-            "l2": "flushed between steps (2 x L2 write, outside the events)"}
+            "l2": "flushed between steps (2 x L2 write, then 2 x L2 read so no dirty line of the flush is written back in the step; outside the events)"}
 
 
 def main():
@@ -361,8 +362,7 @@ def main():
     ws = torch.empty(A.decode_attn_workspace_bytes(plan), dtype=torch.uint8, device=dev)
     out = torch.empty(out_shape(case), dtype=out_dt, device=dev)
     lens = case.seq_lens.tolist()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     launches = count_launches(a_step, plan)
 
     def make_plan():
@@ -398,7 +398,7 @@ def main():
         # each step plans on the host while the flush runs on the GPU, so the
         # events bracket the device work of the step, not host scheduling
         p = make_plan()
-        flush.fill_(float(i))
+        flush(i)
         ev[i][0].record(stream)
         run_step(p)
         ev[i][1].record(stream)
@@ -409,7 +409,7 @@ def main():
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
         p = make_plan()
-        flush.fill_(float(i))
+        flush(i)
         evs[i][0].record(stream)
         split(p)
         evs[i][1].record(stream)
@@ -423,15 +423,17 @@ def main():
     step_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(args.steps)]
     one_us = None if args.no_extra else time_one_launch(case, q, k, v, out_dt, dev, flush, args)
     split_us = [evs[i][0].elapsed_time(evs[i][1]) * 1e3 for i in range(args.steps)]
-    total_us = max_over_ranks(sum(step_us), dev)
-    value = total_us / (args.steps * world)                # µs per layer-step, whole job
+    # value: the median step (max over ranks), which a few steps slowed by the
+    # clock sampler's queries do not move; the mean and every step beside it
+    value = max_over_ranks(statistics.median(step_us), dev)
+    step_mean = max_over_ranks(statistics.mean(step_us), dev)
     split_mean = statistics.mean(split_us)
     peak, peak_src = load_peaks()
     # the dominant kernel: the split kernel (with one launch per step, the step
     # itself)
     kernel_us = statistics.mean(step_us) if launches == 1 else split_mean
     achieved = case.kv_bytes / (kernel_us * 1e-6) / 1e9
-    kv_gbs_step = case.kv_bytes / (statistics.mean(step_us) * 1e-6) / 1e9
+    kv_gbs_step = case.kv_bytes / (value * 1e-6) / 1e9
     kernel, arith = KERNEL.get(args.workload, DEFAULT_KERNEL)
 
     line = {
@@ -442,7 +444,9 @@ def main():
         "config": workload_config(args.workload, case),
         "kv_gbs": round(kv_gbs_step, 1),
         "hbm_frac_of_8tbs": round(kv_gbs_step / 8000.0, 4),
-        "step_us_median": round(statistics.median(step_us), 2),
+        "value_statistic": "median of the timed steps (max over ranks)",
+        "step_us_mean": round(step_mean, 2),
+        "step_us_all": [round(x, 1) for x in step_us[:64]],
         "launches_per_step": launches,
         "one_launch_step_us_median": one_us,
         "split_only_us_median": round(statistics.median(split_us), 2),
@@ -550,15 +554,14 @@ def time_split_and_step(workload, dev, steps):
     p0 = A.decode_attn_plan(a, lens)
     ws = torch.empty(A.decode_attn_workspace_bytes(p0), dtype=torch.uint8, device=dev)
     out = torch.empty(out_shape(case), dtype=out_dt, device=dev)
-    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4 + 1024,
-                        dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     for _ in range(3):
         A.decode_attn_splitk_ex(a, A.decode_attn_plan(a, lens), q, k, v, out, ws, stream)
     torch.cuda.synchronize()
     st, sp = [], []
     for i in range(steps):
         p = A.decode_attn_plan(a, lens)
-        flush.fill_(float(i))
+        flush(i)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         e[0].record(stream)
         A.decode_attn_splitk_ex(a, p, q, k, v, out, ws, stream)
@@ -566,7 +569,7 @@ def time_split_and_step(workload, dev, steps):
         st.append(e)
     for i in range(steps):
         p = A.decode_attn_plan(a_split, lens)
-        flush.fill_(float(i))
+        flush(i)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         e[0].record(stream)
         A.decode_attn_splitk_ex(a_split, p, q, k, v, out, ws, stream)
@@ -615,12 +618,33 @@ def measure_configs(dev, peak, steps=100):
     return res
 
 
+class L2Flush:
+    """The L2 flush between timed steps: a write of a buffer twice the L2's size,
+    then a read of another such buffer. The read evicts the lines the write left
+    dirty, so their write-back to HBM happens here and not inside the next timed
+    step: the timed work starts on an L2 of clean, unrelated lines (the state a
+    profiler's cache control gives, and the one a decode step meets after kernels
+    that mostly read weights). None of the step's inputs is in L2 either way."""
+
+    def __init__(self, dev):
+        import torch
+        n = 2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4 + 1024
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.ones(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self, i):
+        import torch
+        self.w.fill_(float(i))
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
 def _timed_steps(launch, flush, steps, stream):
     """Median CUDA-event time (us) of `launch` over `steps` runs, L2 flushed before each."""
     import torch
     ts = []
     for i in range(steps):
-        flush.fill_(float(i))
+        flush(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         launch()
@@ -811,10 +835,10 @@ def read_probe(dev, stream, nbytes):
     import torch
     x = torch.ones(nbytes // 2, dtype=torch.float16, device=dev)
     y = torch.empty_like(x)
-    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size // 4, device=dev)
+    flush = L2Flush(dev)
     ts = []
     for i in range(13):
-        flush.fill_(float(i))
+        flush(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         y.copy_(x)
