@@ -556,7 +556,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (tc_bar_or(!okw)) break;
             oph ^= 1u;
             tc_fence_after();
-            const size_t base = slot_id * p.n_heads + (size_t)kvh * Gh;
+            // each row's partial row, from its owner thread (the scratch of the
+            // rescale factors is free here), so the store loop has no division
+            int *wrow_sm = reinterpret_cast<int *>(alpha_sm);
+            wrow_sm[r] = owner ? (int)wrow : 0;
+            named_bar_sync(1, 128);
             for (int j = 0; j < NBLK; ++j)
                 for (int g16 = 0; g16 < L.npv / 16; ++g16) {
                     float o[16];
@@ -565,13 +569,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int rr = 16 * g16 + i;
-                        if (rr < R) {
-                            const int tk = rr / Gh;
-                            const size_t wr = base + (size_t)tk * p.hq + (rr - tk * Gh);
-                            p.acc[wr * D + 128 * j + r] = o[i];
-                        }
+                        if (rr < R) p.acc[(size_t)wrow_sm[rr] * D + 128 * j + r] = o[i];
                     }
                 }
+            named_bar_sync(1, 128); // the table is read before the scratch is reused
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar + TB_OFREE);
