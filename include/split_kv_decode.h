@@ -79,16 +79,23 @@ typedef enum {
                                     kernel, whose operands are bf16 (see
                                     DA_MLA_EXACT_BELOW)                              */
 #define DA_FLAG_ONE_LAUNCH 0x20  /* the split kernel merges its own partials (no
-                                    combine launch): the last split of a (sequence,
-                                    KV head) group to finish merges the group (GQA
-                                    kernels), or the CTAs merge shares of the rows
-                                    once all have finished (MLA tensor-core kernel,
-                                    when the GPU holds all its clusters at once); a
-                                    memset of the workspace's arrival counters
-                                    precedes the launch. Measured slower than the
-                                    default two launches on GB300 (the merge runs in
-                                    one CTA per group instead of hundreds), so it is
-                                    an option, not the default                     */
+                                    combine launch). SIMT GQA kernel: once a CTA
+                                    has written all its items, each item merges a
+                                    share of its (sequence, KV head) group after
+                                    waiting for the group's last arrival (only when
+                                    the plan's grid is resident at once, else the
+                                    combine launch merges); tensor-core GQA kernel:
+                                    the last split of a group to finish merges it;
+                                    MLA tensor-core kernel: the CTAs merge shares of
+                                    the rows once all have finished (when the GPU
+                                    holds all its clusters at once). A memset of the
+                                    workspace's arrival counters precedes the
+                                    launch. The waits assume the launch is not
+                                    sharing the SMs with kernels of other streams;
+                                    if it is, they may run out (DA_ETIMEOUT in the
+                                    status word). Measured on GB300 within -1 to
+                                    +5 us of the default two launches, so it is an
+                                    option, not the default                       */
 #define DA_FLAG_TEST_NO_TMA 0x100 /* test hook: the producer issues no copy, so every
                                      consumer wait runs out after timeout_us and the
                                      kernel reports DA_ETIMEOUT through device_status */

@@ -336,6 +336,18 @@ int check_plan(const da_args_t *a, const da_plan_t *pl, KernelChoice *kc)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// SMs of the current device (0 if the query fails)
+int device_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 // the split kernel's grid; the test hook DA_FLAG_TEST_BAD_LAUNCH asks for an
 // empty one, which the runtime refuses before anything runs
 int split_grid(const da_args_t *a, const da_plan_t *pl)
@@ -522,10 +534,15 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
         p.items.split_base[b] = pl->split_base[b];
     }
     p.items.split_base[a->batch] = pl->total_splits;
+    const bool tc = pl->kernel == DA_KERNEL_GQA_TC;
+    // The SIMT kernel merges with every CTA of the launch waiting for its groups,
+    // so it fuses only when the whole grid is resident at once (the plan's CTAs
+    // per SM on this device's SMs); otherwise the combine launch merges.
+    const bool fuse = want_fuse && (tc || pl->grid <= device_sms() * pl->ctas_per_sm);
     p.fused = fused_out(a, pl, ws, out);
-    p.fused.on = want_fuse;
-    *fused = want_fuse;
-    if (want_fuse) {
+    p.fused.on = fuse;
+    *fused = fuse;
+    if (fuse) {
         const int rc = zero_counters(a, pl, p.fused, st);
         if (rc) return rc;
     }
@@ -533,7 +550,6 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     GqaMaps m;
     std::memset(&m, 0, sizeof m);
     int rc;
-    const bool tc = pl->kernel == DA_KERNEL_GQA_TC;
     if (dev && dev->block_table) {
         p.block_table = dev->block_table;
         p.max_blocks = dev->max_blocks_per_seq;

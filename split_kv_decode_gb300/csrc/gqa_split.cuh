@@ -791,32 +791,59 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             }
         }
         if (p.fused.on) {
-            // The last partial of this (sequence, KV head) group to arrive merges
-            // the group's rows into out, so no combine launch is needed. Warp 0
-            // publishes its partial before the arrival is counted.
-            volatile int *last_flag = abort_flag + 1; // the header's spare word
-            __threadfence(); // this thread's share of the partial, before the arrival
+            // the merge without a combine launch: every writer publishes its share
+            // of the partial, then one arrival on the group's counter
+            __threadfence();
             named_bar_sync(1, K::CONSUMERS);
-            if (warp == 0) {
-                if (lane == 0) {
-                    const int rgs = it.row_groups > 1 ? it.row_groups : 1;
-                    const uint32_t n = (uint32_t)((it.split_base[b + 1] - it.split_base[b]) * rgs);
-                    const bool last = arrive(p.fused.ctr + (size_t)b * it.n_kv_heads + kvh) == n;
-                    if (last) __threadfence(); // the other partials, before they are read
-                    *last_flag = last ? 1 : 0;
+            if (threadIdx.x == 0) (void)arrive(p.fused.ctr + (size_t)b * it.n_kv_heads + kvh);
+        }
+    }
+    if (p.fused.on && !*abort_flag) {
+        // Once all of this CTA's items are written, each of its items merges a
+        // share of its (sequence, KV head) group: the group's rows x float4
+        // columns are cut into as many shares as the group has items, and item k
+        // of the group (split s, row group rg: k = s * row groups + rg) takes
+        // share k, one warp per float4, after waiting (bounded) for the group's
+        // last arrival. The library fuses only when every CTA of the launch is
+        // resident at once, so no wait depends on a CTA that has not started;
+        // a CTA waits only after all its own arrivals, so none depends on
+        // another's wait.
+        volatile int *go = abort_flag + 1; // the header's spare word
+        const int rgs = it.row_groups > 1 ? it.row_groups : 1;
+        for (int item = blockIdx.x; item < it.n_items; item += gridDim.x) {
+            int b, kvh, s, rg;
+            decode_item(it, item, b, kvh, s, rg);
+            const int S = it.split_base[b + 1] - it.split_base[b];
+            const uint32_t n = (uint32_t)(S * rgs);
+            if (threadIdx.x == 0) {
+                const volatile uint32_t *ctr = p.fused.ctr + (size_t)b * it.n_kv_heads + kvh;
+                const uint64_t t0 = global_ns();
+                bool ok = true;
+                while (*ctr < n) {
+                    if (*abort_flag || global_ns() - t0 > p.timeout_ns) {
+                        ok = false;
+                        *abort_flag = 1;
+                        atomicCAS(p.status, 0, kStatusTimeoutGqa);
+                        break;
+                    }
+                    __nanosleep(64);
                 }
+                *go = ok ? 1 : 0;
             }
             named_bar_sync(1, K::CONSUMERS);
-            if (*last_flag) {
-                constexpr int NB = (D + 127) / 128; // 128-column blocks of a row
-                const int S = it.split_base[b + 1] - it.split_base[b];
-                for (int u = warp; u < rows_grp * NB; u += NCW) {
-                    const int row = kvh * Gh + row_off(u / NB);
-                    warp_merge_row(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D,
-                                   (u % NB) * 128, out_row_ptr(p.fused, b, p.n_heads, row, D),
-                                   p.fused.out_dtype);
-                }
+            if (!*go) break;
+            __threadfence(); // the group's partials, before they are read
+            const int K4 = D / 4;
+            const int U = rows_grp * K4, k = s * rgs + rg;
+            const int u0 = (int)((int64_t)k * U / (int64_t)n);
+            const int u1 = (int)((int64_t)(k + 1) * U / (int64_t)n);
+            for (int u = u0 + warp; u < u1; u += NCW) {
+                const int row = kvh * Gh + row_off(u / K4);
+                warp_merge_float4(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D,
+                                  u % K4, out_row_ptr(p.fused, b, p.n_heads, row, D),
+                                  p.fused.out_dtype);
             }
+            named_bar_sync(1, K::CONSUMERS); // *go is read before it is rewritten
         }
     }
     if (threadIdx.x == 0) griddep_launch_dependents();

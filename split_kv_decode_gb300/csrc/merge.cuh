@@ -108,6 +108,64 @@ __device__ __forceinline__ void warp_merge_row(const float2 *ml, const float *ac
     }
 }
 
+// One warp merges the S partials of one float4 of row `row` (value columns
+// [4*c4, 4*c4 + 4)) and stores the normalised result at out_row + 4*c4: the
+// lanes take the splits (all of them in flight at once for S <= 32), each
+// lane merges its splits online and the lanes merge pairwise. The partials
+// were written by other CTAs of the same launch and are read through L2.
+__device__ __forceinline__ void warp_merge_float4(const float2 *ml, const float *acc, size_t slot0,
+                                                  int S, int n_rows, int row, int v_dim, int c4,
+                                                  void *out_row, int out_dtype)
+{
+    const int lane = threadIdx.x & 31;
+    float M = kNeutralM, L = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 *acc4 = reinterpret_cast<const float4 *>(acc);
+    for (int s = lane; s < S; s += 32) {
+        const size_t r = (slot0 + s) * n_rows + row;
+        const float2 x = __ldcg(ml + r);
+        const float4 v = __ldcg(acc4 + r * (v_dim / 4) + c4);
+        if (x.y > 0.f) {
+            const float mn = fmaxf(M, x.x);
+            const float f0 = ex2((M - mn) * kLog2e), f1 = ex2((x.x - mn) * kLog2e);
+            a.x = a.x * f0 + v.x * f1;
+            a.y = a.y * f0 + v.y * f1;
+            a.z = a.z * f0 + v.z * f1;
+            a.w = a.w * f0 + v.w * f1;
+            L = L * f0 + x.y * f1;
+            M = mn;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+        const float Lo = __shfl_xor_sync(0xffffffffu, L, o);
+        const float ax = __shfl_xor_sync(0xffffffffu, a.x, o);
+        const float ay = __shfl_xor_sync(0xffffffffu, a.y, o);
+        const float az = __shfl_xor_sync(0xffffffffu, a.z, o);
+        const float aw = __shfl_xor_sync(0xffffffffu, a.w, o);
+        const float mn = fmaxf(M, Mo);
+        const float f0 = ex2((M - mn) * kLog2e), f1 = ex2((Mo - mn) * kLog2e);
+        a.x = a.x * f0 + ax * f1;
+        a.y = a.y * f0 + ay * f1;
+        a.z = a.z * f0 + az * f1;
+        a.w = a.w * f0 + aw * f1;
+        L = L * f0 + Lo * f1;
+        M = mn;
+    }
+    if (lane != 0) return;
+    const float inv = 1.f / L;
+    a.x *= inv;
+    a.y *= inv;
+    a.z *= inv;
+    a.w *= inv;
+    switch (out_dtype) {
+    case DA_F32: store4<float>(static_cast<float *>(out_row) + 4 * c4, a); break;
+    case DA_F16: store4<__half>(static_cast<__half *>(out_row) + 4 * c4, a); break;
+    default: store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(out_row) + 4 * c4, a); break;
+    }
+}
+
 // Output row `row` of sequence b in the [B][rows][v_dim] output.
 __device__ __forceinline__ void *out_row_ptr(const FusedOut &f, int b, int rows, int row,
                                              int v_dim)
