@@ -246,6 +246,63 @@ template <typename DT, int D, int G, int T, int NCW, int NST, int LPR> struct Gq
     static_assert(NCW * G * D * 4 <= NST * STAGE_BYTES, "flat merge slots in the stage ring");
 };
 
+// The SIMT kernel's merge without a combine launch (DA_FLAG_ONE_LAUNCH), run
+// once all of a CTA's items are written: each of its items merges a share of
+// its (sequence, KV head) group. The group's rows x float4 columns are cut into
+// as many shares as the group has items, and item k of the group (split s, row
+// group rg: k = s * row groups + rg) takes share k, one warp per float4, after
+// waiting (bounded) for the group's last arrival. The library fuses only when
+// every CTA of the launch is resident at once, so no wait depends on a CTA
+// that has not started; a CTA waits only after all its own arrivals, so none
+// depends on another's wait. Kept out of line: the kernel's main loop keeps
+// its own register allocation.
+template <int D, int NCW>
+__device__ __noinline__ void fused_merge_shares(const SplitParams &p, volatile int *abort_flag, int G)
+{
+    const ItemTable &it = p.items;
+    const int warp = threadIdx.x >> 5;
+    const int Gh = p.hq / it.n_kv_heads;
+    const int rows_grp = Gh * p.q_len;
+    auto row_off = [&](int jf) { return p.q_len == 1 ? jf : (jf / Gh) * p.hq + jf % Gh; };
+    volatile int *go = abort_flag + 1; // the header's spare word
+    const int rgs = it.row_groups > 1 ? it.row_groups : 1;
+    (void)G;
+    for (int item = blockIdx.x; item < it.n_items; item += gridDim.x) {
+        int b, kvh, s, rg;
+        decode_item(it, item, b, kvh, s, rg);
+        const int S = it.split_base[b + 1] - it.split_base[b];
+        const uint32_t n = (uint32_t)(S * rgs);
+        if (threadIdx.x == 0) {
+            const volatile uint32_t *ctr = p.fused.ctr + (size_t)b * it.n_kv_heads + kvh;
+            const uint64_t t0 = global_ns();
+            bool ok = true;
+            while (*ctr < n) {
+                if (*abort_flag || global_ns() - t0 > p.timeout_ns) {
+                    ok = false;
+                    *abort_flag = 1;
+                    atomicCAS(p.status, 0, kStatusTimeoutGqa);
+                    break;
+                }
+                __nanosleep(64);
+            }
+            *go = ok ? 1 : 0;
+        }
+        named_bar_sync(1, NCW * 32);
+        if (!*go) break;
+        __threadfence(); // the group's partials, before they are read
+        constexpr int K4 = D / 4;
+        const int U = rows_grp * K4, k = s * rgs + rg;
+        const int u0 = (int)((int64_t)k * U / (int64_t)n);
+        const int u1 = (int)((int64_t)(k + 1) * U / (int64_t)n);
+        for (int u = u0 + warp; u < u1; u += NCW) {
+            const int row = kvh * Gh + row_off(u / K4);
+            warp_merge_float4(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D, u % K4,
+                              out_row_ptr(p.fused, b, p.n_heads, row, D), p.fused.out_dtype);
+        }
+        named_bar_sync(1, NCW * 32); // *go is read before it is rewritten
+    }
+}
+
 template <typename DT, int D, int G, int T, int NCW, int NST, int LPR>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1)
     gqa_split_kernel(const __grid_constant__ GqaMaps maps, const __grid_constant__ SplitParams p)
@@ -798,54 +855,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             if (threadIdx.x == 0) (void)arrive(p.fused.ctr + (size_t)b * it.n_kv_heads + kvh);
         }
     }
-    if (p.fused.on && !*abort_flag) {
-        // Once all of this CTA's items are written, each of its items merges a
-        // share of its (sequence, KV head) group: the group's rows x float4
-        // columns are cut into as many shares as the group has items, and item k
-        // of the group (split s, row group rg: k = s * row groups + rg) takes
-        // share k, one warp per float4, after waiting (bounded) for the group's
-        // last arrival. The library fuses only when every CTA of the launch is
-        // resident at once, so no wait depends on a CTA that has not started;
-        // a CTA waits only after all its own arrivals, so none depends on
-        // another's wait.
-        volatile int *go = abort_flag + 1; // the header's spare word
-        const int rgs = it.row_groups > 1 ? it.row_groups : 1;
-        for (int item = blockIdx.x; item < it.n_items; item += gridDim.x) {
-            int b, kvh, s, rg;
-            decode_item(it, item, b, kvh, s, rg);
-            const int S = it.split_base[b + 1] - it.split_base[b];
-            const uint32_t n = (uint32_t)(S * rgs);
-            if (threadIdx.x == 0) {
-                const volatile uint32_t *ctr = p.fused.ctr + (size_t)b * it.n_kv_heads + kvh;
-                const uint64_t t0 = global_ns();
-                bool ok = true;
-                while (*ctr < n) {
-                    if (*abort_flag || global_ns() - t0 > p.timeout_ns) {
-                        ok = false;
-                        *abort_flag = 1;
-                        atomicCAS(p.status, 0, kStatusTimeoutGqa);
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-                *go = ok ? 1 : 0;
-            }
-            named_bar_sync(1, K::CONSUMERS);
-            if (!*go) break;
-            __threadfence(); // the group's partials, before they are read
-            const int K4 = D / 4;
-            const int U = rows_grp * K4, k = s * rgs + rg;
-            const int u0 = (int)((int64_t)k * U / (int64_t)n);
-            const int u1 = (int)((int64_t)(k + 1) * U / (int64_t)n);
-            for (int u = u0 + warp; u < u1; u += NCW) {
-                const int row = kvh * Gh + row_off(u / K4);
-                warp_merge_float4(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D,
-                                  u % K4, out_row_ptr(p.fused, b, p.n_heads, row, D),
-                                  p.fused.out_dtype);
-            }
-            named_bar_sync(1, K::CONSUMERS); // *go is read before it is rewritten
-        }
-    }
+    if (p.fused.on && !*abort_flag) fused_merge_shares<D, NCW>(p, abort_flag, G);
     if (threadIdx.x == 0) griddep_launch_dependents();
 }
 
