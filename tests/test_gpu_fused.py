@@ -129,3 +129,24 @@ def test_one_launch_workspace_shared_by_calls_of_other_shapes():
         A.decode_attn_device_status(ws)
         worst, rel = errors(case, out.double().cpu().numpy(), oracle_rows(case))
         assert worst <= TOL["f16"], (worst, rel)
+
+
+def test_one_launch_plan_wider_than_the_gpu_falls_back_to_the_combine():
+    # a plan made for more SMs than the device has gives a grid that is not
+    # resident at once: the SIMT kernel then leaves the merge to the combine
+    # launch, and the result still matches the oracle
+    case = W.make_case("t", batch=2, n_heads=16, n_kv_heads=4, head_dim=256,
+                       seq_lens=[30000, 9000], kv_dtype="f16", scale=1 / 16, seed=8500)
+    q, k, v = to_device(case)
+    a = A.make_args(q, k, v, case.scale, flags=N.DA_FLAG_ONE_LAUNCH)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = A.decode_attn_plan(a, case.seq_lens.tolist(), num_sms=4 * sms)
+    assert p.kernel == N.DA_KERNEL_GQA_TMA and p.grid > sms
+    ws = A.new_workspace(p)
+    ws.fill_(0xFF)
+    out = torch.full((case.batch, case.n_heads, case.v_dim), float("nan"), device="cuda")
+    A.decode_attn_splitk_ex(a, p, q, k, v, out, ws)
+    torch.cuda.synchronize()
+    A.decode_attn_device_status(ws)
+    worst, rel = errors(case, out.double().cpu().numpy(), oracle_rows(case))
+    assert worst <= TOL["f16"], (worst, rel)
