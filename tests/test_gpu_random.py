@@ -1,7 +1,9 @@
 """Seeded random shapes against the oracle: for each seed a random geometry
 (heads per KV head, head_dim, storage type, batch, lengths from 1 to a few
 thousand, new tokens per sequence, output type, forced split count) runs through
-whichever kernel the plan picks, and every row is compared with the oracle."""
+whichever kernel the plan picks, with the default two launches and with the
+merge in the split kernel (DA_FLAG_ONE_LAUNCH), and every row is compared with
+the oracle."""
 
 import numpy as np
 import pytest
@@ -26,11 +28,8 @@ def draw(seed):
     hkv = int(g.integers(1, 5))
     gh = int(g.integers(1, 9))
     q_len = int(g.choice([1, 1, 1, 2, 3, 4]))
-    if dtype == "f32":                       # the SIMT kernel: at most 8 rows per item
-        while gh * q_len > 8:
-            q_len -= 1
-            if q_len == 0:
-                q_len, gh = 1, 8
+    # (an f32 cache with more than 8 rows per KV head runs on the SIMT kernel in
+    # row groups; 16-bit caches with 8 or more on the tensor-core kernel)
     batch = int(g.integers(1, 7))
     lens = [int(x) for x in g.integers(q_len, 6000, size=batch)]
     if g.random() < 0.3:
@@ -40,8 +39,9 @@ def draw(seed):
     return dtype, d, hkv, gh, q_len, batch, lens, out_dtype, force
 
 
+@pytest.mark.parametrize("one_launch", [False, True])
 @pytest.mark.parametrize("seed", range(24))
-def test_random_shape(seed):
+def test_random_shape(seed, one_launch):
     dtype, d, hkv, gh, q_len, batch, lens, out_dtype, force = draw(1000 + seed)
     hq = hkv * gh
     case = W.make_case("r", batch=batch, n_heads=hq, n_kv_heads=hkv, head_dim=d, seq_lens=lens,
@@ -50,7 +50,7 @@ def test_random_shape(seed):
     q = q4.cuda() if q_len > 1 else q4[:, 0].contiguous().cuda()
     k, v = case.k.cuda(), case.v.cuda()
     da = A.DecodeAttention(q, k, v, lens, case.scale, out_dtype=_TDT[out_dtype],
-                           force_splits=force)
+                           force_splits=force, flags=N.DA_FLAG_ONE_LAUNCH if one_launch else 0)
     da.workspace.fill_(0xFF)
     out = da(q, k, v)
     torch.cuda.synchronize()
@@ -66,7 +66,8 @@ def test_random_shape(seed):
             bound = TOL[dtype] * vm + _ROUND[out_dtype] * float(np.max(np.abs(ref[b, t])))
             worst = max(worst, err / bound)
     kernel = {N.DA_KERNEL_GQA_TMA: "simt", N.DA_KERNEL_GQA_TC: "tc"}[da.plan.kernel]
-    assert worst <= 1.0, (dtype, d, hkv, gh, q_len, lens, out_dtype, force, kernel, worst)
+    assert worst <= 1.0, (dtype, d, hkv, gh, q_len, lens, out_dtype, force, kernel, one_launch,
+                          worst)
 
 
 @pytest.mark.parametrize("seed", range(16))
