@@ -257,7 +257,7 @@ template <typename DT, int D, int G, int T, int NCW, int NST, int LPR> struct Gq
 // depends on another's wait. Kept out of line: the kernel's main loop keeps
 // its own register allocation.
 template <int D, int NCW>
-__device__ __noinline__ void fused_merge_shares(const SplitParams &p, volatile int *abort_flag, int G)
+__device__ __noinline__ void fused_merge_shares(const SplitParams &p, volatile int *abort_flag)
 {
     const ItemTable &it = p.items;
     const int warp = threadIdx.x >> 5;
@@ -266,7 +266,6 @@ __device__ __noinline__ void fused_merge_shares(const SplitParams &p, volatile i
     auto row_off = [&](int jf) { return p.q_len == 1 ? jf : (jf / Gh) * p.hq + jf % Gh; };
     volatile int *go = abort_flag + 1; // the header's spare word
     const int rgs = it.row_groups > 1 ? it.row_groups : 1;
-    (void)G;
     for (int item = blockIdx.x; item < it.n_items; item += gridDim.x) {
         int b, kvh, s, rg;
         decode_item(it, item, b, kvh, s, rg);
@@ -855,7 +854,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             if (threadIdx.x == 0) (void)arrive(p.fused.ctr + (size_t)b * it.n_kv_heads + kvh);
         }
     }
-    if (p.fused.on && !*abort_flag) fused_merge_shares<D, NCW>(p, abort_flag, G);
+    if (p.fused.on && !*abort_flag) fused_merge_shares<D, NCW>(p, abort_flag);
     if (threadIdx.x == 0) griddep_launch_dependents();
 }
 
