@@ -175,7 +175,9 @@ typedef struct {
     int32_t ctas_per_sm;                /* resident split CTAs per SM                   */
     int32_t tile;                       /* positions per staged tile                    */
     int32_t grid;                       /* split-kernel CTAs (persistent)               */
-    int32_t n_items;                    /* (sequence, KV head, split) work items        */
+    int32_t n_items;                    /* work items: (sequence, KV head, split),
+                                           and per row group on an f32 cache with
+                                           more than 8 rows per KV head             */
     int32_t total_splits;               /* sum over b of n_splits[b]                    */
     int32_t max_splits;                 /* max over b of n_splits[b]                    */
     int32_t batch;
