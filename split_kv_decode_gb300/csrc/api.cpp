@@ -535,10 +535,11 @@ int launch_split(const da_args_t *a, const da_plan_t *pl, const float *q, const 
     }
     p.items.split_base[a->batch] = pl->total_splits;
     const bool tc = pl->kernel == DA_KERNEL_GQA_TC;
-    // The SIMT kernel merges with every CTA of the launch waiting for its groups,
-    // so it fuses only when the whole grid is resident at once (the plan's CTAs
-    // per SM on this device's SMs); otherwise the combine launch merges.
-    const bool fuse = want_fuse && (tc || pl->grid <= device_sms() * pl->ctas_per_sm);
+    // Both GQA kernels merge with every CTA of the launch waiting for its
+    // groups, so they fuse only when the whole grid is resident at once (the
+    // plan's CTAs per SM on this device's SMs); otherwise the combine launch
+    // merges.
+    const bool fuse = want_fuse && pl->grid <= device_sms() * pl->ctas_per_sm;
     p.fused = fused_out(a, pl, ws, out);
     p.fused.on = fuse;
     *fused = fuse;

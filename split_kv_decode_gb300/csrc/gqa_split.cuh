@@ -248,10 +248,10 @@ template <typename DT, int D, int G, int T, int NCW, int NST, int LPR> struct Gq
 
 // The SIMT kernel's merge without a combine launch (DA_FLAG_ONE_LAUNCH), run
 // once all of a CTA's items are written: each of its items merges a share of
-// its (sequence, KV head) group. The group's rows x float4 columns are cut into
-// as many shares as the group has items, and item k of the group (split s, row
-// group rg: k = s * row groups + rg) takes share k, one warp per float4, after
-// waiting (bounded) for the group's last arrival. The library fuses only when
+// its (sequence, KV head) group. The group's (row, 16 value columns) units are
+// cut into as many shares as the group has items, and item k of the group
+// (split s, row group rg: k = s * row groups + rg) takes share k, one warp per
+// unit, after waiting (bounded) for the group's last arrival. The library fuses only when
 // every CTA of the launch is resident at once, so no wait depends on a CTA
 // that has not started; a CTA waits only after all its own arrivals, so none
 // depends on another's wait. Kept out of line: the kernel's main loop keeps
@@ -289,14 +289,15 @@ __device__ __noinline__ void fused_merge_shares(const SplitParams &p, volatile i
         named_bar_sync(1, NCW * 32);
         if (!*go) break;
         __threadfence(); // the group's partials, before they are read
-        constexpr int K4 = D / 4;
-        const int U = rows_grp * K4, k = s * rgs + rg;
+        constexpr int C = 4, CU = D / (4 * C); // float4s per unit, units per row
+        const int U = rows_grp * CU, k = s * rgs + rg;
         const int u0 = (int)((int64_t)k * U / (int64_t)n);
         const int u1 = (int)((int64_t)(k + 1) * U / (int64_t)n);
         for (int u = u0 + warp; u < u1; u += NCW) {
-            const int row = kvh * Gh + row_off(u / K4);
-            warp_merge_float4(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D, u % K4,
-                              out_row_ptr(p.fused, b, p.n_heads, row, D), p.fused.out_dtype);
+            const int row = kvh * Gh + row_off(u / CU);
+            warp_merge_cols<C, 8>(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D,
+                                  (u % CU) * C, out_row_ptr(p.fused, b, p.n_heads, row, D),
+                                  p.fused.out_dtype);
         }
         named_bar_sync(1, NCW * 32); // *go is read before it is rewritten
     }
@@ -854,7 +855,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1)
             if (threadIdx.x == 0) (void)arrive(p.fused.ctr + (size_t)b * it.n_kv_heads + kvh);
         }
     }
-    if (p.fused.on && !*abort_flag) fused_merge_shares<D, NCW>(p, abort_flag);
+    // the consumer warps take the same decision (a barrier-wide or of the flag)
+    if (p.fused.on && !named_bar_or(1, K::CONSUMERS, *abort_flag != 0))
+        fused_merge_shares<D, NCW>(p, abort_flag);
     if (threadIdx.x == 0) griddep_launch_dependents();
 }
 

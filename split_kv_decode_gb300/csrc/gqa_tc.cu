@@ -139,6 +139,56 @@ template <int T> struct Walk {
     }
 };
 
+// The merge without a combine launch, run by the four softmax warps of every
+// CTA once all its own partials are written and counted: for each of its items
+// the CTA waits (bounded) until every split of the item's (sequence, KV head)
+// group has arrived, then merges share s (the item's split) of the group's
+// (row, 16 value columns) units into out. The library fuses only when the
+// whole grid is resident at once, so no wait depends on a CTA that has not
+// started, and a CTA waits only after its own arrivals.
+template <int D>
+__device__ __noinline__ void tc_merge_shares(const SplitParams &p, volatile int *abort_flag)
+{
+    constexpr int C = 4, CU = D / (4 * C); // float4s per unit, units per row
+    const ItemTable &it = p.items;
+    const int warp = threadIdx.x >> 5;
+    const int Gh = p.hq / it.n_kv_heads;
+    const int U = Gh * p.q_len * CU;
+    volatile int *go = abort_flag + 1;
+    for (int item = blockIdx.x; item < it.n_items; item += gridDim.x) {
+        int b, kvh, s;
+        decode_item(it, item, b, kvh, s);
+        const int S = it.split_base[b + 1] - it.split_base[b];
+        if (threadIdx.x == 0) {
+            const volatile uint32_t *ctr = p.fused.ctr + (size_t)b * it.n_kv_heads + kvh;
+            const uint64_t t0 = global_ns();
+            bool ok = true;
+            while (*ctr < (uint32_t)S) {
+                if (*abort_flag || global_ns() - t0 > p.timeout_ns) {
+                    ok = false;
+                    *abort_flag = 1;
+                    atomicCAS(p.status, 0, kStatusTimeoutTc);
+                    break;
+                }
+                __nanosleep(64);
+            }
+            *go = ok ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        if (!*go) break;
+        __threadfence(); // the group's partials, before they are read
+        const int u0 = (int)((int64_t)s * U / S), u1 = (int)((int64_t)(s + 1) * U / S);
+        for (int u = u0 + warp; u < u1; u += 4) {
+            const int rr = u / CU, tk = rr / Gh;
+            const int row = kvh * Gh + tk * p.hq + (rr - tk * Gh);
+            warp_merge_cols<C, 8>(p.ml, p.acc, (size_t)it.split_base[b], S, p.n_heads, row, D,
+                                  (u - rr * CU) * C, out_row_ptr(p.fused, b, p.n_heads, row, D),
+                                  p.fused.out_dtype);
+        }
+        named_bar_sync(1, 128); // *go is read before it is rewritten
+    }
+}
+
 template <typename DT, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gqa_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -373,30 +423,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t sph = 0, pfp = 0, qfp = 0, oph = 0;
         bool ab = false;
         int items = 0, gt = 0;
-        // After an item's partial is written: the last partial of its (sequence,
-        // KV head) group to arrive merges the group's rows into out (no combine
-        // launch). The four warps publish their writes before the arrival.
+        // After an item's partial is written: the four warps publish their
+        // writes, then one arrival on the item's (sequence, KV head) group.
         auto arrive_merge = [&](int b, int kvh) {
-            volatile int *last_flag = abort_flag + 1;
             __threadfence();
             named_bar_sync(1, 128);
-            if (threadIdx.x == 0) {
-                const uint32_t n = (uint32_t)(p.items.split_base[b + 1] - p.items.split_base[b]);
-                const bool last = arrive(p.fused.ctr + (size_t)b * p.items.n_kv_heads + kvh) == n;
-                if (last) __threadfence(); // the other partials, before they are read
-                *last_flag = last ? 1 : 0;
-            }
-            named_bar_sync(1, 128);
-            if (*last_flag) {
-                const int S = p.items.split_base[b + 1] - p.items.split_base[b];
-                for (int u = warp; u < R * NBLK; u += 4) {
-                    const int rr = u / NBLK, tk = rr / Gh;
-                    const int row = kvh * Gh + tk * p.hq + (rr - tk * Gh);
-                    warp_merge_row(p.ml, p.acc, (size_t)p.items.split_base[b], S, p.n_heads, row,
-                                   D, (u % NBLK) * 128, out_row_ptr(p.fused, b, p.n_heads, row, D),
-                                   p.fused.out_dtype);
-                }
-            }
+            if (threadIdx.x == 0) (void)arrive(p.fused.ctr + (size_t)b * p.items.n_kv_heads + kvh);
         };
         for (int item = blockIdx.x; !ab && item < p.items.n_items; item += gridDim.x) {
             int b, kvh, s;
@@ -583,6 +615,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             *abort_flag = 1;
             atomicCAS(p.status, 0, kStatusTimeoutTc);
         }
+        // the four warps take the same decision (a barrier-wide or of the flag)
+        if (p.fused.on && !tc_bar_or(*abort_flag != 0)) tc_merge_shares<D>(p, abort_flag);
     }
 
     // ---------------------------------- teardown ----------------------------------

@@ -45,99 +45,56 @@ __device__ __forceinline__ void fma4(float4 &a, float w, const float4 &v)
     a.w = fmaf(w, v.w, a.w);
 }
 
-// One warp merges the S partials of row `row` of the slots slot0 .. slot0+S-1
-// over the 128 value columns [col0, col0 + 128), a float4 per lane, and stores
-// the normalised result at out_row + col0 in the output type. The partials were
-// written by other CTAs of the same launch, so they are read through L2 (.cg),
-// after the arrival that made them visible.
-__device__ __forceinline__ void warp_merge_row(const float2 *ml, const float *acc, size_t slot0,
-                                               int S, int n_rows, int row, int v_dim, int col0,
-                                               void *out_row, int out_dtype)
+// One warp merges the S partials of C consecutive float4s of row `row` (value
+// columns [4*c4, 4*(c4 + C))) and stores the normalised result at
+// out_row + 4*c4. Lane sl*C + c takes float4 c4 + c of the splits sl,
+// sl + 32/C, sl + 2*32/C, ..., NB of them in flight at a time; each lane merges
+// its splits online, then the 32/C lanes of each float4 merge pairwise, so a
+// unit costs one round trip to L2 for up to NB*32/C splits. The partials were
+// written by other CTAs of the same launch and are read through L2.
+template <int C, int NB>
+__device__ __forceinline__ void warp_merge_cols(const float2 *ml, const float *acc, size_t slot0,
+                                                int S, int n_rows, int row, int v_dim, int c4,
+                                                void *out_row, int out_dtype)
 {
-    const int lane = threadIdx.x & 31;
-    const int col = col0 + lane * 4;
-    const bool live = col < v_dim;
-    // m = max_i m_i and l = sum_i e^{m_i - m} l_i: each lane merges its splits
-    // online, then the lanes merge theirs pairwise (all lanes end equal)
-    float M = kNeutralM, L = 0.f;
-    for (int s = lane; s < S; s += 32) {
-        const float2 x = __ldcg(ml + (slot0 + s) * n_rows + row);
-        if (x.x > M) {
-            L = fmaf(L, ex2((M - x.x) * kLog2e), x.y);
-            M = x.x;
-        } else {
-            L = fmaf(x.y, ex2((x.x - M) * kLog2e), L);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
-        const float Lo = __shfl_xor_sync(0xffffffffu, L, o);
-        const float Mn = fmaxf(M, Mo);
-        L = L * ex2((M - Mn) * kLog2e) + Lo * ex2((Mo - Mn) * kLog2e);
-        M = Mn;
-    }
-    // sum_i w_i acc_i, eight splits' loads in flight at a time
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    static_assert(C == 1 || C == 2 || C == 4 || C == 8 || C == 16, "C divides 32");
+    constexpr int SL = 32 / C;
+    const int lane = threadIdx.x & 31, c = lane % C, sl = lane / C;
+    const int V4 = v_dim / 4;
+    const bool live = c4 + c < V4;
     const float4 *acc4 = reinterpret_cast<const float4 *>(acc);
-    const size_t stride = (size_t)n_rows * v_dim / 4;    // float4s between slots
-    const size_t base = ((slot0 * n_rows + row) * (size_t)v_dim + (live ? col : col0)) / 4;
-    for (int s0 = 0; s0 < S; s0 += 8) {
-        float2 x[8];
-        float4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int s = min(s0 + i, S - 1);
-            x[i] = __ldcg(ml + (slot0 + s) * n_rows + row);
-            v[i] = __ldcg(acc4 + base + (size_t)s * stride);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (s0 + i < S && x[i].y > 0.f) fma4(a, ex2((x[i].x - M) * kLog2e), v[i]);
-    }
-    if (!live) return;
-    const float inv = 1.f / L;
-    a.x *= inv;
-    a.y *= inv;
-    a.z *= inv;
-    a.w *= inv;
-    switch (out_dtype) {
-    case DA_F32: store4<float>(static_cast<float *>(out_row) + col, a); break;
-    case DA_F16: store4<__half>(static_cast<__half *>(out_row) + col, a); break;
-    default: store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(out_row) + col, a); break;
-    }
-}
-
-// One warp merges the S partials of one float4 of row `row` (value columns
-// [4*c4, 4*c4 + 4)) and stores the normalised result at out_row + 4*c4: the
-// lanes take the splits (all of them in flight at once for S <= 32), each
-// lane merges its splits online and the lanes merge pairwise. The partials
-// were written by other CTAs of the same launch and are read through L2.
-__device__ __forceinline__ void warp_merge_float4(const float2 *ml, const float *acc, size_t slot0,
-                                                  int S, int n_rows, int row, int v_dim, int c4,
-                                                  void *out_row, int out_dtype)
-{
-    const int lane = threadIdx.x & 31;
     float M = kNeutralM, L = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 *acc4 = reinterpret_cast<const float4 *>(acc);
-    for (int s = lane; s < S; s += 32) {
-        const size_t r = (slot0 + s) * n_rows + row;
-        const float2 x = __ldcg(ml + r);
-        const float4 v = __ldcg(acc4 + r * (v_dim / 4) + c4);
-        if (x.y > 0.f) {
-            const float mn = fmaxf(M, x.x);
-            const float f0 = ex2((M - mn) * kLog2e), f1 = ex2((x.x - mn) * kLog2e);
-            a.x = a.x * f0 + v.x * f1;
-            a.y = a.y * f0 + v.y * f1;
-            a.z = a.z * f0 + v.z * f1;
-            a.w = a.w * f0 + v.w * f1;
-            L = L * f0 + x.y * f1;
-            M = mn;
+    for (int s0 = sl; s0 < S; s0 += SL * NB) {
+        float2 x[NB];
+        float4 v[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int s = s0 + i * SL;
+            x[i] = make_float2(kNeutralM, 0.f);
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s < S) {
+                const size_t r = (slot0 + s) * n_rows + row;
+                x[i] = __ldcg(ml + r);
+                if (live) v[i] = __ldcg(acc4 + r * V4 + c4 + c);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            if (x[i].y > 0.f) { // a neutral partial (l = 0) takes no part
+                const float mn = fmaxf(M, x[i].x);
+                const float f0 = ex2((M - mn) * kLog2e), f1 = ex2((x[i].x - mn) * kLog2e);
+                a.x = a.x * f0 + v[i].x * f1;
+                a.y = a.y * f0 + v[i].y * f1;
+                a.z = a.z * f0 + v[i].z * f1;
+                a.w = a.w * f0 + v[i].w * f1;
+                L = L * f0 + x[i].y * f1;
+                M = mn;
+            }
         }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = C; o < 32; o <<= 1) {
         const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
         const float Lo = __shfl_xor_sync(0xffffffffu, L, o);
         const float ax = __shfl_xor_sync(0xffffffffu, a.x, o);
@@ -153,16 +110,18 @@ __device__ __forceinline__ void warp_merge_float4(const float2 *ml, const float 
         L = L * f0 + Lo * f1;
         M = mn;
     }
-    if (lane != 0) return;
+    if (sl != 0 || !live) return;
     const float inv = 1.f / L;
     a.x *= inv;
     a.y *= inv;
     a.z *= inv;
     a.w *= inv;
+    void *dst = static_cast<unsigned char *>(out_row) +
+                (size_t)4 * (c4 + c) * (out_dtype == DA_F32 ? 4 : 2);
     switch (out_dtype) {
-    case DA_F32: store4<float>(static_cast<float *>(out_row) + 4 * c4, a); break;
-    case DA_F16: store4<__half>(static_cast<__half *>(out_row) + 4 * c4, a); break;
-    default: store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(out_row) + 4 * c4, a); break;
+    case DA_F32: store4<float>(static_cast<float *>(dst), a); break;
+    case DA_F16: store4<__half>(static_cast<__half *>(dst), a); break;
+    default: store4<__nv_bfloat16>(static_cast<__nv_bfloat16 *>(dst), a); break;
     }
 }
 

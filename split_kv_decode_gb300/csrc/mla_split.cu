@@ -234,6 +234,25 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag, uint32_t a
     }
 }
 
+// The merge without a combine launch, once every CTA of the launch has written
+// its partials: the grid's warps take the (sequence, row, 16 value columns)
+// units in turn, one round trip to L2 per unit for up to 80 splits.
+__device__ __noinline__ void mla_merge_units(const MlaParams &p)
+{
+    constexpr int C = 4, CU = kDv / (4 * C); // float4s per unit, units per row
+    const ItemTable &it = p.items;
+    const int warp = threadIdx.x >> 5;
+    const int rows = p.n_heads, units = it.batch * rows * CU;
+    const int nw = (int)gridDim.x * (kThreads / 32);
+    for (int u = (int)blockIdx.x * (kThreads / 32) + warp; u < units; u += nw) {
+        const int b = u / (rows * CU), r = u - b * (rows * CU);
+        const int row = r / CU, z = r - row * CU;
+        warp_merge_cols<C, 10>(p.ml, p.acc, (size_t)it.split_base[b],
+                               it.split_base[b + 1] - it.split_base[b], rows, row, kDv, z * C,
+                               out_row_ptr(p.fused, b, rows, row, kDv), p.fused.out_dtype);
+    }
+}
+
 template <int N, typename CT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_split_kernel(const __grid_constant__ MlaParams p)
@@ -702,7 +721,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // The merge without a combine launch: once every CTA of the launch has
         // written its partials (a grid-wide arrival count; the library fuses
         // only when the GPU holds all the launch's clusters at once), every warp
-        // of the grid merges a share of the (sequence, row, 128 columns) units.
+        // of the grid merges a share of the units.
         volatile int *go = abort_flag + 1;
         uint32_t *arrived = p.fused.ctr;
         __threadfence(); // this thread's partial writes, before the arrival
@@ -723,17 +742,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *go = ok && *reinterpret_cast<volatile int *>(p.status) == 0;
         }
         __syncthreads();
-        if (*go) {
-            const int rows = p.n_heads, units = it.batch * rows * (kDv / 128);
-            const int nw = (int)gridDim.x * (kThreads / 32);
-            for (int u = (int)blockIdx.x * (kThreads / 32) + warp; u < units; u += nw) {
-                const int b = u / (rows * (kDv / 128)), r = u % (rows * (kDv / 128));
-                const int row = r / (kDv / 128), z = r % (kDv / 128);
-                warp_merge_row(p.ml, p.acc, (size_t)it.split_base[b],
-                               it.split_base[b + 1] - it.split_base[b], rows, row, kDv, z * 128,
-                               out_row_ptr(p.fused, b, rows, row, kDv), p.fused.out_dtype);
-            }
-        }
+        if (*go) mla_merge_units(p);
     }
     if (threadIdx.x == 0) griddep_launch_dependents();
 }
