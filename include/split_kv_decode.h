@@ -79,26 +79,34 @@ typedef enum {
                                     kernel, whose operands are bf16 (see
                                     DA_MLA_EXACT_BELOW)                              */
 #define DA_FLAG_ONE_LAUNCH 0x20  /* the split kernel merges its own partials (no
-                                    combine launch). SIMT GQA kernel: once a CTA
-                                    has written all its items, each item merges a
-                                    share of its (sequence, KV head) group after
-                                    waiting for the group's last arrival (only when
-                                    the plan's grid is resident at once, else the
-                                    combine launch merges); tensor-core GQA kernel:
-                                    the last split of a group to finish merges it;
-                                    MLA tensor-core kernel: the CTAs merge shares of
-                                    the rows once all have finished (when the GPU
-                                    holds all its clusters at once). A memset of the
-                                    workspace's arrival counters precedes the
-                                    launch. The waits assume the launch is not
-                                    sharing the SMs with kernels of other streams;
-                                    if it is, they may run out (DA_ETIMEOUT in the
-                                    status word). Measured on GB300 within -1 to
-                                    +5 us of the default two launches, so it is an
-                                    option, not the default                       */
+                                    combine launch). GQA kernels (SIMT and tensor
+                                    cores): once a CTA has written all its items,
+                                    each item merges a share of its (sequence, KV
+                                    head) group after waiting for the group's last
+                                    arrival; MLA tensor-core kernel: once all CTAs
+                                    have finished, each stages its share of the
+                                    rows in shared memory and merges it. Only when
+                                    the plan's grid (the MLA kernel's clusters) is
+                                    resident at once, else the combine launch
+                                    merges. A memset of the workspace's arrival
+                                    counters precedes the launch. The waits assume
+                                    the launch is not sharing the SMs with kernels
+                                    of other streams; if it is, they may run out
+                                    (DA_ETIMEOUT in the status word). Measured on
+                                    GB300 within -1.5 to +2 us of the default two
+                                    launches, so it is an option, not the default */
+#define DA_FLAG_COMBINE_LOADS 0x40 /* the combine kernel reads the partials with
+                                    plain loads instead of staging them in shared
+                                    memory by bulk copies (kept for comparison;
+                                    partials of several ranks, a v_dim that is not
+                                    a multiple of 128 or more than 256 splits of a
+                                    sequence always take this form)                */
 #define DA_FLAG_TEST_NO_TMA 0x100 /* test hook: the producer issues no copy, so every
                                      consumer wait runs out after timeout_us and the
-                                     kernel reports DA_ETIMEOUT through device_status */
+                                     kernel reports DA_ETIMEOUT through device_status;
+                                     the staged combine (and the projection) issues
+                                     none either and reports its own timeout when
+                                     no earlier one is recorded                      */
 #define DA_FLAG_TEST_BAD_LAUNCH 0x200 /* test hook: the split kernel is launched with an
                                      empty grid, which the runtime refuses before
                                      anything runs (a launch error that does not stick

@@ -23,6 +23,7 @@ DA_FLAG_NO_CAUSAL = 0x4
 DA_FLAG_MLA_SIMT = 0x8
 DA_FLAG_MLA_TC = 0x10
 DA_FLAG_ONE_LAUNCH = 0x20
+DA_FLAG_COMBINE_LOADS = 0x40
 DA_MLA_EXACT_BELOW = 2048
 DA_FLAG_TEST_NO_TMA = 0x100
 DA_FLAG_TEST_BAD_LAUNCH = 0x200

@@ -647,15 +647,15 @@ int launch_combine_phase(const da_args_t *a, const da_plan_t *pl, const void *ws
         c.split_base[b] = pl->split_base[b];
     }
     cudaError_t e;
+    c.status = reinterpret_cast<int *>(const_cast<uint8_t *>(w));
+    c.timeout_ns = (uint64_t)(a->timeout_us > 0 ? a->timeout_us : 2000000) * 1000ull;
+    c.flags = a->flags;
     if (proj) {
         c.w = proj->w;
         c.w_head_stride = proj->head_stride;
         c.w_row_stride = proj->row_stride;
         c.out_dim = proj->out_dim;
         c.w_heads = a->n_heads;
-        c.status = reinterpret_cast<int *>(const_cast<uint8_t *>(w));
-        c.timeout_ns = (uint64_t)(a->timeout_us > 0 ? a->timeout_us : 2000000) * 1000ull;
-        c.flags = a->flags;
         e = launch_combine_proj(a->out_dtype, proj->w_dtype, c, rows_of(a), a->batch, st, true);
     } else {
         e = launch_combine(a->out_dtype, a->v_dim, c, rows_of(a), a->batch, st, true);
@@ -1012,6 +1012,7 @@ int decode_attn_device_status(void *ws, da_stream_t stream)
                     kernel == DA_KERNEL_MLA_TC   ? "split (mla)"
                     : kernel == DA_KERNEL_GQA_TC ? "split (gqa, tensor cores)"
                     : kernel == (kStatusTimeoutProj >> 8) ? "combine (projection)"
+                    : kernel == (kStatusTimeoutCombine >> 8) ? "combine"
                                                           : "split (gqa)",
                     "a bounded in-kernel wait ran out");
     return fail(DA_ECUDA, "status", "unexpected status word 0x%x", v);

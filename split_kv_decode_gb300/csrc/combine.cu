@@ -55,15 +55,22 @@ __device__ __forceinline__ float4 merge_columns(const CombineParams &p, int h, i
     const size_t slot0 = (size_t)p.split_base[b];
     const int col = z * kCombineCols + lane * 4;
     const bool live = col < p.v_dim;
-    // pair i = r * S + s: rank r's split s
+    // pair i = r * S + s: rank r's split s (a division only with several ranks)
+    const float2 *ml0 = p.ml + slot0 * p.n_heads + h;
+    const float *acc0 = p.acc + (slot0 * p.n_heads + h) * p.v_dim + (live ? col : 0);
+    const size_t acc_step = (size_t)p.n_heads * p.v_dim;
     auto ml_of = [&](int i) {
+        if (p.n_ranks == 1) return __ldg(ml0 + (size_t)i * p.n_heads);
         const int r = i / S;
-        return __ldg(p.ml + r * p.rank_ml + (slot0 + (i - r * S)) * p.n_heads + h);
+        return __ldg(ml0 + r * p.rank_ml + (size_t)(i - r * S) * p.n_heads);
     };
     auto acc_of = [&](int i) {
-        const int r = i / S;
-        return __ldg(reinterpret_cast<const float4 *>(
-            p.acc + r * p.rank_acc + ((slot0 + (i - r * S)) * p.n_heads + h) * p.v_dim + col));
+        const float *a = acc0 + (size_t)i * acc_step;
+        if (p.n_ranks > 1) {
+            const int r = i / S;
+            a = acc0 + r * p.rank_acc + (size_t)(i - r * S) * acc_step;
+        }
+        return __ldg(reinterpret_cast<const float4 *>(a));
     };
 
     // acc vectors of this warp's first pairs, in flight while m and l are formed
@@ -77,6 +84,7 @@ __device__ __forceinline__ float4 merge_columns(const CombineParams &p, int h, i
     // one pass: each lane merges its pairs online, then the lanes merge theirs
     // pairwise with the same rescaling (every lane ends with the same M and L)
     float M = kNeutralM, L = 0.f;
+#pragma unroll 4
     for (int sp = lane; sp < SR; sp += 32) {
         const float2 x = ml_of(sp);
         if (x.x > M) {
@@ -138,6 +146,144 @@ __global__ void __launch_bounds__(kCombineThreads)
     const int col = blockIdx.z * kCombineCols + lane * 4;
     if (threadIdx.x < 32 && col < p.v_dim) {
         OT *out = reinterpret_cast<OT *>(p.out) + ((size_t)b * p.n_heads + h) * p.v_dim + col;
+        store4<OT>(out, t);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The same merge with the partials staged in shared memory, for one rank's
+// partials and a v_dim that is a multiple of 128: bulk copies bring each
+// split's 512-byte block of the CTA's 128 columns (one mbarrier for all of
+// them) while warp 0 forms the weights w_s = e^{m_s - m} / sum_i e^{m_i - m} l_i
+// from the (m, l) pairs (w_s = 0 for a neutral partial, whose block is never
+// used); then warp w sums w_s acc_s over the splits w, w + 8, ... from shared
+// memory and warp 0 adds the 8 sums in a fixed order. The copies are issued
+// right after griddepcontrol.wait, so the CTA waits for one round trip.
+constexpr int kStagedMaxSplits = 256;
+
+int combine_staged_smem_bytes(int max_splits)
+{
+    // blocks [S][512 B] | weights [S] | per-warp sums [8][32] float4 | mbarrier, flag
+    return max_splits * (kCombineCols * 4 + 4) + ((max_splits * 4) % 16 ? 16 - (max_splits * 4) % 16 : 0) +
+           kCombineWarps * 32 * 16 + 16;
+}
+
+template <typename OT>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_staged_kernel(const __grid_constant__ CombineParams p, int max_splits)
+{
+    extern __shared__ __align__(128) unsigned char dsm[];
+    constexpr int BLK = kCombineCols * 4;
+    const int h = blockIdx.x, b = blockIdx.y, z = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.n_splits[b];
+    const size_t slot0 = (size_t)p.split_base[b];
+    const int wts_bytes = (max_splits * 4 + 15) / 16 * 16;
+    float *wts = reinterpret_cast<float *>(dsm + (size_t)max_splits * BLK);
+    float4 *red = reinterpret_cast<float4 *>(dsm + (size_t)max_splits * BLK + wts_bytes);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(dsm + (size_t)max_splits * BLK + wts_bytes +
+                                                 kCombineWarps * 32 * 16);
+    volatile int *ok_flag = reinterpret_cast<volatile int *>(bar + 1);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    griddep_wait();
+    fence_proxy_async_global(); // the split kernel's partials, for the bulk copies
+
+    const bool load = !(p.flags & DA_FLAG_TEST_NO_TMA);
+    if (threadIdx.x == 0 && load) mbar_arrive_expect_tx(bar, (uint32_t)(S * BLK));
+    __syncthreads(); // the expected bytes are set before any copy completes
+    if (load)
+        for (int s = threadIdx.x; s < S; s += kCombineThreads)
+            bulk_load_g2s(dsm + (size_t)s * BLK,
+                          p.acc + ((slot0 + s) * p.n_heads + h) * p.v_dim + z * kCombineCols, BLK,
+                          bar);
+    if (warp == 0) {
+        // m = max_i m_i, l = sum_i e^{m_i - m} l_i: the lanes merge their splits
+        // online (all pairs of up to 128 splits in flight at once), then pairwise
+        constexpr int WB = 4;
+        const float2 *ml = p.ml + slot0 * p.n_heads + h;
+        float2 x[WB];
+        float M = kNeutralM, L = 0.f;
+        for (int s0 = 0; s0 < S; s0 += 32 * WB) {
+#pragma unroll
+            for (int i = 0; i < WB; ++i) {
+                const int s = s0 + 32 * i + lane;
+                x[i] = s < S ? __ldg(ml + (size_t)s * p.n_heads) : make_float2(kNeutralM, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < WB; ++i) {
+                if (x[i].y > 0.f) {
+                    const float mn = fmaxf(M, x[i].x);
+                    L = L * ex2((M - mn) * kLog2e) + x[i].y * ex2((x[i].x - mn) * kLog2e);
+                    M = mn;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+            const float Lo = __shfl_xor_sync(0xffffffffu, L, o);
+            const float mn = fmaxf(M, Mo);
+            L = L * ex2((M - mn) * kLog2e) + Lo * ex2((Mo - mn) * kLog2e);
+            M = mn;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        if (S <= 32 * WB) { // the pairs are still in registers
+#pragma unroll
+            for (int i = 0; i < WB; ++i) {
+                const int s = 32 * i + lane;
+                if (s < S) wts[s] = x[i].y > 0.f ? ex2((x[i].x - M) * kLog2e) * inv : 0.f;
+            }
+        } else {
+            for (int s = lane; s < S; s += 32) {
+                const float2 y = __ldg(ml + (size_t)s * p.n_heads);
+                wts[s] = y.y > 0.f ? ex2((y.x - M) * kLog2e) * inv : 0.f;
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        // a wait that runs out (or copies never requested, the test hook)
+        // leaves this CTA's columns unwritten and records the timeout
+        volatile int never = 0;
+        bool ok = load && mbar_wait_bounded(bar, 0, p.timeout_ns, &never);
+        if (!ok) {
+            atomicCAS(p.status, 0, kStatusTimeoutCombine);
+            // copies still in flight land before the CTA's memory is released
+            if (load) (void)mbar_wait_bounded(bar, 0, p.timeout_ns, &never);
+        }
+        *ok_flag = ok ? 1 : 0;
+    }
+    __syncthreads(); // also publishes the weights
+    if (!*ok_flag) return;
+    {
+        volatile int never = 0;
+        (void)mbar_wait_bounded(bar, 0, p.timeout_ns, &never); // complete: this thread's view
+    }
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = warp; s < S; s += kCombineWarps) {
+        const float w = wts[s];
+        const float4 v = reinterpret_cast<const float4 *>(dsm + (size_t)s * BLK)[lane];
+        if (w > 0.f) fma4(a, w, v);
+    }
+    red[warp * 32 + lane] = a;
+    __syncthreads();
+    if (warp == 0) {
+        float4 t = red[lane];
+#pragma unroll
+        for (int w = 1; w < kCombineWarps; ++w) {
+            const float4 u = red[w * 32 + lane];
+            t.x += u.x;
+            t.y += u.y;
+            t.z += u.z;
+            t.w += u.w;
+        }
+        OT *out = reinterpret_cast<OT *>(p.out) + ((size_t)b * p.n_heads + h) * p.v_dim +
+                  z * kCombineCols + lane * 4;
         store4<OT>(out, t);
     }
 }
@@ -264,6 +410,17 @@ __global__ void __launch_bounds__(kCombineThreads)
     }
 }
 
+template <typename OT>
+static cudaError_t launch_staged(cudaLaunchConfig_t &cfg, const CombineParams &p, int max_splits)
+{
+    const int smem = combine_staged_smem_bytes(max_splits);
+    cudaError_t e = cudaFuncSetAttribute(combine_staged_kernel<OT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cfg.dynamicSmemBytes = smem;
+    return cudaLaunchKernelEx(&cfg, combine_staged_kernel<OT>, p, max_splits);
+}
+
 cudaError_t launch_combine(int out_dtype, int v_dim, const CombineParams &p, int grid_x,
                            int grid_y, cudaStream_t stream, bool pdl)
 {
@@ -278,6 +435,18 @@ cudaError_t launch_combine(int out_dtype, int v_dim, const CombineParams &p, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    int max_splits = 0;
+    for (int b = 0; b < p.batch; ++b) max_splits = p.n_splits[b] > max_splits ? p.n_splits[b] : max_splits;
+    // one rank's partials in whole 128-column blocks: staged in shared memory
+    if (p.n_ranks == 1 && v_dim % kCombineCols == 0 && max_splits <= kStagedMaxSplits &&
+        !(p.flags & DA_FLAG_COMBINE_LOADS)) {
+        switch (out_dtype) {
+        case DA_F32: return launch_staged<float>(cfg, p, max_splits);
+        case DA_F16: return launch_staged<__half>(cfg, p, max_splits);
+        case DA_BF16: return launch_staged<__nv_bfloat16>(cfg, p, max_splits);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (out_dtype) {
     case DA_F32: return cudaLaunchKernelEx(&cfg, combine_kernel<float>, p);
     case DA_F16: return cudaLaunchKernelEx(&cfg, combine_kernel<__half>, p);

@@ -58,6 +58,7 @@ constexpr int kStatusTimeoutGqa = DA_ETIMEOUT | (DA_KERNEL_GQA_TMA << 8);
 constexpr int kStatusTimeoutMla = DA_ETIMEOUT | (DA_KERNEL_MLA_TC << 8);
 constexpr int kStatusTimeoutTc = DA_ETIMEOUT | (DA_KERNEL_GQA_TC << 8);
 constexpr int kStatusTimeoutProj = DA_ETIMEOUT | (15 << 8); // combine with the projection
+constexpr int kStatusTimeoutCombine = DA_ETIMEOUT | (14 << 8); // staged combine
 
 // Per-launch description of the work items shared by the split kernels.
 struct ItemTable {

@@ -235,21 +235,186 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag, uint32_t a
 }
 
 // The merge without a combine launch, once every CTA of the launch has written
-// its partials: the grid's warps take the (sequence, row, 16 value columns)
-// units in turn, one round trip to L2 per unit for up to 80 splits.
-__device__ __noinline__ void mla_merge_units(const MlaParams &p)
+// its partials. CTA c takes the (sequence, row, 128 value columns) units c,
+// c + gridDim.x, ... and stages them in its tile slots, idle by now: bulk
+// copies bring each split's 512-byte block of a unit, as many units per pass
+// as fit, while warp k forms the weights w_s = e^{m_s - m} / sum_i e^{m_i - m} l_i
+// of the pass's unit k from the (m, l) pairs (w_s = 0 for a neutral partial,
+// whose block is never used). The warps then share out each unit's splits, sum
+// w_s acc_s from shared memory and add their sums in a fixed order. A unit with
+// more splits than the stage holds is merged from L2 by eight warps instead.
+constexpr int kNW = kThreads / 32;
+constexpr int kStageBytes = 2 * kSlotBytes;                 // the two tile slots
+constexpr int kSBarOff = kStageBytes - 64;                  // staging mbarrier, pass header
+constexpr int kRedOff = kSBarOff - kNW * 32 * 16;           // per-warp sums, float4 per lane
+constexpr int kTabOff = kRedOff - 256;                      // the pass's unit table
+constexpr int kPassUnits = 8;
+constexpr int kBlk = 128 * 4;                               // bytes of one split's block
+
+struct PassUnit {
+    int b, row, z, S, off; // off: the unit's first block in the stage
+};
+static_assert(kPassUnits * sizeof(PassUnit) <= 256 && kPassUnits <= kNW, "pass table");
+static_assert(kRedOff % 16 == 0 && kTabOff % 16 == 0, "staging alignment");
+
+__device__ __noinline__ void mla_merge_staged(const MlaParams &p, uint8_t *sm)
 {
-    constexpr int C = 4, CU = kDv / (4 * C); // float4s per unit, units per row
+    constexpr int CU = kDv / 128;
     const ItemTable &it = p.items;
-    const int warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows = p.n_heads, units = it.batch * rows * CU;
-    const int nw = (int)gridDim.x * (kThreads / 32);
-    for (int u = (int)blockIdx.x * (kThreads / 32) + warp; u < units; u += nw) {
-        const int b = u / (rows * CU), r = u - b * (rows * CU);
-        const int row = r / CU, z = r - row * CU;
-        warp_merge_cols<C, 10>(p.ml, p.acc, (size_t)it.split_base[b],
-                               it.split_base[b + 1] - it.split_base[b], rows, row, kDv, z * C,
-                               out_row_ptr(p.fused, b, rows, row, kDv), p.fused.out_dtype);
+    uint64_t *sbar = reinterpret_cast<uint64_t *>(sm + kSBarOff);
+    volatile int *hdr = reinterpret_cast<volatile int *>(sm + kSBarOff + 16); // nu, nb, next, ok
+    PassUnit *tab = reinterpret_cast<PassUnit *>(sm + kTabOff);
+    float4 *red = reinterpret_cast<float4 *>(sm + kRedOff);
+    volatile int never = 0;
+    // the tile slots' generic and tensor-core accesses, and the acquire of the
+    // partials, before the bulk copies
+    fence_proxy_async_smem();
+    fence_proxy_async_global();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_init(sbar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < units;) {
+        if (threadIdx.x == 0) {
+            int nu = 0, nb = 0, v = u;
+            while (v < units && nu < kPassUnits) {
+                const int b = v / (rows * CU), r = v - b * (rows * CU);
+                const int S = it.split_base[b + 1] - it.split_base[b];
+                if ((nb + S) * (kBlk + 4) > kTabOff) break;
+                tab[nu] = PassUnit{b, r / CU, r % CU, S, nb};
+                nb += S;
+                ++nu;
+                v += gridDim.x;
+            }
+            hdr[0] = nu;
+            hdr[1] = nb;
+            hdr[2] = v;
+            if (nu > 0) mbar_arrive_expect_tx(sbar, (uint32_t)(nb * kBlk));
+        }
+        __syncthreads();
+        const int nu = hdr[0], nb = hdr[1], next = hdr[2];
+        if (nu == 0) {
+            // more splits than the stage holds: from L2, a warp per 16 columns
+            const int b = u / (rows * CU), r = u - b * (rows * CU), row = r / CU;
+            if (warp < 8)
+                warp_merge_cols<4, 10>(p.ml, p.acc, (size_t)it.split_base[b],
+                                       it.split_base[b + 1] - it.split_base[b], rows, row, kDv,
+                                       (r % CU) * 32 + warp * 4, out_row_ptr(p.fused, b, rows, row, kDv),
+                                       p.fused.out_dtype);
+            __syncthreads(); // the header is read before it is rewritten
+            u += gridDim.x;
+            continue;
+        }
+        // block j of the pass: split j - off of the unit it falls in
+        for (int j = threadIdx.x; j < nb; j += kThreads) {
+            int k = 0;
+            while (k + 1 < nu && tab[k + 1].off <= j) ++k;
+            const PassUnit t = tab[k];
+            const float *src = p.acc +
+                               (((size_t)it.split_base[t.b] + (j - t.off)) * rows + t.row) * kDv +
+                               t.z * 128;
+            bulk_load_g2s(sm + (size_t)j * kBlk, src, kBlk, sbar);
+        }
+        float *wts = reinterpret_cast<float *>(sm + (size_t)nb * kBlk);
+        if (warp < nu) {
+            const PassUnit t = tab[warp];
+            const float2 *ml = p.ml + (size_t)it.split_base[t.b] * rows + t.row;
+            constexpr int WB = 4; // pairs per lane in flight at once: 128 splits per round trip
+            float2 x[WB];
+            float M = kNeutralM, L = 0.f;
+            for (int s0 = 0; s0 < t.S; s0 += 32 * WB) {
+#pragma unroll
+                for (int i = 0; i < WB; ++i) {
+                    const int s = s0 + 32 * i + lane;
+                    x[i] = s < t.S ? __ldcg(ml + (size_t)s * rows) : make_float2(kNeutralM, 0.f);
+                }
+#pragma unroll
+                for (int i = 0; i < WB; ++i) {
+                    if (x[i].y > 0.f) {
+                        const float mn = fmaxf(M, x[i].x);
+                        L = L * ex2((M - mn) * kLog2e) + x[i].y * ex2((x[i].x - mn) * kLog2e);
+                        M = mn;
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+                const float Lo = __shfl_xor_sync(0xffffffffu, L, o);
+                const float mn = fmaxf(M, Mo);
+                L = L * ex2((M - mn) * kLog2e) + Lo * ex2((Mo - mn) * kLog2e);
+                M = mn;
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            if (t.S <= 32 * WB) { // the pairs are still in registers
+#pragma unroll
+                for (int i = 0; i < WB; ++i) {
+                    const int s = 32 * i + lane;
+                    if (s < t.S)
+                        wts[t.off + s] = x[i].y > 0.f ? ex2((x[i].x - M) * kLog2e) * inv : 0.f;
+                }
+            } else {
+                for (int s = lane; s < t.S; s += 32) {
+                    const float2 y = __ldcg(ml + (size_t)s * rows);
+                    wts[t.off + s] = y.y > 0.f ? ex2((y.x - M) * kLog2e) * inv : 0.f;
+                }
+            }
+        }
+        if (threadIdx.x == 0) {
+            const bool ok = mbar_wait_bounded(sbar, phase, p.timeout_ns, &never);
+            if (!ok) {
+                atomicCAS(p.status, 0, kStatusTimeoutMla);
+                // copies still in flight land before the CTA's memory is released
+                (void)mbar_wait_bounded(sbar, phase, p.timeout_ns, &never);
+            }
+            hdr[3] = ok ? 1 : 0;
+        }
+        __syncthreads(); // also publishes the weights
+        if (!hdr[3]) break;
+        (void)mbar_wait_bounded(sbar, phase, p.timeout_ns, &never); // complete: this thread's view
+        phase ^= 1u;
+        {
+            // warp w sums unit w % nu over the splits w / nu, w / nu + G, ...
+            const int k = warp % nu, g = warp / nu, G = (kNW - 1 - k) / nu + 1;
+            const PassUnit t = tab[k];
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int s = g; s < t.S; s += G) {
+                const float w = wts[t.off + s];
+                const float4 v = reinterpret_cast<const float4 *>(sm + (size_t)(t.off + s) * kBlk)[lane];
+                if (w > 0.f) fma4(a, w, v);
+            }
+            red[warp * 32 + lane] = a;
+        }
+        __syncthreads();
+        if (warp < nu) {
+            const PassUnit t = tab[warp];
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int w = warp; w < kNW; w += nu) {
+                const float4 v = red[w * 32 + lane];
+                o.x += v.x;
+                o.y += v.y;
+                o.z += v.z;
+                o.w += v.w;
+            }
+            unsigned char *dst = static_cast<unsigned char *>(out_row_ptr(p.fused, t.b, rows, t.row, kDv));
+            const int col = t.z * 128 + lane * 4;
+            switch (p.fused.out_dtype) {
+            case DA_F32: store4<float>(reinterpret_cast<float *>(dst) + col, o); break;
+            case DA_F16: store4<__half>(reinterpret_cast<__half *>(dst) + col, o); break;
+            default: store4<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(dst) + col, o); break;
+            }
+        }
+        if (next >= units) break;
+        // the stage, the table and the sums are rewritten by the next pass
+        fence_proxy_async_smem();
+        __syncthreads();
+        u = next;
     }
 }
 
@@ -742,7 +907,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *go = ok && *reinterpret_cast<volatile int *>(p.status) == 0;
         }
         __syncthreads();
-        if (*go) mla_merge_units(p);
+        if (*go) mla_merge_staged(p, sm);
     }
     if (threadIdx.x == 0) griddep_launch_dependents();
 }

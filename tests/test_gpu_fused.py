@@ -2,9 +2,10 @@
 kernel merges its own partials (no combine launch), against the oracle.
 
 The GQA kernels count the arrivals of each (sequence, KV head) group's
-partials; the last one to arrive merges the group. The MLA tensor-core kernel
-counts the arrivals of all its CTAs and then merges shares of the rows on every
-CTA. The library zeroes the counters on the stream before each such launch, so
+partials, and every CTA, after its own arrivals, waits for its items' groups
+and merges a share of each. The MLA tensor-core kernel counts the arrivals of
+all its CTAs; then every CTA stages its share of the rows in shared memory and
+merges it. The library zeroes the counters on the stream before each such launch, so
 a poisoned workspace, a workspace shared by calls of other shapes and a CUDA
 graph replay all start from zero. Each case is checked against the oracle in
 both forms (one launch, and the default two launches) with the same bars as
@@ -74,6 +75,19 @@ def test_one_launch_mla_full_context_sampled():
     assert worst <= TOL["f32"], (worst, rel)
 
 
+@pytest.mark.parametrize("heads,splits", [(128, 0), (96, 300), (32, 0), (64, 7)])
+def test_one_launch_mla_staged_passes(heads, splits):
+    # each CTA stages its (row, 128 columns) units in shared memory: with 128
+    # heads a CTA's units take two passes; with 300 splits one unit outgrows
+    # the stage and is merged from L2 instead; the workspace is poisoned, so a
+    # neutral partial's unwritten acc would show
+    case = mla_case([20000], heads=heads, seed=8600 + heads + splits)
+    got, da = run(case, flags=N.DA_FLAG_ONE_LAUNCH, force_splits=splits, poison_ws=True)
+    worst, rel = errors(case, got, oracle_rows(case))
+    assert np.all(np.isfinite(got))
+    assert worst <= TOL["f32"], (heads, splits, worst, rel)
+
+
 @pytest.mark.parametrize("kind", ["gqa", "mla"])
 def test_one_launch_replayed_from_a_cuda_graph(kind):
     # a graph replays the counter reset and the launch together, so every
@@ -131,17 +145,20 @@ def test_one_launch_workspace_shared_by_calls_of_other_shapes():
         assert worst <= TOL["f16"], (worst, rel)
 
 
-def test_one_launch_plan_wider_than_the_gpu_falls_back_to_the_combine():
+@pytest.mark.parametrize("kind", ["simt", "tc"])
+def test_one_launch_plan_wider_than_the_gpu_falls_back_to_the_combine(kind):
     # a plan made for more SMs than the device has gives a grid that is not
-    # resident at once: the SIMT kernel then leaves the merge to the combine
+    # resident at once: the GQA kernels then leave the merge to the combine
     # launch, and the result still matches the oracle
-    case = W.make_case("t", batch=2, n_heads=16, n_kv_heads=4, head_dim=256,
-                       seq_lens=[30000, 9000], kv_dtype="f16", scale=1 / 16, seed=8500)
+    hq, hkv, dt = (16, 4, "f16") if kind == "simt" else (32, 2, "f16")
+    case = W.make_case("t", batch=2, n_heads=hq, n_kv_heads=hkv, head_dim=256,
+                       seq_lens=[30000, 9000], kv_dtype=dt, scale=1 / 16, seed=8500)
     q, k, v = to_device(case)
     a = A.make_args(q, k, v, case.scale, flags=N.DA_FLAG_ONE_LAUNCH)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     p = A.decode_attn_plan(a, case.seq_lens.tolist(), num_sms=4 * sms)
-    assert p.kernel == N.DA_KERNEL_GQA_TMA and p.grid > sms
+    want = N.DA_KERNEL_GQA_TMA if kind == "simt" else N.DA_KERNEL_GQA_TC
+    assert p.kernel == want and p.grid > sms
     ws = A.new_workspace(p)
     ws.fill_(0xFF)
     out = torch.full((case.batch, case.n_heads, case.v_dim), float("nan"), device="cuda")
