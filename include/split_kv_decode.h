@@ -93,8 +93,10 @@ typedef enum {
                                     the launch is not sharing the SMs with kernels
                                     of other streams; if it is, they may run out
                                     (DA_ETIMEOUT in the status word). Measured on
-                                    GB300 within -1.5 to +2 us of the default two
-                                    launches, so it is an option, not the default */
+                                    GB300 slower than the default two launches on
+                                    every benchmarked workload (by 1 to 8 us on
+                                    one sequence, more on batches), so it is an
+                                    option, not the default                        */
 #define DA_FLAG_COMBINE_LOADS 0x40 /* the combine kernel reads the partials with
                                     plain loads instead of staging them in shared
                                     memory by bulk copies (kept for comparison;

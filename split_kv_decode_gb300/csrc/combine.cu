@@ -161,46 +161,70 @@ __global__ void __launch_bounds__(kCombineThreads)
 // right after griddepcontrol.wait, so the CTA waits for one round trip.
 constexpr int kStagedMaxSplits = 256;
 
+// [max_splits blocks of 512 B][max_splits weights][8 x 32 float4 sums][mbarrier, flag]
+struct Stage {
+    unsigned char *blk;
+    float *wts;
+    float4 *red;
+    uint64_t *bar;
+    volatile int *flag;
+};
+
+__host__ __device__ constexpr int staged_wts_bytes(int max_splits)
+{
+    return (max_splits * 4 + 15) / 16 * 16;
+}
+
 int combine_staged_smem_bytes(int max_splits)
 {
-    // blocks [S][512 B] | weights [S] | per-warp sums [8][32] float4 | mbarrier, flag
-    return max_splits * (kCombineCols * 4 + 4) + ((max_splits * 4) % 16 ? 16 - (max_splits * 4) % 16 : 0) +
+    return max_splits * kCombineCols * 4 + staged_wts_bytes(max_splits) +
            kCombineWarps * 32 * 16 + 16;
 }
 
-template <typename OT>
-__global__ void __launch_bounds__(kCombineThreads)
-    combine_staged_kernel(const __grid_constant__ CombineParams p, int max_splits)
+__device__ __forceinline__ Stage stage_at(unsigned char *base, int max_splits)
 {
-    extern __shared__ __align__(128) unsigned char dsm[];
+    Stage st;
+    st.blk = base;
+    st.wts = reinterpret_cast<float *>(base + (size_t)max_splits * kCombineCols * 4);
+    st.red = reinterpret_cast<float4 *>(base + (size_t)max_splits * kCombineCols * 4 +
+                                        staged_wts_bytes(max_splits));
+    st.bar = reinterpret_cast<uint64_t *>(reinterpret_cast<unsigned char *>(st.red) +
+                                          kCombineWarps * 32 * 16);
+    st.flag = reinterpret_cast<volatile int *>(st.bar + 1);
+    return st;
+}
+
+// Thread 0 sets the stage's mbarrier up; the caller syncs the block before use.
+__device__ __forceinline__ void stage_init(const Stage &st)
+{
+    if (threadIdx.x == 0) {
+        mbar_init(st.bar, 1);
+        fence_mbar_init();
+    }
+}
+
+// The merge of row h of sequence b over the 128 columns of block z, after
+// griddepcontrol.wait. Warp 0 gets the normalised result of its lane's four
+// columns; *ok (the same in every thread) is false when the wait for the
+// blocks ran out (recorded in the status word; the result is then zero), as
+// it does when `load` is false (a test hook: no copy is issued). Every thread
+// of the block calls it; it ends with a block barrier.
+__device__ __forceinline__ float4 staged_merge(const CombineParams &p, int h, int b, int z,
+                                               const Stage &st, bool load, bool *ok)
+{
     constexpr int BLK = kCombineCols * 4;
-    const int h = blockIdx.x, b = blockIdx.y, z = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.n_splits[b];
     const size_t slot0 = (size_t)p.split_base[b];
-    const int wts_bytes = (max_splits * 4 + 15) / 16 * 16;
-    float *wts = reinterpret_cast<float *>(dsm + (size_t)max_splits * BLK);
-    float4 *red = reinterpret_cast<float4 *>(dsm + (size_t)max_splits * BLK + wts_bytes);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(dsm + (size_t)max_splits * BLK + wts_bytes +
-                                                 kCombineWarps * 32 * 16);
-    volatile int *ok_flag = reinterpret_cast<volatile int *>(bar + 1);
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    griddep_wait();
     fence_proxy_async_global(); // the split kernel's partials, for the bulk copies
 
-    const bool load = !(p.flags & DA_FLAG_TEST_NO_TMA);
-    if (threadIdx.x == 0 && load) mbar_arrive_expect_tx(bar, (uint32_t)(S * BLK));
+    if (threadIdx.x == 0 && load) mbar_arrive_expect_tx(st.bar, (uint32_t)(S * BLK));
     __syncthreads(); // the expected bytes are set before any copy completes
     if (load)
         for (int s = threadIdx.x; s < S; s += kCombineThreads)
-            bulk_load_g2s(dsm + (size_t)s * BLK,
+            bulk_load_g2s(st.blk + (size_t)s * BLK,
                           p.acc + ((slot0 + s) * p.n_heads + h) * p.v_dim + z * kCombineCols, BLK,
-                          bar);
+                          st.bar);
     if (warp == 0) {
         // m = max_i m_i, l = sum_i e^{m_i - m} l_i: the lanes merge their splits
         // online (all pairs of up to 128 splits in flight at once), then pairwise
@@ -236,54 +260,75 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
             for (int i = 0; i < WB; ++i) {
                 const int s = 32 * i + lane;
-                if (s < S) wts[s] = x[i].y > 0.f ? ex2((x[i].x - M) * kLog2e) * inv : 0.f;
+                if (s < S) st.wts[s] = x[i].y > 0.f ? ex2((x[i].x - M) * kLog2e) * inv : 0.f;
             }
         } else {
             for (int s = lane; s < S; s += 32) {
                 const float2 y = __ldg(ml + (size_t)s * p.n_heads);
-                wts[s] = y.y > 0.f ? ex2((y.x - M) * kLog2e) * inv : 0.f;
+                st.wts[s] = y.y > 0.f ? ex2((y.x - M) * kLog2e) * inv : 0.f;
             }
         }
     }
     if (threadIdx.x == 0) {
         // a wait that runs out (or copies never requested, the test hook)
-        // leaves this CTA's columns unwritten and records the timeout
+        // leaves this CTA's result zero and records the timeout
         volatile int never = 0;
-        bool ok = load && mbar_wait_bounded(bar, 0, p.timeout_ns, &never);
-        if (!ok) {
+        const bool done = load && mbar_wait_bounded(st.bar, 0, p.timeout_ns, &never);
+        if (!done) {
             atomicCAS(p.status, 0, kStatusTimeoutCombine);
             // copies still in flight land before the CTA's memory is released
-            if (load) (void)mbar_wait_bounded(bar, 0, p.timeout_ns, &never);
+            if (load) (void)mbar_wait_bounded(st.bar, 0, p.timeout_ns, &never);
         }
-        *ok_flag = ok ? 1 : 0;
+        *st.flag = done ? 1 : 0;
     }
     __syncthreads(); // also publishes the weights
-    if (!*ok_flag) return;
-    {
-        volatile int never = 0;
-        (void)mbar_wait_bounded(bar, 0, p.timeout_ns, &never); // complete: this thread's view
-    }
+    *ok = *st.flag != 0;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (*ok) {
+        volatile int never = 0;
+        (void)mbar_wait_bounded(st.bar, 0, p.timeout_ns, &never); // complete: this thread's view
 #pragma unroll 4
-    for (int s = warp; s < S; s += kCombineWarps) {
-        const float w = wts[s];
-        const float4 v = reinterpret_cast<const float4 *>(dsm + (size_t)s * BLK)[lane];
-        if (w > 0.f) fma4(a, w, v);
+        for (int s = warp; s < S; s += kCombineWarps) {
+            const float w = st.wts[s];
+            const float4 v = reinterpret_cast<const float4 *>(st.blk + (size_t)s * BLK)[lane];
+            if (w > 0.f) fma4(a, w, v);
+        }
     }
-    red[warp * 32 + lane] = a;
+    st.red[warp * 32 + lane] = a;
     __syncthreads();
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == 0) {
-        float4 t = red[lane];
+        t = st.red[lane];
 #pragma unroll
         for (int w = 1; w < kCombineWarps; ++w) {
-            const float4 u = red[w * 32 + lane];
+            const float4 u = st.red[w * 32 + lane];
             t.x += u.x;
             t.y += u.y;
             t.z += u.z;
             t.w += u.w;
         }
-        OT *out = reinterpret_cast<OT *>(p.out) + ((size_t)b * p.n_heads + h) * p.v_dim +
-                  z * kCombineCols + lane * 4;
+    }
+    __syncthreads(); // the stage may be reused
+    return t;
+}
+
+template <typename OT>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_staged_kernel(const __grid_constant__ CombineParams p, int max_splits)
+{
+    extern __shared__ __align__(128) unsigned char dsm[];
+    const Stage st = stage_at(dsm, max_splits);
+    stage_init(st);
+    __syncthreads();
+
+    griddep_wait();
+
+    bool ok;
+    const float4 t = staged_merge(p, blockIdx.x, blockIdx.y, blockIdx.z, st,
+                                  !(p.flags & DA_FLAG_TEST_NO_TMA), &ok);
+    if (ok && threadIdx.x < 32) {
+        OT *out = reinterpret_cast<OT *>(p.out) + ((size_t)blockIdx.y * p.n_heads + blockIdx.x) * p.v_dim +
+                  blockIdx.z * kCombineCols + threadIdx.x * 4;
         store4<OT>(out, t);
     }
 }

@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int items = 0, gt = 0;
         // After an item's partial is written: the four warps publish their
         // writes, then one arrival on the item's (sequence, KV head) group.
-        auto arrive_merge = [&](int b, int kvh) {
+        auto arrive_group = [&](int b, int kvh) {
             __threadfence();
             named_bar_sync(1, 128);
             if (threadIdx.x == 0) (void)arrive(p.fused.ctr + (size_t)b * p.items.n_kv_heads + kvh);
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const size_t wrow = slot_id * p.n_heads + (size_t)kvh * Gh + row_off;
             if (p1 <= p0) { // an empty item: a neutral partial, no MMA took part
                 if (owner) p.ml[wrow] = make_float2(kNeutralM, 0.f);
-                if (p.fused.on) arrive_merge(b, kvh);
+                if (p.fused.on) arrive_group(b, kvh);
                 continue;
             }
             // ---- Q of this item's rows, once the previous item's QK is done with Q
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar + TB_OFREE);
             if (owner) p.ml[wrow] = make_float2(l > 0.f ? m * kLn2 : kNeutralM, l);
-            if (p.fused.on) arrive_merge(b, kvh);
+            if (p.fused.on) arrive_group(b, kvh);
         }
         if (ab && threadIdx.x == 0 && !*abort_flag) {
             *abort_flag = 1;
