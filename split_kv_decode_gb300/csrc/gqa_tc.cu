@@ -450,26 +450,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (tc_bar_or(!okw)) break;
                 qfp ^= 1u;
             }
-            if (r < L.rpad) {
-                const float *qr =
-                    p.q + ((size_t)(b * p.q_len + token) * p.hq + (size_t)kvh * Gh + g) * D;
+            // the item's q rows [rpad][D], scaled and rounded to the cache type, in
+            // the swizzled layout (rows past R zero): the four warps take 8-column
+            // units, four per thread in flight, so q arrives in one round trip
+            {
+                constexpr int U8 = D / 8; // 8-column units of a row
+                const int units = L.rpad * U8;
+                const float sc = p.scale_log2;
+                for (int u0 = threadIdx.x; u0 < units; u0 += 4 * 128) {
+                    float4 qa[4], qb[4];
 #pragma unroll
-                for (int c = 0; c < NCH; ++c)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint32_t w4[4] = {0u, 0u, 0u, 0u};
-                        if (owner) {
-                            const float4 a = __ldg(reinterpret_cast<const float4 *>(qr + c * 64 + j * 8));
-                            const float4 bq =
-                                __ldg(reinterpret_cast<const float4 *>(qr + c * 64 + j * 8 + 4));
-                            const float sc = p.scale_log2;
-                            w4[0] = pack2<DT>(a.x * sc, a.y * sc);
-                            w4[1] = pack2<DT>(a.z * sc, a.w * sc);
-                            w4[2] = pack2<DT>(bq.x * sc, bq.y * sc);
-                            w4[3] = pack2<DT>(bq.z * sc, bq.w * sc);
+                    for (int i = 0; i < 4; ++i) {
+                        const int u = u0 + i * 128, rr = u / U8;
+                        qa[i] = qb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (u < units && rr < R) {
+                            const int tk = rr / Gh;
+                            const float *qr = p.q +
+                                              ((size_t)(b * p.q_len + tk) * p.hq +
+                                               (size_t)kvh * Gh + (rr - tk * Gh)) * D +
+                                              (u - rr * U8) * 8;
+                            qa[i] = __ldg(reinterpret_cast<const float4 *>(qr));
+                            qb[i] = __ldg(reinterpret_cast<const float4 *>(qr + 4));
                         }
-                        sts_v4(sb + L.q_off + c * L.qch + tsw(r, j * 16), w4[0], w4[1], w4[2], w4[3]);
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int u = u0 + i * 128;
+                        if (u < units) {
+                            const int rr = u / U8, j8 = u - rr * U8;
+                            sts_v4(sb + L.q_off + (j8 >> 3) * L.qch + tsw(rr, (j8 & 7) * 16),
+                                   pack2<DT>(qa[i].x * sc, qa[i].y * sc),
+                                   pack2<DT>(qa[i].z * sc, qa[i].w * sc),
+                                   pack2<DT>(qb[i].x * sc, qb[i].y * sc),
+                                   pack2<DT>(qb[i].z * sc, qb[i].w * sc));
+                        }
+                    }
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
