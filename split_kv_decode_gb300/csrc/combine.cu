@@ -175,23 +175,34 @@ __host__ __device__ constexpr int staged_wts_bytes(int max_splits)
     return (max_splits * 4 + 15) / 16 * 16;
 }
 
-int combine_staged_smem_bytes(int max_splits)
+// bytes of the blocks, weights and sums (the mbarrier and flag apart)
+__host__ __device__ constexpr int staged_area_bytes(int max_splits)
 {
-    return max_splits * kCombineCols * 4 + staged_wts_bytes(max_splits) +
-           kCombineWarps * 32 * 16 + 16;
+    return max_splits * kCombineCols * 4 + staged_wts_bytes(max_splits) + kCombineWarps * 32 * 16;
 }
 
-__device__ __forceinline__ Stage stage_at(unsigned char *base, int max_splits)
+int combine_staged_smem_bytes(int max_splits)
+{
+    return staged_area_bytes(max_splits) + 16;
+}
+
+// the blocks, weights and sums at base; the mbarrier and the flag at bar
+__device__ __forceinline__ Stage stage_in(unsigned char *base, int max_splits, uint64_t *bar)
 {
     Stage st;
     st.blk = base;
     st.wts = reinterpret_cast<float *>(base + (size_t)max_splits * kCombineCols * 4);
     st.red = reinterpret_cast<float4 *>(base + (size_t)max_splits * kCombineCols * 4 +
                                         staged_wts_bytes(max_splits));
-    st.bar = reinterpret_cast<uint64_t *>(reinterpret_cast<unsigned char *>(st.red) +
-                                          kCombineWarps * 32 * 16);
-    st.flag = reinterpret_cast<volatile int *>(st.bar + 1);
+    st.bar = bar;
+    st.flag = reinterpret_cast<volatile int *>(bar + 1);
     return st;
+}
+
+__device__ __forceinline__ Stage stage_at(unsigned char *base, int max_splits)
+{
+    return stage_in(base, max_splits,
+                    reinterpret_cast<uint64_t *>(base + staged_area_bytes(max_splits)));
 }
 
 // Thread 0 sets the stage's mbarrier up; the caller syncs the block before use.
@@ -341,12 +352,15 @@ __global__ void __launch_bounds__(kCombineThreads)
 // write-up: the output projection moves into the combine).
 //
 // A cluster of Z = ceil(v_dim / 128) CTAs serves one (row, sequence); CTA z
-// merges the columns [128 z, 128 z + 128) as the plain combine does, projects
-// them with its slice W[h][:][128 z ...] (held in shared memory) into out_dim
+// merges the columns [128 z, 128 z + 128) as the combine does, projects them
+// with its slice W[h][:][128 z ...] (held in shared memory) into out_dim
 // partial sums, and the cluster adds the Z partial vectors through distributed
-// shared memory in a fixed order (bit-reproducible). The weight slice is
-// fetched with bulk copies before griddepcontrol.wait, so its load overlaps the
-// tail of the split kernel.
+// shared memory in a fixed order (bit-reproducible). Where the combine stages
+// the partials (one rank, whole 128-column blocks), the slice shares their
+// shared memory: its rows are asked into L2 as the CTA starts and copied in by
+// bulk copies once the merge is done, so the CTA holds max(slice, stage)
+// rather than both. Otherwise the slice is copied in before
+// griddepcontrol.wait and the partials are read with plain loads.
 template <typename WT> struct WLoad;
 template <> struct WLoad<float> {
     static __device__ __forceinline__ float4 get(const unsigned char *row, int c)
@@ -363,51 +377,78 @@ template <> struct WLoad<__nv_bfloat16> {
     }
 };
 
-int combine_proj_smem_bytes(int w_dtype, int out_dim)
+// [region: the W slice [out_dim][128], or the staged partials, whichever is
+// larger][partial outputs [out_dim]][slice mbarrier | stage mbarrier, flag]
+__host__ __device__ constexpr int proj_region_bytes(int es, int out_dim, int max_splits)
+{
+    return ((out_dim * kCombineCols * es > staged_area_bytes(max_splits)
+                 ? out_dim * kCombineCols * es
+                 : staged_area_bytes(max_splits)) + 15) / 16 * 16;
+}
+
+int combine_proj_smem_bytes(int w_dtype, int out_dim, int max_splits)
 {
     const int es = w_dtype == DA_BF16 ? 2 : 4;
-    // W slice [out_dim][128] | partial outputs [out_dim] | mbarrier
-    return out_dim * kCombineCols * es + ((out_dim * 4 + 15) / 16) * 16 + 16;
+    return proj_region_bytes(es, out_dim, max_splits) + ((out_dim * 4 + 15) / 16) * 16 + 32;
 }
 
 template <typename OT, typename WT>
 __global__ void __launch_bounds__(kCombineThreads)
-    combine_proj_kernel(const __grid_constant__ CombineParams p)
+    combine_proj_kernel(const __grid_constant__ CombineParams p, int max_splits)
 {
     __shared__ __align__(16) float4 part[kCombineWarps][32];
     __shared__ __align__(16) float merged[kCombineCols];
     extern __shared__ __align__(128) unsigned char dsm[];
     constexpr int ES = sizeof(WT);
+    const int rb = proj_region_bytes(ES, p.out_dim, max_splits);
     unsigned char *wsl = dsm;                                           // [out_dim][128] WT
-    float *po = reinterpret_cast<float *>(dsm + p.out_dim * kCombineCols * ES);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(
-        dsm + p.out_dim * kCombineCols * ES + ((p.out_dim * 4 + 15) / 16) * 16);
+    float *po = reinterpret_cast<float *>(dsm + rb);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(dsm + rb + ((p.out_dim * 4 + 15) / 16) * 16);
+    const bool staged = max_splits > 0;
+    const Stage st = stage_in(dsm, max_splits, bar + 1);
 
     const int h = blockIdx.x, b = blockIdx.y, z = blockIdx.z, Z = gridDim.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = z * kCombineCols;
     const int ncols = min(kCombineCols, p.v_dim - c0);
     const uint32_t row_bytes = (uint32_t)(ncols * ES);
+    const bool load_w = !(p.flags & DA_FLAG_TEST_NO_TMA);
+    const unsigned char *w0 = static_cast<const unsigned char *>(p.w) +
+                              ((size_t)(h % p.w_heads) * p.w_head_stride + c0) * ES;
+    auto copy_slice = [&]() {
+        if (threadIdx.x == 0 && load_w) mbar_arrive_expect_tx(bar, row_bytes * p.out_dim);
+        if (load_w)
+            for (int e = threadIdx.x; e < p.out_dim; e += kCombineThreads)
+                bulk_load_g2s(wsl + (size_t)e * kCombineCols * ES,
+                              w0 + (size_t)e * p.w_row_stride * ES, row_bytes, bar);
+    };
 
-    // the weight slice of this CTA: out_dim rows of ncols elements
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
+        if (staged) stage_init(st);
         fence_mbar_init();
     }
     __syncthreads();
-    const bool load_w = !(p.flags & DA_FLAG_TEST_NO_TMA);
-    if (threadIdx.x == 0 && load_w) mbar_arrive_expect_tx(bar, row_bytes * p.out_dim);
-    if (load_w) {
-        const unsigned char *w0 = static_cast<const unsigned char *>(p.w) +
-                                  ((size_t)(h % p.w_heads) * p.w_head_stride + c0) * ES;
+    if (!staged) {
+        copy_slice();
+    } else if (load_w) {
         for (int e = threadIdx.x; e < p.out_dim; e += kCombineThreads)
-            bulk_load_g2s(wsl + (size_t)e * kCombineCols * ES,
-                          w0 + (size_t)e * p.w_row_stride * ES, row_bytes, bar);
+            bulk_prefetch_l2(w0 + (size_t)e * p.w_row_stride * ES, row_bytes);
     }
 
     griddep_wait();
 
-    const float4 t = merge_columns(p, h, b, z, part);
+    float4 t;
+    if (staged) {
+        bool ok; // a timed-out wait leaves t zero and is recorded; the cluster still meets below
+        t = staged_merge(p, h, b, z, st, true, &ok);
+        // the staged blocks are read; the slice's bulk copies may overwrite them
+        fence_proxy_async_smem();
+        __syncthreads();
+        copy_slice();
+    } else {
+        t = merge_columns(p, h, b, z, part);
+    }
     if (warp == 0) reinterpret_cast<float4 *>(merged)[lane] = t; // zeros past v_dim
     __syncthreads();
 
@@ -504,8 +545,15 @@ template <typename OT, typename WT>
 cudaError_t launch_proj_t(const CombineParams &p, int grid_x, int grid_y, cudaStream_t stream,
                           bool pdl)
 {
+    // the partials staged (sharing the slice's shared memory) for one rank's
+    // partials in whole 128-column blocks
+    int max_splits = 0;
+    for (int b = 0; b < p.batch; ++b) max_splits = p.n_splits[b] > max_splits ? p.n_splits[b] : max_splits;
+    if (!(p.n_ranks == 1 && p.v_dim % kCombineCols == 0 && max_splits <= kStagedMaxSplits &&
+          !(p.flags & DA_FLAG_COMBINE_LOADS)))
+        max_splits = 0;
     const int smem = combine_proj_smem_bytes(std::is_same<WT, float>::value ? DA_F32 : DA_BF16,
-                                             p.out_dim);
+                                             p.out_dim, max_splits);
     cudaError_t e = cudaFuncSetAttribute(combine_proj_kernel<OT, WT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -524,7 +572,7 @@ cudaError_t launch_proj_t(const CombineParams &p, int grid_x, int grid_y, cudaSt
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, combine_proj_kernel<OT, WT>, p);
+    return cudaLaunchKernelEx(&cfg, combine_proj_kernel<OT, WT>, p, max_splits);
 }
 
 cudaError_t launch_combine_proj(int out_dtype, int w_dtype, const CombineParams &p, int grid_x,
