@@ -161,6 +161,13 @@ __global__ void __launch_bounds__(kCombineThreads)
 // right after griddepcontrol.wait, so the CTA waits for one round trip.
 constexpr int kStagedMaxSplits = 256;
 
+// asks for `bytes` (multiple of 16, address 16-byte aligned) of global memory
+// to be brought into L2, without waiting for them
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // [max_splits blocks of 512 B][max_splits weights][8 x 32 float4 sums][mbarrier, flag]
 struct Stage {
     unsigned char *blk;
@@ -181,7 +188,7 @@ __host__ __device__ constexpr int staged_area_bytes(int max_splits)
     return max_splits * kCombineCols * 4 + staged_wts_bytes(max_splits) + kCombineWarps * 32 * 16;
 }
 
-int combine_staged_smem_bytes(int max_splits)
+static int combine_staged_smem_bytes(int max_splits)
 {
     return staged_area_bytes(max_splits) + 16;
 }
@@ -386,7 +393,7 @@ __host__ __device__ constexpr int proj_region_bytes(int es, int out_dim, int max
                  : staged_area_bytes(max_splits)) + 15) / 16 * 16;
 }
 
-int combine_proj_smem_bytes(int w_dtype, int out_dim, int max_splits)
+static int combine_proj_smem_bytes(int w_dtype, int out_dim, int max_splits)
 {
     const int es = w_dtype == DA_BF16 ? 2 : 4;
     return proj_region_bytes(es, out_dim, max_splits) + ((out_dim * 4 + 15) / 16) * 16 + 32;

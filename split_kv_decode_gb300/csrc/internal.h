@@ -263,7 +263,6 @@ cudaError_t launch_combine(int out_dtype, int v_dim, const CombineParams &p, int
 // 128) CTAs (at most 8), each merging 128 columns and projecting them
 constexpr int kProjMaxOut = 256;
 constexpr int kProjMaxVdim = 1024;
-int combine_proj_smem_bytes(int w_dtype, int out_dim, int max_splits);
 cudaError_t launch_combine_proj(int out_dtype, int w_dtype, const CombineParams &p, int grid_x,
                                 int grid_y, cudaStream_t stream, bool pdl);
 

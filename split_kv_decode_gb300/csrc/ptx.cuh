@@ -226,13 +226,6 @@ __device__ __forceinline__ void bulk_load_g2s(void *dst, const void *src, uint32
                  : "memory");
 }
 
-// asks for `bytes` (multiple of 16, address 16-byte aligned) of global memory
-// to be brought into L2, without waiting for them
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
