@@ -161,14 +161,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 // right after griddepcontrol.wait, so the CTA waits for one round trip.
 constexpr int kStagedMaxSplits = 256;
 
-// asks for `bytes` (multiple of 16, address 16-byte aligned) of global memory
-// to be brought into L2, without waiting for them
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// [max_splits blocks of 512 B][max_splits weights][8 x 32 float4 sums][mbarrier, flag]
+// A stage: [max_splits blocks of 512 B][max_splits weights][8 x 32 float4
+// sums], and an mbarrier and a flag (right after it, or elsewhere)
 struct Stage {
     unsigned char *blk;
     float *wts;
@@ -368,6 +362,13 @@ __global__ void __launch_bounds__(kCombineThreads)
 // bulk copies once the merge is done, so the CTA holds max(slice, stage)
 // rather than both. Otherwise the slice is copied in before
 // griddepcontrol.wait and the partials are read with plain loads.
+// asks for `bytes` (multiple of 16, address 16-byte aligned) of global memory
+// to be brought into L2, without waiting for them
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 template <typename WT> struct WLoad;
 template <> struct WLoad<float> {
     static __device__ __forceinline__ float4 get(const unsigned char *row, int c)
