@@ -67,6 +67,17 @@ def test_one_launch_with_forced_splits(splits):
     assert worst <= TOL["f32"], (splits, worst, rel)
 
 
+@pytest.mark.parametrize("splits", [1, 100])
+def test_one_launch_tensor_cores_with_forced_splits(splits):
+    # the shares of a group merge 100 splits in two batches of 64 per lane group
+    case = W.make_case("t", batch=2, n_heads=32, n_kv_heads=2, head_dim=128,
+                       seq_lens=[20000, 3000], kv_dtype="bf16", seed=8210)
+    got, da = run(case, force_splits=splits, flags=N.DA_FLAG_ONE_LAUNCH, poison_ws=True)
+    assert da.plan.kernel == N.DA_KERNEL_GQA_TC
+    worst, rel = errors(case, got, oracle_rows(case))
+    assert worst <= TOL["bf16"], (splits, worst, rel)
+
+
 def test_one_launch_mla_full_context_sampled():
     case = W.named("mla_96")
     got, da = run(case, flags=N.DA_FLAG_ONE_LAUNCH)
