@@ -677,14 +677,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                // no sleep between polls: the thread issues as soon as a product is
+                // ready (a 32 ns sleep here cost 2 us per launch)
                 if (progress) {
                     last = global_ns();
-                } else {
-                    if (*abort_flag || global_ns() - last > p.timeout_ns) {
-                        ok = false;
-                        break;
-                    }
-                    __nanosleep(32);
+                } else if (*abort_flag || global_ns() - last > p.timeout_ns) {
+                    ok = false;
+                    break;
                 }
             }
             if (!ok) raise_abort(abort_flag, abort_peer, p.status);
